@@ -1,0 +1,222 @@
+/*
+ * attn_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of exact attention with explicit masks.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg may load
+ * this code; the product path never calls it and shares no code with it.
+ *
+ * What it computes, row by row (no tiling, no fusion, no online softmax):
+ *
+ *   s_ij  = scale * sum_t q_it k_jt                for j in A(i)
+ *   M_i   = max_{j in A(i)} s_ij
+ *   l_i   = sum_{j in A(i)} exp(s_ij - M_i)
+ *   o_i   = sum_{j in A(i)} exp(s_ij - M_i) v_j / l_i
+ *   lse_i = M_i + ln l_i
+ *
+ * Sources:
+ *   - "Fused Self Attention" (NKI tutorial), section "Background": S = Q K^T,
+ *     R = softmax(S) V over (seqlen, d_head) operands.
+ *   - "Profiling in PyTorch" part 3, section "Deconstructing Naive Attention":
+ *     scores are multiplied by scale = 1/sqrt(head_dim), masked positions are
+ *     filled with -inf, a row softmax follows, then the product with v.
+ *   - NATTEN issue #142 ("circular windowed attention"): a query attends the
+ *     keys between its window start and window end; in wrap mode the window
+ *     wraps around the borders like a circularly padded convolution, and the
+ *     worked example (5x5 grid, kernel 3) gives every query exactly 9 keys.
+ *     The forward returns a float32 logsumexp of shape q.shape[:-1]; here it
+ *     is the natural log of sum_{j in A(i)} exp(s_ij).
+ *
+ * Allowed sets A(i) (mask_kind):
+ *   0 NONE   : every key j < Nk.
+ *   1 CAUSAL : j <= i (top-left alignment, as is_causal=True).
+ *   2 NA2D   : tokens are laid out row-major on a grid_h x grid_w grid;
+ *              query (qy, qx), key (ky, kx); the key is allowed iff both axes
+ *              are allowed by the one-axis rule below (window k odd, dilation).
+ *     clamp (wrap = 0): the window keeps its full size k and is shifted inward
+ *              at the borders. With dilation delta, keys share the query's
+ *              residue modulo delta, and the dilation-1 rule is applied to the
+ *              index inside that residue class.
+ *     wrap  (wrap = 1): the keys are (q + delta*t) mod G for t in [-k/2, k/2].
+ *   A row whose allowed set is empty gets o = 0 and lse = -inf (the
+ *   NaN-guarding convention of a "safe" softmax).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_MASK_NONE 0
+#define ORACLE_MASK_CAUSAL 1
+#define ORACLE_MASK_NA2D 2
+
+typedef struct {
+  int Nq, Nk, d;
+  double scale;
+  int mask_kind, window, dilation, wrap, grid_h, grid_w;
+} problem_t;
+
+/* One axis of the clamped neighbourhood: is key coordinate kc in the window of
+ * query coordinate qc on an axis of length G?  Window size k (odd), dilation dl. */
+static int axis_allowed_clamp(int qc, int kc, int G, int k, int dl) {
+  int residue = qc % dl;
+  if (kc % dl != residue) return 0;
+  /* number of grid positions that share this residue */
+  int len = (G - residue + dl - 1) / dl;
+  int a = qc / dl;     /* query index inside its residue class */
+  int b = kc / dl;     /* key index inside the same class       */
+  int start = a - k / 2;
+  if (start < 0) start = 0;
+  if (start > len - k) start = len - k;
+  return b >= start && b < start + k;
+}
+
+/* One axis of the circular ("wrap") neighbourhood. */
+static int axis_allowed_wrap(int qc, int kc, int G, int k, int dl) {
+  int half = k / 2;
+  for (int t = -half; t <= half; ++t) {
+    int c = qc + dl * t;
+    c %= G;
+    if (c < 0) c += G;
+    if (c == kc) return 1;
+  }
+  return 0;
+}
+
+static int allowed(const problem_t* p, int i, int j) {
+  switch (p->mask_kind) {
+    case ORACLE_MASK_NONE:
+      return 1;
+    case ORACLE_MASK_CAUSAL:
+      return j <= i;
+    case ORACLE_MASK_NA2D: {
+      int qy = i / p->grid_w, qx = i % p->grid_w;
+      int ky = j / p->grid_w, kx = j % p->grid_w;
+      if (p->wrap)
+        return axis_allowed_wrap(qy, ky, p->grid_h, p->window, p->dilation) &&
+               axis_allowed_wrap(qx, kx, p->grid_w, p->window, p->dilation);
+      return axis_allowed_clamp(qy, ky, p->grid_h, p->window, p->dilation) &&
+             axis_allowed_clamp(qx, kx, p->grid_w, p->window, p->dilation);
+    }
+    default:
+      return 0;
+  }
+}
+
+/* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
+static int check_args(const problem_t* p, int B, int H) {
+  if (B < 1 || H < 1 || p->Nq < 1 || p->Nk < 1 || p->d < 1) return -1;
+  if (p->mask_kind < 0 || p->mask_kind > 2) return -1;
+  if (p->mask_kind == ORACLE_MASK_NA2D) {
+    if (p->grid_h < 1 || p->grid_w < 1) return -1;
+    if (p->grid_h * p->grid_w != p->Nq || p->Nq != p->Nk) return -1;
+    if (p->window < 1 || p->window % 2 == 0 || p->dilation < 1) return -1;
+    if (p->window * p->dilation > p->grid_h || p->window * p->dilation > p->grid_w) return -1;
+  }
+  return 0;
+}
+
+/* One output row: flat row index r in [0, B*H*Nq).  scores: scratch of Nk. */
+static void one_row(const problem_t* p, const double* q, const double* k,
+                    const double* v, int64_t r, double* o_row, double* lse_out,
+                    double* scores, unsigned char* ok) {
+  const int Nq = p->Nq, Nk = p->Nk, d = p->d;
+  const int64_t bh = r / Nq;
+  const int i = (int)(r % Nq);
+  const double* qi = q + r * d;
+  const double* kb = k + bh * (int64_t)Nk * d;
+  const double* vb = v + bh * (int64_t)Nk * d;
+
+  double M = -INFINITY;
+  int any = 0;
+  for (int j = 0; j < Nk; ++j) {
+    ok[j] = (unsigned char)allowed(p, i, j);
+    if (!ok[j]) continue;
+    const double* kj = kb + (int64_t)j * d;
+    double dot = 0.0;
+    for (int t = 0; t < d; ++t) dot += qi[t] * kj[t];
+    scores[j] = p->scale * dot;
+    if (!any || scores[j] > M) M = scores[j];
+    any = 1;
+  }
+  for (int t = 0; t < d; ++t) o_row[t] = 0.0;
+  if (!any) {
+    *lse_out = -INFINITY;
+    return;
+  }
+  double l = 0.0;
+  for (int j = 0; j < Nk; ++j) {
+    if (!ok[j]) continue;
+    double w = exp(scores[j] - M);
+    l += w;
+    const double* vj = vb + (int64_t)j * d;
+    for (int t = 0; t < d; ++t) o_row[t] += w * vj[t];
+  }
+  for (int t = 0; t < d; ++t) o_row[t] /= l;
+  *lse_out = M + log(l);
+}
+
+/*
+ * q: [B,H,Nq,d], k,v: [B,H,Nk,d], all fp64 contiguous.
+ * rows == NULL: every row; o is [B,H,Nq,d], lse is [B,H,Nq].
+ * rows != NULL: nrows flat row indices in [0, B*H*Nq); o is [nrows,d], lse [nrows].
+ * nthreads <= 0 leaves the OpenMP default.
+ */
+int oracle_attn_rows(const double* q, const double* k, const double* v,
+                     double* o, double* lse, int B, int H, int Nq, int Nk, int d,
+                     double scale, int mask_kind, int window, int dilation,
+                     int wrap, int grid_h, int grid_w, const int64_t* rows,
+                     int64_t nrows, int nthreads) {
+  problem_t p = {Nq, Nk, d, scale, mask_kind, window, dilation, wrap, grid_h, grid_w};
+  if (check_args(&p, B, H) != 0) return -1;
+  const int64_t total = (int64_t)B * H * Nq;
+  const int64_t n = rows ? nrows : total;
+  if (rows) {
+    for (int64_t x = 0; x < n; ++x)
+      if (rows[x] < 0 || rows[x] >= total) return -1;
+  }
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* scores = (double*)malloc(sizeof(double) * (size_t)Nk);
+    unsigned char* ok = (unsigned char*)malloc((size_t)Nk);
+    if (!scores || !ok) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 16)
+      for (int64_t x = 0; x < n; ++x) {
+        int64_t r = rows ? rows[x] : x;
+        one_row(&p, q, k, v, r, o + x * d, lse + x, scores, ok);
+      }
+    }
+    free(scores);
+    free(ok);
+  }
+  return failed ? -2 : 0;
+}
+
+/* Number of threads the OpenMP runtime will use (for reporting). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* The allowed-set predicate itself, exposed so tests can inspect masks. */
+int oracle_allowed(int i, int j, int Nq, int Nk, int mask_kind, int window,
+                   int dilation, int wrap, int grid_h, int grid_w) {
+  problem_t p = {Nq, Nk, 1, 1.0, mask_kind, window, dilation, wrap, grid_h, grid_w};
+  if (check_args(&p, 1, 1) != 0) return -1;
+  if (i < 0 || i >= Nq || j < 0 || j >= Nk) return -1;
+  return allowed(&p, i, j);
+}

@@ -1,0 +1,161 @@
+"""ctypes front end of the fp64 C oracle -- TEST INFRASTRUCTURE ONLY.
+
+Builds ``liboracle.so`` from ``attn_oracle.c`` with gcc (OpenMP) on first use
+and evaluates exact attention row by row in fp64. See ``attn_oracle.c`` for the
+definition and its sources.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_NA2D = 2
+MASK_CODES = {"none": MASK_NONE, "causal": MASK_CAUSAL, "clamp": MASK_NA2D, "wrap": MASK_NA2D}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def compile_oracle(src: str, out: str) -> str:
+    """gcc -O2 -fopenmp, portable flags (no -march), into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE):
+        return _LIB
+    return compile_oracle(SOURCE, _LIB)
+
+
+def _dptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _grid(mask_kind, Nq, grid):
+    if mask_kind != MASK_NA2D:
+        return 0, 0
+    if grid is None:
+        g = int(round(Nq ** 0.5))
+        if g * g != Nq:
+            raise ValueError("NA2D without explicit grid needs a square token count")
+        return g, g
+    return int(grid[0]), int(grid[1])
+
+
+class Oracle:
+    """One loaded copy of the oracle library (the default one, or a test build)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.oracle_attn_rows.restype = ctypes.c_int
+        lib.oracle_attn_rows.argtypes = [
+            dp, dp, dp, dp, dp,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int,
+            ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int,
+        ]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_allowed.restype = ctypes.c_int
+        lib.oracle_allowed.argtypes = [ctypes.c_int] * 10
+        self._lib = lib
+        self.path = path
+
+    def attention_rows(self, q, k, v, rows=None, *, scale, mask_kind=MASK_NONE, window=0,
+                       dilation=1, wrap=False, grid=None, nthreads=0):
+        """Exact attention in fp64 for the given flat rows of [B, H, Nq].
+
+        q: [B, H, Nq, d]; k, v: [B, H, Nk, d] (anything numpy reads as float64).
+        rows: None for every row, else flat indices b*H*Nq + h*Nq + i.
+        Returns (o, lse): o [B,H,Nq,d] / lse [B,H,Nq] for rows=None, else
+        o [len(rows), d] / lse [len(rows)].
+        """
+        if isinstance(mask_kind, str):
+            wrap = wrap or mask_kind == "wrap"
+            mask_kind = MASK_CODES[mask_kind]
+        q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
+        k = np.ascontiguousarray(np.asarray(k, dtype=np.float64))
+        v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
+        B, H, Nq, d = q.shape
+        Nk = k.shape[2]
+        assert k.shape == (B, H, Nk, d) and v.shape == (B, H, Nk, d)
+        gh, gw = _grid(mask_kind, Nq, grid)
+        if rows is None:
+            o = np.empty((B, H, Nq, d), dtype=np.float64)
+            lse = np.empty((B, H, Nq), dtype=np.float64)
+            rp, n = None, 0
+        else:
+            rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+            n = rows.size
+            o = np.empty((n, d), dtype=np.float64)
+            lse = np.empty((n,), dtype=np.float64)
+            rp = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+        rc = self._lib.oracle_attn_rows(
+            _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
+            B, H, Nq, Nk, d, float(scale), int(mask_kind), int(window), int(dilation),
+            int(bool(wrap)), gh, gw, rp, n, int(nthreads),
+        )
+        if rc != 0:
+            raise ValueError(f"oracle rejected the problem (code {rc})")
+        return o, lse
+
+    def attention(self, q, k, v, **kw):
+        """Every row; see attention_rows."""
+        return self.attention_rows(q, k, v, None, **kw)
+
+    def allowed(self, i, j, *, Nq, Nk, mask_kind, window=0, dilation=1, wrap=False, grid=None):
+        """The oracle's allowed-set predicate for one (query, key) pair."""
+        if isinstance(mask_kind, str):
+            wrap = wrap or mask_kind == "wrap"
+            mask_kind = MASK_CODES[mask_kind]
+        gh, gw = _grid(mask_kind, Nq, grid)
+        r = self._lib.oracle_allowed(int(i), int(j), int(Nq), int(Nk), int(mask_kind),
+                                     int(window), int(dilation), int(bool(wrap)), gh, gw)
+        if r < 0:
+            raise ValueError("bad arguments")
+        return bool(r)
+
+    def max_threads(self) -> int:
+        return int(self._lib.oracle_max_threads())
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default
+
+
+def attention_rows(*a, **kw):
+    return default().attention_rows(*a, **kw)
+
+
+def attention(*a, **kw):
+    return default().attention(*a, **kw)
+
+
+def allowed(*a, **kw):
+    return default().allowed(*a, **kw)
+
+
+def max_threads() -> int:
+    return default().max_threads()

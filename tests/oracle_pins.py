@@ -1,0 +1,305 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+Each check takes an ``Oracle`` instance and raises AssertionError on failure,
+so the same checks run against the shipped oracle (test_oracle_pins.py) and
+against copies with a planted mistake (test_oracle_mutants.py), which must
+each fail at least one of them.
+
+What pins what:
+  golden_wrap_example     NATTEN issue #142 worked example (values printed on the page)
+  golden_clamp_by_hand    the shifted-window reading, spelled out by hand on 5x5/k=3
+  window_sets_by_hand     literal key sets of a few queries (clamp, wrap, dilation 2)
+  constant_v              a convex combination of equal rows returns that row
+  zero_qk_means           Q=K=0: the mean of V over the allowed set, LSE = ln |A(i)|
+  single_key              N=1: o = v_0, lse = scale q.k
+  numpy_twin              independent dense numpy statement on tiny shapes
+  sdpa_fp64               torch scaled_dot_product_attention (math) in fp64, none/causal/mask
+  invariants              key shift, linearity in V, key permutation, causal prefix
+  wrap_equals_pad_clamp   circular pad + clamped NA + crop == wrap NA (issue #142's recipe)
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from oracle import reference_np as twin
+
+RNG = np.random.default_rng(1234)
+
+
+def _rand(*shape, rng=None):
+    rng = rng or RNG
+    return rng.standard_normal(shape)
+
+
+def golden_wrap_example(orc, printed):
+    q = np.ones((1, 1, 25, 8))
+    k = np.ones((1, 1, 25, 8))
+    v = np.zeros((1, 1, 25, 8))
+    v[0, 0, 0, :] = 1.0
+    o, lse = orc.attention(q, k, v, scale=1 / math.sqrt(8), mask_kind="wrap", window=3)
+    x = o[0, 0, :, 0].reshape(5, 5)
+    assert np.array_equal(np.round(x, 4), np.asarray(printed)), x
+    exact = np.where(np.asarray(printed) > 0, 1.0 / 9.0, 0.0)
+    assert np.max(np.abs(x - exact)) < 1e-15
+    # every query sees exactly 9 keys of score 8/sqrt(8)
+    assert np.allclose(lse, math.sqrt(8) + math.log(9), atol=1e-13, rtol=0)
+
+
+def golden_clamp_by_hand(orc, expected):
+    q = np.ones((1, 1, 25, 8))
+    k = np.ones((1, 1, 25, 8))
+    v = np.zeros((1, 1, 25, 8))
+    v[0, 0, 0, :] = 1.0
+    o, _ = orc.attention(q, k, v, scale=1 / math.sqrt(8), mask_kind="clamp", window=3)
+    x = o[0, 0, :, 0].reshape(5, 5)
+    assert np.max(np.abs(x - np.asarray(expected))) < 1e-15, x
+
+
+def window_sets_by_hand(orc):
+    def keys(i, mask, window, grid, dilation=1):
+        n = grid[0] * grid[1]
+        return {j for j in range(n)
+                if orc.allowed(i, j, Nq=n, Nk=n, mask_kind=mask, window=window,
+                               dilation=dilation, grid=grid)}
+
+    def tok(y, x, w):
+        return y * w + x
+
+    g = (5, 5)
+    # clamp, k=3: corner (0,0) -> rows {0,1,2} x cols {0,1,2}; (4,4) -> {2,3,4}^2; (2,1) -> {1,2,3} x {0,1,2}
+    assert keys(tok(0, 0, 5), "clamp", 3, g) == {tok(y, x, 5) for y in (0, 1, 2) for x in (0, 1, 2)}
+    assert keys(tok(4, 4, 5), "clamp", 3, g) == {tok(y, x, 5) for y in (2, 3, 4) for x in (2, 3, 4)}
+    assert keys(tok(2, 1, 5), "clamp", 3, g) == {tok(y, x, 5) for y in (1, 2, 3) for x in (0, 1, 2)}
+    # wrap, k=3: corner (0,0) -> rows {4,0,1} x cols {4,0,1}
+    assert keys(tok(0, 0, 5), "wrap", 3, g) == {tok(y, x, 5) for y in (4, 0, 1) for x in (4, 0, 1)}
+    # rectangular grid 3 x 7, clamp k=3 at (0,6): rows {0,1,2} x cols {4,5,6}
+    assert keys(tok(0, 6, 7), "clamp", 3, (3, 7)) == {tok(y, x, 7) for y in (0, 1, 2) for x in (4, 5, 6)}
+    # dilation 2 on an 8 x 8 grid, k=3, clamp: query (1,6) -> rows with residue 1: 1,3,5
+    # (1 is the first member, so the window starts there) x cols with residue 0: 2,4,6
+    # (6 is the last member of {0,2,4,6}, window pushed inward to {2,4,6})
+    assert keys(tok(1, 6, 8), "clamp", 3, (8, 8), 2) == {tok(y, x, 8) for y in (1, 3, 5) for x in (2, 4, 6)}
+    # dilation 2, wrap, 8 x 8, k=3: query (0,0) -> {6,0,2} x {6,0,2}
+    assert keys(tok(0, 0, 8), "wrap", 3, (8, 8), 2) == {tok(y, x, 8) for y in (6, 0, 2) for x in (6, 0, 2)}
+
+
+CASES = [
+    dict(mask_kind="none", Nq=37, Nk=37),
+    dict(mask_kind="none", Nq=19, Nk=41),
+    dict(mask_kind="causal", Nq=37, Nk=37),
+    dict(mask_kind="causal", Nq=41, Nk=23),
+    dict(mask_kind="clamp", Nq=49, Nk=49, window=3, grid=(7, 7)),
+    dict(mask_kind="wrap", Nq=49, Nk=49, window=5, grid=(7, 7)),
+    dict(mask_kind="clamp", Nq=48, Nk=48, window=3, grid=(6, 8)),
+    dict(mask_kind="wrap", Nq=48, Nk=48, window=3, grid=(6, 8)),
+    dict(mask_kind="clamp", Nq=64, Nk=64, window=3, grid=(8, 8), dilation=2),
+    dict(mask_kind="wrap", Nq=64, Nk=64, window=3, grid=(8, 8), dilation=2),
+]
+
+
+def _kw(case):
+    kw = dict(mask_kind=case["mask_kind"])
+    for name in ("window", "grid", "dilation"):
+        if name in case:
+            kw[name] = case[name]
+    return kw
+
+
+def _twin_mask(case):
+    return twin.mask_matrix(case["Nq"], case["Nk"], case["mask_kind"], case.get("window", 0),
+                            case.get("dilation", 1), case.get("grid"))
+
+
+def constant_v(orc):
+    rng = np.random.default_rng(7)
+    for case in CASES:
+        Nq, Nk, d = case["Nq"], case["Nk"], 6
+        q = _rand(2, 1, Nq, d, rng=rng)
+        k = _rand(2, 1, Nk, d, rng=rng)
+        c = rng.standard_normal(d)
+        v = np.broadcast_to(c, (2, 1, Nk, d)).copy()
+        o, _ = orc.attention(q, k, v, scale=0.7, **_kw(case))
+        assert np.max(np.abs(o - c)) < 1e-13, case
+
+
+def zero_qk_means(orc):
+    rng = np.random.default_rng(8)
+    for case in CASES:
+        Nq, Nk, d = case["Nq"], case["Nk"], 5
+        q = np.zeros((1, 1, Nq, d))
+        k = np.zeros((1, 1, Nk, d))
+        v = _rand(1, 1, Nk, d, rng=rng)
+        o, lse = orc.attention(q, k, v, scale=1.3, **_kw(case))
+        m = case["mask_kind"]
+        if m == "none":
+            exp_o = np.broadcast_to(v[0, 0].mean(axis=0), (Nq, d))
+            exp_n = np.full(Nq, Nk)
+        elif m == "causal":
+            cnt = np.minimum(np.arange(Nq) + 1, Nk)
+            csum = np.cumsum(v[0, 0], axis=0)
+            exp_o = csum[cnt - 1] / cnt[:, None]
+            exp_n = cnt
+        else:
+            kk = case["window"]
+            exp_n = np.full(Nq, kk * kk)        # every query sees a full k x k window
+            allowed = _twin_mask(case)
+            exp_o = np.stack([v[0, 0][allowed[i]].mean(axis=0) for i in range(Nq)])
+        assert np.max(np.abs(o[0, 0] - exp_o)) < 1e-13, case
+        assert np.max(np.abs(lse[0, 0] - np.log(exp_n))) < 1e-13, case
+
+
+def single_key(orc):
+    rng = np.random.default_rng(9)
+    q = _rand(1, 2, 1, 8, rng=rng)
+    k = _rand(1, 2, 1, 8, rng=rng)
+    v = _rand(1, 2, 1, 8, rng=rng)
+    for mask in ("none", "causal"):
+        o, lse = orc.attention(q, k, v, scale=0.37, mask_kind=mask)
+        assert np.max(np.abs(o - v)) < 1e-15
+        exp = 0.37 * np.einsum("bhid,bhid->bhi", q, k)
+        assert np.max(np.abs(lse - exp)) < 1e-14
+
+
+def numpy_twin(orc):
+    rng = np.random.default_rng(10)
+    for case in CASES:
+        for d in (1, 4, 8):
+            Nq, Nk = case["Nq"], case["Nk"]
+            q = _rand(1, 2, Nq, d, rng=rng)
+            k = _rand(1, 2, Nk, d, rng=rng)
+            v = _rand(1, 2, Nk, d, rng=rng)
+            scale = 0.5 / math.sqrt(d)
+            o, lse = orc.attention(q, k, v, scale=scale, **_kw(case))
+            allowed = _twin_mask(case)
+            for h in range(2):
+                to, tl = twin.attention(q[0, h], k[0, h], v[0, h], scale, allowed)
+                assert np.max(np.abs(o[0, h] - to)) < 1e-12, (case, d)
+                assert np.max(np.abs(lse[0, h] - tl)) < 1e-12, (case, d)
+
+
+def sdpa_fp64(orc):
+    import torch
+    import torch.nn.functional as F
+
+    rng = np.random.default_rng(11)
+    for case in CASES:
+        Nq, Nk, d = case["Nq"], case["Nk"], 8
+        q = _rand(2, 3, Nq, d, rng=rng)
+        k = _rand(2, 3, Nk, d, rng=rng)
+        v = _rand(2, 3, Nk, d, rng=rng)
+        scale = 1 / math.sqrt(d)
+        o, _ = orc.attention(q, k, v, scale=scale, **_kw(case))
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        m = case["mask_kind"]
+        if m == "none":
+            ref = F.scaled_dot_product_attention(tq, tk, tv, scale=scale)
+        elif m == "causal":
+            # explicit top-left lower-triangular boolean mask (True = attend)
+            tri = torch.ones(Nq, Nk, dtype=torch.bool).tril()
+            ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=tri, scale=scale)
+        else:
+            am = torch.from_numpy(_twin_mask(case))
+            ref = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=am, scale=scale)
+        assert np.max(np.abs(o - ref.numpy())) < 1e-12, case
+
+
+def invariants(orc):
+    rng = np.random.default_rng(12)
+    d = 6
+    for case in CASES:
+        Nq, Nk = case["Nq"], case["Nk"]
+        kw = _kw(case)
+        q = _rand(1, 1, Nq, d, rng=rng)
+        k = _rand(1, 1, Nk, d, rng=rng)
+        v = _rand(1, 1, Nk, d, rng=rng)
+        v2 = _rand(1, 1, Nk, d, rng=rng)
+        s = 0.8
+        o, lse = orc.attention(q, k, v, scale=s, **kw)
+        # shifting every key by u leaves o alone and shifts lse_i by s * q_i . u
+        u = rng.standard_normal(d)
+        o_u, lse_u = orc.attention(q, k + u, v, scale=s, **kw)
+        assert np.max(np.abs(o_u - o)) < 1e-12, case
+        assert np.max(np.abs(lse_u - lse - s * (q[0, 0] @ u))) < 1e-12, case
+        # linear in V
+        o2, _ = orc.attention(q, k, v2, scale=s, **kw)
+        o3, _ = orc.attention(q, k, 2.0 * v - 3.0 * v2, scale=s, **kw)
+        assert np.max(np.abs(o3 - (2.0 * o - 3.0 * o2))) < 1e-12, case
+    # NONE is invariant under a joint permutation of the keys and values
+    Nq, Nk = 17, 29
+    q = _rand(1, 1, Nq, d, rng=rng)
+    k = _rand(1, 1, Nk, d, rng=rng)
+    v = _rand(1, 1, Nk, d, rng=rng)
+    perm = rng.permutation(Nk)
+    o, lse = orc.attention(q, k, v, scale=0.9, mask_kind="none")
+    op, lp = orc.attention(q, k[:, :, perm], v[:, :, perm], scale=0.9, mask_kind="none")
+    assert np.max(np.abs(op - o)) < 1e-12 and np.max(np.abs(lp - lse)) < 1e-12
+    # causal row i == unmasked attention of query i over the first i+1 keys
+    N = 23
+    q = _rand(1, 1, N, d, rng=rng)
+    k = _rand(1, 1, N, d, rng=rng)
+    v = _rand(1, 1, N, d, rng=rng)
+    oc, lc = orc.attention(q, k, v, scale=0.6, mask_kind="causal")
+    for i in (0, 1, 11, N - 1):
+        on, ln = orc.attention(q[:, :, i:i + 1], k[:, :, :i + 1], v[:, :, :i + 1], scale=0.6,
+                               mask_kind="none")
+        assert np.max(np.abs(on[0, 0, 0] - oc[0, 0, i])) < 1e-12
+        assert abs(ln[0, 0, 0] - lc[0, 0, i]) < 1e-12
+    # scale -> 0 gives the plain mean over the allowed set
+    o0, l0 = orc.attention(q, k, v, scale=0.0, mask_kind="none")
+    assert np.max(np.abs(o0[0, 0] - v[0, 0].mean(axis=0))) < 1e-13
+    assert np.max(np.abs(l0 - math.log(N))) < 1e-13
+
+
+def wrap_equals_pad_clamp(orc):
+    """Issue #142's recipe: circularly pad Q, K, V by (k//2)*dilation, run clamped
+    NA on the padded grid, crop. It must equal the wrap mode on random inputs."""
+    rng = np.random.default_rng(13)
+    for (gh, gw, win, dil) in ((7, 7, 3, 1), (6, 9, 5, 1), (9, 8, 3, 2), (5, 5, 5, 1)):
+        d = 4
+        x = [rng.standard_normal((gh, gw, d)) for _ in range(3)]
+        p = (win // 2) * dil
+        padded = [np.pad(t, ((p, p), (p, p), (0, 0)), mode="wrap") for t in x]
+        PH, PW = gh + 2 * p, gw + 2 * p
+
+        def flat(t, h, w):
+            return t.reshape(1, 1, h * w, d)
+
+        ow, lw = orc.attention(*(flat(t, gh, gw) for t in x), scale=0.7, mask_kind="wrap",
+                               window=win, dilation=dil, grid=(gh, gw))
+        oc, lc = orc.attention(*(flat(t, PH, PW) for t in padded), scale=0.7, mask_kind="clamp",
+                               window=win, dilation=dil, grid=(PH, PW))
+        oc = oc.reshape(PH, PW, d)[p:p + gh, p:p + gw].reshape(1, 1, gh * gw, d)
+        lc = lc.reshape(PH, PW)[p:p + gh, p:p + gw].reshape(1, 1, gh * gw)
+        assert np.max(np.abs(oc - ow)) < 1e-12, (gh, gw, win, dil)
+        assert np.max(np.abs(lc - lw)) < 1e-12, (gh, gw, win, dil)
+
+
+def row_subset_matches_full(orc):
+    rng = np.random.default_rng(14)
+    q = _rand(2, 2, 33, 8, rng=rng)
+    k = _rand(2, 2, 33, 8, rng=rng)
+    v = _rand(2, 2, 33, 8, rng=rng)
+    o, lse = orc.attention(q, k, v, scale=0.4, mask_kind="causal")
+    rows = np.array([0, 5, 32, 33, 70, 131])
+    os_, ls = orc.attention_rows(q, k, v, rows, scale=0.4, mask_kind="causal")
+    assert np.array_equal(os_, o.reshape(-1, 8)[rows])
+    assert np.array_equal(ls, lse.reshape(-1)[rows])
+
+
+def all_checks(goldens):
+    """(name, callable(orc)) for every check, goldens = (wrap_printed, clamp_by_hand)."""
+    wrap_printed, clamp_by_hand = goldens
+    return [
+        ("golden_wrap_example", lambda o: golden_wrap_example(o, wrap_printed)),
+        ("golden_clamp_by_hand", lambda o: golden_clamp_by_hand(o, clamp_by_hand)),
+        ("window_sets_by_hand", window_sets_by_hand),
+        ("constant_v", constant_v),
+        ("zero_qk_means", zero_qk_means),
+        ("single_key", single_key),
+        ("numpy_twin", numpy_twin),
+        ("sdpa_fp64", sdpa_fp64),
+        ("invariants", invariants),
+        ("wrap_equals_pad_clamp", wrap_equals_pad_clamp),
+        ("row_subset_matches_full", row_subset_matches_full),
+    ]

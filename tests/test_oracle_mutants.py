@@ -1,0 +1,53 @@
+"""Planted mistakes in copies of the oracle must each fail at least one pin.
+
+Each mutant is a one-line textual change to a temporary copy of the C oracle
+(the shipped source is never touched), compiled with gcc and run through the
+same checks as tests/test_oracle_pins.py. A mutant that no check catches means
+the pins leave that part of the oracle unpinned.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+from tests.helpers import read_golden
+
+GOLDENS = (read_golden("natten_issue142_wrap_5x5_k3.txt"),
+           read_golden("na2d_clamp_5x5_k3_by_hand.txt"))
+
+MUTANTS = {
+    "causal_off_by_one": ("return j <= i;", "return j < i + (i == 0);"),
+    "dropped_scale": ("scores[j] = p->scale * dot;", "scores[j] = dot;"),
+    "lse_dropped_max": ("*lse_out = M + log(l);", "*lse_out = log(l);"),
+    "v_wrong_operand": ("o_row[t] += w * vj[t];", "o_row[t] += w * qi[t % d];"),
+    "key_index_transposed": ("const double* kj = kb + (int64_t)j * d;",
+                             "const double* kj = kb + (int64_t)(j % (i + 1)) * d;"),
+    "wrap_negative_modulo": ("if (c < 0) c += G;", ""),
+    "clamp_no_upper_shift": ("if (start > len - k) start = len - k;", ""),
+    "clamp_window_off_centre": ("int start = a - k / 2;", "int start = a - k / 2 + 1;"),
+    "na_axis_swapped": ("axis_allowed_clamp(qx, kx, p->grid_w, p->window, p->dilation);",
+                        "axis_allowed_clamp(qx, kx, p->grid_h, p->window, p->dilation);"),
+    "dilation_residue_ignored": ("if (kc % dl != residue) return 0;", ""),
+    "softmax_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = src.replace(old, new)
+    path = os.path.join(tmp_path, f"mut_{name}.c")
+    with open(path, "w") as f:
+        f.write(mutated)
+    lib = oracle.compile_oracle(path, os.path.join(tmp_path, f"libmut_{name}.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for check_name, check in pins.all_checks(GOLDENS):
+        try:
+            check(orc)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(check_name)
+    assert caught, f"no pin catches the planted mistake {name}"
