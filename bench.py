@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused exact-attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one forward pass (one launch of the sm_103a kernel through the C
+ABI) over one batch of the workload; the default workload is the SD2.1 UNet
+self-attention block (B=2, H=5, N=4096, d=64, no mask), on which the metric is
+quoted. Inputs are seeded synthetic bf16 tensors already resident in HBM; the
+timed steps rotate over enough input sets that together exceed the 129 MB L2,
+so no step reads another step's inputs from L2.
+
+Metric: attention forward TFLOP/s, counting 4 * 128 * 128 * d per 128x128
+(query, key) tile of a fixed reference grid that holds at least one allowed
+pair (for no mask this is 4 * Nq * Nk * d per head); the exact count of
+allowed pairs is reported beside it.
+
+One JSON line on rank 0 with: value (whole-job TFLOP/s), roofline of the
+kernel (measured per launch with CUDA events on its stream, against the
+measured bf16 peak), e2e (the same metric with host inputs and outputs copied
+inside the timed region), cpu_baseline (the fp64 CPU oracle on a bounded
+sample), clocks sampled during the timed region.
+
+With --impl reference the line is the CPU oracle itself (the only reference
+implementation: the pages ship no code), timed on the host cores.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own instance of
+the workload (independent problems, no data-path collective); value = all
+ranks' work / the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from seeded_inputs import WORKLOADS, make_qkv  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (4·Nq·Nk·d/head) and % of GB300 bf16 tensor peak"
+DEFAULT_WORKLOAD = "sd21_unet_block"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_attention_69_gb300/csrc/attn_sm103.cuh",
+                  "exact_attention_69_gb300/csrc/tmem_ldst.inc",
+                  "exact_attention_69_gb300/csrc/attn_kernel.h"]
+
+
+# ------------------------------------------------------------------ counting
+
+def _axis_allowed(G: int, k: int, wrap: bool) -> np.ndarray:
+    c = np.arange(G)[:, None]
+    e = np.arange(G)[None, :]
+    if wrap:
+        return ((e - c + k // 2) % G) < k
+    s = np.clip(c - k // 2, 0, G - k)
+    return (e >= s) & (e < s + k)
+
+
+def allowed_pairs_matrix(w) -> np.ndarray | None:
+    """Boolean [Nq, Nk] allowed-pair matrix for masked workloads (None: no mask)."""
+    if w.mask == "none":
+        return None
+    if w.mask == "causal":
+        return np.tril(np.ones((w.Nq, w.Nk), dtype=bool))
+    gh, gw = w.grid
+    return np.kron(_axis_allowed(gh, w.window, w.mask == "wrap"),
+                   _axis_allowed(gw, w.window, w.mask == "wrap")).astype(bool)
+
+
+def count_flops(w):
+    """(tile-rule flops, exact allowed-pair flops) for the whole workload."""
+    per_pair = 4.0 * w.d * w.B * w.H
+    m = allowed_pairs_matrix(w)
+    if m is None:
+        f = per_pair * w.Nq * w.Nk
+        return f, f
+    nq, nk = -(-w.Nq // 128), -(-w.Nk // 128)
+    pad = np.zeros((nq * 128, nk * 128), dtype=bool)
+    pad[:w.Nq, :w.Nk] = m
+    tiles = pad.reshape(nq, 128, nk, 128).any(axis=(1, 3)).sum()
+    return per_pair * 128 * 128 * float(tiles), per_pair * float(m.sum())
+
+
+# ------------------------------------------------------------------ environment
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons in a background thread."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return None
+        inside = [p for (t, p) in self.samples if t0 - 0.05 <= t <= t1 + 0.05]
+        window = "timed region"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            window = "nearest sample to a timed region shorter than the 100 ms sampling period"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, target_s: float, seed_rows: int = 7):
+    """Time the fp64 oracle on a bounded row sample of workload w.
+
+    Returns (seconds, rows, total_rows, threads). Rows are spread over every
+    (batch, head); the sample size is calibrated to take about target_s."""
+    import oracle
+    from seeded_inputs import make_workload, to_f64
+    q, k, v = make_workload(w)
+    qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
+    total = w.B * w.H * w.Nq
+    rng = np.random.default_rng(seed_rows)
+    kw = dict(scale=w.scale, mask_kind=w.mask, window=w.window, grid=w.grid)
+    n = min(total, 64)
+    rows = np.sort(rng.choice(total, size=n, replace=False))
+    t = time.perf_counter()
+    oracle.attention_rows(qf, kf, vf, rows, **kw)
+    per_row = max((time.perf_counter() - t) / n, 1e-7)
+    n = int(min(total, max(64, target_s / per_row)))
+    rows = np.sort(rng.choice(total, size=n, replace=False))
+    t = time.perf_counter()
+    oracle.attention_rows(qf, kf, vf, rows, **kw)
+    dt = time.perf_counter() - t
+    return dt, n, total, oracle.max_threads()
+
+
+def reference_arm(args, w):
+    """--impl reference: the CPU oracle timed on the host cores, one bounded
+    row sample of the workload per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    flops_tile, _ = count_flops(w)
+    per_step_target = float(os.environ.get("ATTN_REF_STEP_S", "3.0"))
+    times, rows_done = [], 0
+    total_rows = w.B * w.H * w.Nq
+    threads = 1
+    for i in range(args.warmup + args.steps):
+        dt, n, total_rows, threads = oracle_sample(w, per_step_target, seed_rows=100 + i)
+        if i >= args.warmup:
+            times.append(dt)
+            rows_done += n
+    total_s = sum(times)
+    value = flops_tile * (rows_done / total_rows) / total_s / 1e12
+    sample = (f"{rows_done} of {total_rows} query rows per run over {args.steps} steps "
+              f"(~{rows_done // max(args.steps, 1)} rows/step, random rows of every head), "
+              f"fp64, {threads} OpenMP threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, rotating_sets=None),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, rotating_sets):
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+           "mask": w.mask, "scale": w.scale, "sigma": w.sigma, "seed": w.seed,
+           "flop_rule": "4*128*128*d per 128x128 reference tile holding an allowed pair"}
+    if w.mask in ("clamp", "wrap"):
+        cfg.update({"window": w.window, "grid": list(w.grid), "dilation": w.dilation})
+    if rotating_sets is not None:
+        cfg["l2"] = (f"inputs larger than L2: {rotating_sets} rotating input sets "
+                     f"(> {L2_BYTES // 2**20} MiB in total), no explicit flush")
+    return cfg
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def ours_arm(args, w):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from exact_attention_69_gb300 import build as _build
+    _build.build()
+    import exact_attention_69_gb300 as E
+
+    flops_tile, flops_exact = count_flops(w)
+    set_bytes = 2 * (2 * w.B * w.H * w.Nq * w.d + 2 * w.B * w.H * w.Nk * w.d) + 4 * w.B * w.H * w.Nq
+    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes))
+    q, k, v = make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.sigma, w.seed + 1000 * rank)
+    sets = []
+    for i in range(n_sets):
+        # distinct device buffers per set (same values): no step hits L2 from the last
+        sets.append((q.to(dev), k.to(dev), v.to(dev),
+                     torch.empty(w.B, w.H, w.Nq, w.d, dtype=torch.bfloat16, device=dev),
+                     torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device=dev)))
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(scale=w.scale, mask=w.mask, window=w.window, grid=w.grid)
+
+    def step(i, events=None):
+        qq, kk, vv, oo, ll = sets[i % n_sets]
+        E.attn_fwd(qq, kk, vv, out=oo, lse=ll, events=events, **kw)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    code, detail = E.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} {detail} after warm-up")
+
+    # per-launch kernel events (the roofline's duration) and whole-region events
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()).start() if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)  # let nvidia-smi start sampling
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, events=kev[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.summary(h0, h1) if sampler else None
+    if sampler:
+        sampler.stop()
+    code, detail = E.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} {detail} in the timed region")
+    ms_total = t_start.elapsed_time(t_stop)
+    k_ms = [a.elapsed_time(b) for a, b in kev]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * flops_tile * args.steps / (ms_total * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, host outputs back
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    qd, kd, vd, od, ld = sets[0]
+    oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
+    lh = torch.empty(ld.shape, dtype=ld.dtype, pin_memory=True)
+    e_steps = max(3, min(args.steps, 200))
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        E.attn_fwd(qd, kd, vd, out=od, lse=ld, **kw)
+        oh.copy_(od, non_blocking=True)
+        lh.copy_(ld, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    e2e = {"value": world * flops_tile * e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    k_avg_ms = sum(k_ms) / len(k_ms)
+    achieved = flops_tile / (k_avg_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)",
+                "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
+                "kernel_ms_avg": k_avg_ms, "kernel_ms_min": min(k_ms),
+                "exact_pairs_tflops": flops_exact / (k_avg_ms * 1e-3) / 1e12,
+                "hbm_gbs_compulsory": set_bytes / (k_avg_ms * 1e-3) / 1e9}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        dt, n, total, threads = oracle_sample(w, float(os.environ.get("ATTN_CPU_S", "12")))
+        cpu = {"value": flops_tile * (n / total) / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"{n} of {total} query rows (random, every head) in {dt:.1f} s, fp64"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(w, n_sets),
+        "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": args.steps, "impl": "ours",
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+    return ours_arm(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,159 @@
+"""Python entry points over libattn.so.
+
+PyTorch provides device memory and streams; the computation is one launch of
+the library's sm_103a kernel per call. Nothing here computes attention.
+
+    attn_fwd(q, k, v, ...)        q,k,v [B,H,N,d] bf16 (CUDA, or CPU tensors that
+                                  are staged to the GPU and back)
+    na2d(q, k, v, kernel_size, mode)
+                                  NATTEN's heads-last [B, X, Y, heads, d] layout,
+                                  'clamp' or 'wrap' windows (NATTEN issue #142)
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+_MASKS = {"none": _lib.ATTN_MASK_NONE, "causal": _lib.ATTN_MASK_CAUSAL,
+          "clamp": _lib.ATTN_MASK_NA2D, "wrap": _lib.ATTN_MASK_NA2D}
+
+
+def _strides(t: torch.Tensor, layout: str):
+    """Element strides (b, h, n) of a tensor viewed as [B, H, N, d]."""
+    if t.stride(-1) != 1:
+        raise ValueError("the last (head) dimension must be contiguous")
+    if layout == "bhnd":
+        sb, sh, sn, _ = t.stride()
+    else:  # heads-last [B, X, Y, H, d]: token n = x * Y + y
+        sb, sx, sy, sh, _ = t.stride()
+        if sx != sy * t.shape[2]:
+            raise ValueError("X and Y must be jointly contiguous in a heads-last layout")
+        sn = sy
+    return (sb, sh, sn)
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t.dtype != torch.bfloat16:
+            raise TypeError("q, k, v must be bfloat16")
+        if not t.is_cuda:
+            raise ValueError("expected CUDA tensors")
+
+
+def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, grid,
+            layout, num_ctas, timeout_ns, inject, events, stream):
+    p = _lib.params()
+    p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
+    p.lse = lse.data_ptr() if lse is not None else None
+    p.B, p.H, p.Nq, p.Nk, p.d = B, H, Nq, Nk, d
+    p.scale = float(scale)
+    p.mask_kind = _MASKS[mask]
+    if mask in ("clamp", "wrap"):
+        p.window = int(window)
+        p.dilation = int(dilation)
+        p.wrap = 1 if mask == "wrap" else 0
+        if grid is not None:
+            p.grid_h, p.grid_w = int(grid[0]), int(grid[1])
+    else:
+        p.window, p.dilation, p.wrap = int(window), int(dilation), 0
+    for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", o)):
+        getattr(p, name)[:] = _strides(t, layout)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    p.stream = stream.cuda_stream
+    p.num_ctas = int(num_ctas)
+    p.timeout_ns = int(timeout_ns)
+    p.inject = int(inject)
+    if events is not None:
+        p.ev_start = events[0].cuda_event
+        p.ev_stop = events[1].cuda_event
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.fwd_ex(p), "attn_fwd")
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
+             mask: str = "none", window: int = 0, dilation: int = 1, grid=None,
+             out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+             return_lse: bool = True, num_ctas: int = 0, timeout_ns: int = 0, inject: int = 0,
+             events=None, stream=None):
+    """Fused exact attention forward over [B, H, N, d] bf16 tensors.
+
+    mask: 'none' | 'causal' | 'clamp' | 'wrap' (the last two: 2-D neighbourhood
+    attention with an odd `window` over a grid_h x grid_w token grid, square
+    by default). Returns (o, lse) or o. CPU inputs are copied to the current
+    CUDA device, and the results back to the CPU (the end-to-end path).
+    """
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    if not q.is_cuda:
+        return _host_roundtrip(q, k, v, scale=scale, mask=mask, window=window,
+                               dilation=dilation, grid=grid, return_lse=return_lse)
+    _check_dev(q, k, v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None and (not lse.is_contiguous() or lse.dtype != torch.float32):
+        raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
+    _launch(q, k, v, out, lse, B=B, H=H, Nq=Nq, Nk=Nk, d=d, scale=scale, mask=mask,
+            window=window, dilation=dilation, grid=grid, layout="bhnd", num_ctas=num_ctas,
+            timeout_ns=timeout_ns, inject=inject, events=events, stream=stream)
+    return (out, lse) if return_lse else out
+
+
+def _host_roundtrip(q, k, v, *, return_lse, **kw):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = torch.cuda.current_stream(dev)
+    qd, kd, vd = (t.to(dev, non_blocking=True) for t in (q, k, v))
+    o, lse = attn_fwd(qd, kd, vd, return_lse=True, **kw)
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    o_h.copy_(o, non_blocking=True)
+    l_h.copy_(lse, non_blocking=True)
+    s.synchronize()
+    return (o_h, l_h) if return_lse else o_h
+
+
+def na2d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size: int, *,
+         mode: str = "clamp", dilation: int = 1, scale: float | None = None,
+         out: torch.Tensor | None = None, return_lse: bool = False, stream=None):
+    """2-D neighbourhood attention in NATTEN's heads-last layout [B, X, Y, heads, d].
+
+    mode 'clamp': windows keep their full kernel_size^2 and shift inward at the
+    borders; mode 'wrap': windows wrap around the borders (circular). The
+    output has the same layout; no permute or copy of the inputs is made.
+    """
+    if mode not in ("clamp", "wrap"):
+        raise ValueError("mode must be 'clamp' or 'wrap'")
+    if q.dim() != 5:
+        raise ValueError("expected [B, X, Y, heads, d] tensors")
+    _check_dev(q, k, v)
+    B, X, Y, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    lse = torch.empty((B, H, X * Y), dtype=torch.float32, device=q.device) if return_lse else None
+    _launch(q, k, v, out, lse, B=B, H=H, Nq=X * Y, Nk=X * Y, d=d, scale=scale, mask=mode,
+            window=kernel_size, dilation=dilation, grid=(X, Y), layout="bxyhd", num_ctas=0,
+            timeout_ns=0, inject=0, events=None, stream=stream)
+    return (out, lse) if return_lse else out
+
+
+def device_status():
+    """Read and clear the device status word: (code, [code, role, tile, cta])."""
+    return _lib.device_status()
+
+
+def sm_count() -> int:
+    n = _lib.load().attn_device_sm_count()
+    if n < 0:
+        _lib.check(-n, "attn_device_sm_count")
+    return n

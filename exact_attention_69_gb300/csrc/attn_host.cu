@@ -1,0 +1,361 @@
+// attn_host.cu -- the C ABI of libattn.so (declared in include/attn.h).
+//
+// Host work per call: validate the arguments (before any CUDA call), encode
+// the three TMA tensor maps, pick the kernel specialisation, launch once on
+// the caller's stream. The only device memory the library owns is one status
+// word per device, allocated on first use.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_kernel.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+thread_local cudaStream_t t_stream = nullptr;
+thread_local char t_err[512] = {0};
+
+struct DeviceState {
+  uint32_t* status = nullptr;  // 4 x u32 device status word
+  int sm_count = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t isqrt64(int64_t n) {
+  int64_t r = static_cast<int64_t>(std::sqrt(static_cast<double>(n)));
+  while (r * r > n) --r;
+  while ((r + 1) * (r + 1) <= n) ++r;
+  return r;
+}
+
+// Host-only argument checks; fills the derived grid and strides.
+struct Checked {
+  int grid_h = 0, grid_w = 0;
+  int64_t qs[3], ks[3], vs[3], os[3];
+};
+
+int check_strides(const int64_t in[3], int64_t out[3], int64_t N, int64_t H, int64_t d,
+                  const char* name) {
+  if (in[0] == 0 && in[1] == 0 && in[2] == 0) {
+    out[2] = d;
+    out[1] = N * d;
+    out[0] = H * N * d;
+    return ATTN_OK;
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (in[i] <= 0) return fail(ATTN_ERR_INVALID_ARG, "%s stride %d must be positive", name, i);
+    if (in[i] % 8 != 0)
+      return fail(ATTN_ERR_MISALIGNED, "%s stride %d (%lld elements) is not a multiple of 8", name,
+                  i, static_cast<long long>(in[i]));
+    out[i] = in[i];
+  }
+  if (out[2] < d) return fail(ATTN_ERR_INVALID_ARG, "%s row stride is smaller than d", name);
+  return ATTN_OK;
+}
+
+int validate(const attn_params_ex* p, Checked* c) {
+  if (p == nullptr) return fail(ATTN_ERR_INVALID_ARG, "null parameter block");
+  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, Nq, Nk must be >= 1 (got %d, %d, %d, %d)", p->B,
+                p->H, p->Nq, p->Nk);
+  if (p->d < 1) return fail(ATTN_ERR_INVALID_ARG, "d must be >= 1");
+  if (p->d != 32 && p->d != 64 && p->d != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head dimension %d is not one of 32, 64, 128", p->d);
+  if (!std::isfinite(p->scale) || !(p->scale > 0.f))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (p->mask_kind < ATTN_MASK_NONE || p->mask_kind > ATTN_MASK_NA2D)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", p->mask_kind);
+  const int64_t BH = static_cast<int64_t>(p->B) * p->H;
+  const int64_t n_qpairs = (static_cast<int64_t>(p->Nq) + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  if (BH * n_qpairs >= (int64_t{1} << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "too many (batch, head, query-tile) tasks");
+  if (p->mask_kind != ATTN_MASK_NA2D) {
+    if (p->window != 0 || p->dilation != 1 || p->wrap != 0 || p->grid_h != 0 || p->grid_w != 0)
+      return fail(ATTN_ERR_INVALID_ARG,
+                  "window/dilation/wrap/grid apply to NA2D only (need 0/1/0/0x0)");
+  } else {
+    if (p->wrap != 0 && p->wrap != 1) return fail(ATTN_ERR_INVALID_ARG, "wrap must be 0 or 1");
+    if (p->window < 1 || p->window % 2 == 0)
+      return fail(ATTN_ERR_INVALID_ARG, "window must be odd and >= 1 (got %d)", p->window);
+    if (p->dilation < 1) return fail(ATTN_ERR_INVALID_ARG, "dilation must be >= 1");
+    if (p->Nq != p->Nk) return fail(ATTN_ERR_INVALID_ARG, "NA2D needs Nq == Nk");
+    if (p->grid_h == 0 && p->grid_w == 0) {
+      const int64_t g = isqrt64(p->Nq);
+      if (g * g != p->Nq)
+        return fail(ATTN_ERR_INVALID_ARG, "NA2D with Nq=%d needs a square grid or grid_h/grid_w",
+                    p->Nq);
+      c->grid_h = c->grid_w = static_cast<int>(g);
+    } else {
+      if (p->grid_h < 1 || p->grid_w < 1 ||
+          static_cast<int64_t>(p->grid_h) * p->grid_w != p->Nq)
+        return fail(ATTN_ERR_INVALID_ARG, "grid %dx%d does not hold Nq=%d tokens", p->grid_h,
+                    p->grid_w, p->Nq);
+      c->grid_h = p->grid_h;
+      c->grid_w = p->grid_w;
+    }
+    const int64_t span = static_cast<int64_t>(p->window) * p->dilation;
+    if (span > c->grid_h || span > c->grid_w)
+      return fail(ATTN_ERR_INVALID_ARG, "window*dilation=%lld exceeds the grid side",
+                  static_cast<long long>(span));
+    if (p->dilation > 1)
+      return fail(ATTN_ERR_UNSUPPORTED, "NA2D dilation > 1 is not implemented on the GPU");
+  }
+  if (!p->q || !p->k || !p->v || !p->o)
+    return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
+  if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o))
+    return fail(ATTN_ERR_MISALIGNED, "q, k, v and o must be 16-byte aligned");
+  if (p->lse && (reinterpret_cast<uintptr_t>(p->lse) & 3u))
+    return fail(ATTN_ERR_MISALIGNED, "lse must be 4-byte aligned");
+  if (p->num_ctas < 0) return fail(ATTN_ERR_INVALID_ARG, "num_ctas must be >= 0");
+  if (p->inject != 0 && p->inject != 1) return fail(ATTN_ERR_INVALID_ARG, "inject must be 0 or 1");
+  int rc;
+  if ((rc = check_strides(p->q_stride, c->qs, p->Nq, p->H, p->d, "q")) != ATTN_OK) return rc;
+  if ((rc = check_strides(p->k_stride, c->ks, p->Nk, p->H, p->d, "k")) != ATTN_OK) return rc;
+  if ((rc = check_strides(p->v_stride, c->vs, p->Nk, p->H, p->d, "v")) != ATTN_OK) return rc;
+  if ((rc = check_strides(p->o_stride, c->os, p->Nq, p->H, p->d, "o")) != ATTN_OK) return rc;
+  return ATTN_OK;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return ATTN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDriverEntryPointByVersion");
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return ATTN_OK;
+}
+
+// Per-device state; creates the status word on first use.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (s.status == nullptr) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                  dev, major, minor);
+    if ((e = cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* ptr = nullptr;
+    if ((e = cudaMalloc(&ptr, 4 * sizeof(uint32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc");
+    if ((e = cudaMemset(ptr, 0, 4 * sizeof(uint32_t))) != cudaSuccess) {
+      cudaFree(ptr);
+      return cuda_fail(e, "cudaMemset");
+    }
+    s.status = static_cast<uint32_t*>(ptr);
+  }
+  *out = &s;
+  return ATTN_OK;
+}
+
+// 4-D bf16 tensor map over (d, n, h, b), box (box_cols, 128, 1, 1).
+int encode_map(CUtensorMap* m, const void* base, int d, int N, int H, int B, const int64_t st[3],
+               int box_cols, CUtensorMapSwizzle swz, const char* name) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(st[2]) * 2, static_cast<cuuint64_t>(st[1]) * 2,
+                           static_cast<cuuint64_t>(st[0]) * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(attn::kBN), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name,
+                static_cast<int>(r));
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void attn_params_init(attn_params_ex* p) {
+  if (!p) return;
+  std::memset(p, 0, sizeof(*p));
+  p->dilation = 1;
+}
+
+int attn_fwd_ex(const attn_params_ex* p) {
+  t_err[0] = 0;
+  Checked c;
+  int rc = validate(p, &c);
+  if (rc != ATTN_OK) return rc;
+  if ((rc = get_encoder()) != ATTN_OK) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+
+  attn::KernelParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  const int box_cols = p->d >= 64 ? 64 : 32;
+  const CUtensorMapSwizzle swz = p->d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if ((rc = encode_map(&kp.tm_q, p->q, p->d, p->Nq, p->H, p->B, c.qs, box_cols, swz, "q")) != ATTN_OK ||
+      (rc = encode_map(&kp.tm_k, p->k, p->d, p->Nk, p->H, p->B, c.ks, box_cols, swz, "k")) != ATTN_OK ||
+      (rc = encode_map(&kp.tm_v, p->v, p->d, p->Nk, p->H, p->B, c.vs, box_cols, swz, "v")) != ATTN_OK)
+    return rc;
+  kp.o = p->o;
+  kp.lse = p->lse;
+  kp.o_sb = c.os[0];
+  kp.o_sh = c.os[1];
+  kp.o_sn = c.os[2];
+  kp.B = p->B;
+  kp.H = p->H;
+  kp.Nq = p->Nq;
+  kp.Nk = p->Nk;
+  kp.c = p->scale * 1.4426950408889634f;
+  kp.grid_h = c.grid_h;
+  kp.grid_w = c.grid_w;
+  kp.window = p->window;
+  kp.n_qpairs = (p->Nq + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  kp.n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
+  kp.n_tasks = p->B * p->H * kp.n_qpairs;
+  kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
+  kp.inject = p->inject;
+  kp.status = ds->status;
+
+  int mask = attn::kMaskNone;
+  if (p->mask_kind == ATTN_MASK_CAUSAL) mask = attn::kMaskCausal;
+  if (p->mask_kind == ATTN_MASK_NA2D) mask = p->wrap ? attn::kMaskNaWrap : attn::kMaskNaClamp;
+
+  int grid = ds->sm_count;
+  if (p->num_ctas > 0 && p->num_ctas < grid) grid = p->num_ctas;
+  if (grid > kp.n_tasks) grid = kp.n_tasks;
+
+  cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
+  cudaError_t e;
+  if (p->ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_start), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(start)");
+  switch (p->d) {
+    case 32: e = attn::launch_d32(kp, mask, grid, s); break;
+    case 64: e = attn::launch_d64(kp, mask, grid, s); break;
+    default: e = attn::launch_d128(kp, mask, grid, s); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (p->ev_stop && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_stop), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(stop)");
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+             int Nk, int d, float scale, int mask_kind, int window, int dilation, int wrap) {
+  attn_params_ex p;
+  attn_params_init(&p);
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.d = d;
+  p.scale = scale;
+  p.mask_kind = mask_kind;
+  p.window = window;
+  p.dilation = dilation;
+  p.wrap = wrap;
+  return attn_fwd_ex(&p);
+}
+
+int attn_set_stream(void* stream) {
+  t_stream = static_cast<cudaStream_t>(stream);
+  return ATTN_OK;
+}
+
+int attn_get_device_status(uint32_t* detail) {
+  t_err[0] = 0;
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != ATTN_OK) return rc;
+  uint32_t word[4] = {0, 0, 0, 0};
+  cudaError_t e = cudaMemcpy(word, ds->status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (word[0] != 0 && (e = cudaMemset(ds->status, 0, sizeof(word))) != cudaSuccess)
+    return cuda_fail(e, "cudaMemset(status)");
+  if (detail) std::memcpy(detail, word, sizeof(word));
+  if (word[0] == 0) return ATTN_OK;
+  if (word[0] == ATTN_ERR_TIMEOUT)
+    return fail(ATTN_ERR_TIMEOUT, "device wait ran out: role %u, KV tile %d, CTA %u", word[1],
+                static_cast<int>(word[2]), word[3]);
+  return fail(ATTN_ERR_CUDA, "unexpected device status %u", word[0]);
+}
+
+const char* attn_error_string(int code) {
+  switch (code) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "misaligned pointer or stride";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status code";
+  }
+}
+
+const char* attn_last_error(void) { return t_err; }
+
+int attn_device_sm_count(void) {
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != ATTN_OK) return -rc;
+  return ds->sm_count;
+}
+
+void attn_shutdown(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < kMaxDevices; ++i) {
+    if (g_dev[i].status) {
+      int prev = 0;
+      cudaGetDevice(&prev);
+      if (cudaSetDevice(i) == cudaSuccess) cudaFree(g_dev[i].status);
+      cudaSetDevice(prev);
+      g_dev[i].status = nullptr;
+    }
+  }
+}
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+int attn_params_size(void) { return static_cast<int>(sizeof(attn_params_ex)); }
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// attn_kernel.h -- parameters shared by the host launcher and the sm_103a
+// attention kernels (one instantiation per head dimension and mask kind).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+constexpr int kBM = 128;        // query rows per Q tile: one TMEM lane and one softmax thread per row
+constexpr int kBN = 128;        // keys per K/V tile
+constexpr int kWarps = 10;      // warp 0 loader, warp 1 MMA issuer, warps 2-5 / 6-9 softmax of Q tile 0 / 1
+constexpr int kThreads = kWarps * 32;
+constexpr float kRescaleLog2 = 8.0f;  // keep a stale row maximum until the true one exceeds it by 2^8
+
+// Mask specialisations (the C-ABI's NA2D splits into clamp and wrap here).
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskNaClamp = 2, kMaskNaWrap = 3 };
+
+// Roles recorded in the device status word when a bounded wait runs out.
+enum Role : uint32_t { kRoleLoader = 0, kRoleMma = 1, kRoleSoftmax = 2 };
+
+struct KernelParams {
+  CUtensorMap tm_q;             // 4-D (d, n, h, b) bf16 maps, box (swizzle span, 128, 1, 1)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  void* o;                      // bf16 output
+  float* lse;                   // fp32 [B, H, Nq] or nullptr
+  int64_t o_sb, o_sh, o_sn;     // element strides of O for b, h, n
+  int B, H, Nq, Nk;
+  float c;                      // scale * log2(e): scores enter exp2 in log2 units
+  int grid_h, grid_w, window;   // neighbourhood masks only
+  int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head
+  int n_kv;                     // ceil(Nk / 128)
+  int n_tasks;                  // B * H * n_qpairs
+  uint64_t timeout_ns;          // bound on every mbarrier wait
+  int inject;                   // 1: loader withholds one K tile (tests the bounded wait)
+  uint32_t* status;             // device status word: code, role, tile, CTA
+};
+
+// Per-head-dimension launchers, defined in attn_fwd_d{32,64,128}.cu.
+cudaError_t launch_d32(const KernelParams& p, int mask, int grid, cudaStream_t s);
+cudaError_t launch_d64(const KernelParams& p, int mask, int grid, cudaStream_t s);
+cudaError_t launch_d128(const KernelParams& p, int mask, int grid, cudaStream_t s);
+
+}  // namespace attn

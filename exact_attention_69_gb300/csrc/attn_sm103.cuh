@@ -1,0 +1,833 @@
+// attn_sm103.cuh -- the fused exact-attention forward kernel for sm_103a.
+//
+// One CTA per SM (persistent). A task is a pair of 128-row Q tiles of one
+// (batch, head); the CTA streams the K/V tiles that the pair needs and keeps
+// the two Q tiles in flight at once, so that the tensor core works on one tile
+// while the softmax warps work on the other.
+//
+//   warp 0      loader: TMA of Q (once per task) and of K_j, V_j into
+//               multi-stage shared-memory rings (mbarrier full/empty pairs)
+//   warp 1      MMA issuer (one thread): S_h = Q_h K_j^T into TMEM
+//               (tcgen05.mma, both operands in shared memory), then
+//               O_h += P_h V_j (A operand P_h read from TMEM)
+//   warps 2-5   softmax of Q tile 0, warps 6-9 softmax of Q tile 1: one thread
+//               per query row reads its S row from TMEM, applies the mask,
+//               keeps the running maximum and row sum, writes P as bf16 back
+//               over S, rescales O when the maximum grew, and finally divides
+//               O by the row sum and stores O and the log-sum-exp.
+//
+// The method: "Fused Self Attention" (NKI tutorial) -- one strip of query rows
+// at a time ("Fusion to Save SBUF Space"), row maxima and row sums with the
+// division delayed until after the product with V ("Softmax implementation");
+// the xformers memory-efficient attention post -- K tiles read in turn with a
+// running softmax, only the end result written to memory; NATTEN issue #142
+// -- a CTA loads a Q tile, loops over the K/V tiles it needs, skips the tiles
+// that no window touches and masks the rest inside the tile.
+//
+// TMEM (512 columns, fp32 per 32-bit cell, one row per lane):
+//   [0,128)   S_0 (P_0 as packed bf16 pairs in columns [0,64))
+//   [128,256) S_1 (P_1 likewise)
+//   [256,256+D) O_0, [256+D,256+2D) O_1
+//
+// Every wait is bounded: when one runs out the kernel records the failure in
+// the device status word, raises a CTA-wide abort flag, lets every role leave
+// its loop, waits (bounded) for its own copies and MMAs in flight, frees TMEM
+// and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "attn_kernel.h"
+
+namespace attn {
+namespace dev {
+
+constexpr uint32_t kStatusTimeout = 5;  // same value as ATTN_ERR_TIMEOUT in attn.h
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
+// True once the phase of `bar` with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 4-D tiled TMA load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// --- tcgen05: tensor memory and the 5th-generation tensor core
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D (TMEM) = A (smem) * B (smem) [+ D]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (TMEM) = A (TMEM) * B (smem) [+ D]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+#include "tmem_ldst.inc"
+
+// --- arithmetic helpers (single PTX instructions)
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two floats to a bf16 pair (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ------------------------------------------------------------- descriptors
+
+// Shared-memory matrix descriptor of tcgen05.mma: start address, leading and
+// stride byte offsets (all >> 4), the fixed descriptor version bit 46, and
+// the swizzle layout code in bits 61-63 (2 = 128-byte, 4 = 64-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>(layout) << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: f32 accumulator, bf16 A
+// and B, A K-major, B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- layout
+
+template <int D>
+struct Cfg {
+  static_assert(D == 32 || D == 64 || D == 128, "head dimension");
+  // A K/V/Q tile of 128 rows x D bf16 is stored as D / kBoxCols column chunks;
+  // each chunk is 128 rows of kSwizzle bytes, swizzled the same way by TMA and
+  // by the MMA descriptor, and lands 1024-byte aligned.
+  static constexpr int kSwizzle = D >= 64 ? 128 : 64;
+  static constexpr int kBoxCols = kSwizzle / 2;
+  static constexpr int kChunks = D / kBoxCols;
+  static constexpr int kChunkBytes = kBN * kSwizzle;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kKStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
+  static constexpr int kVStages = kKStages;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kLayout = D >= 64 ? 2u : 4u;
+  static constexpr uint32_t kIdescS = make_idesc(kBM, kBN, false);
+  static constexpr uint32_t kIdescO = make_idesc(kBM, D, true);
+  static constexpr uint32_t kTmemCols = 512;
+  __host__ __device__ static constexpr uint32_t tm_s(int h) { return 128u * h; }
+  __host__ __device__ static constexpr uint32_t tm_o(int h) { return 256u + static_cast<uint32_t>(D) * h; }
+};
+
+// Barrier slots (8 bytes each) after the tiles.
+struct Bars {
+  uint32_t base;
+  int kst, vst;
+  __device__ uint32_t q_full() const { return base; }
+  __device__ uint32_t q_empty() const { return base + 8; }
+  __device__ uint32_t s_full(int h) const { return base + 16 + 8 * h; }
+  __device__ uint32_t p_full(int h) const { return base + 32 + 8 * h; }
+  __device__ uint32_t o_full(int h) const { return base + 48 + 8 * h; }
+  __device__ uint32_t o_empty(int h) const { return base + 64 + 8 * h; }
+  __device__ uint32_t done() const { return base + 80; }
+  __device__ uint32_t k_full(int s) const { return base + 88 + 8 * s; }
+  __device__ uint32_t k_empty(int s) const { return base + 88 + 8 * (kst + s); }
+  __device__ uint32_t v_full(int s) const { return base + 88 + 8 * (2 * kst + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 88 + 8 * (2 * kst + vst + s); }
+  __device__ int count() const { return 11 + 2 * kst + 2 * vst; }
+};
+
+// ------------------------------------------------------------- bounded waits
+
+struct Ctl {
+  volatile uint32_t* abort;   // CTA-wide abort flag in shared memory
+  uint32_t* status;           // device status word (4 x u32)
+  uint64_t timeout_ns;
+};
+
+static __device__ __noinline__ void report_timeout(const Ctl& c, uint32_t role, int tile) {
+  if (atomicCAS(c.status, 0u, kStatusTimeout) == 0u) {
+    c.status[1] = role;
+    c.status[2] = static_cast<uint32_t>(tile);
+    c.status[3] = blockIdx.x;
+    __threadfence();
+  }
+  *c.abort = 1u;
+}
+
+static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t role,
+                                       int tile, bool honour_abort) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test(bar, parity)) return true;
+    if (honour_abort && *c.abort) return false;
+    if ((n & 63u) == 0u) {
+      if (global_ns() - t0 > c.timeout_ns || n >= (1u << 28)) {
+        report_timeout(c, role, tile);
+        return false;
+      }
+    }
+  }
+}
+
+// Waits for the phase of parity `parity` of `bar`. False: the CTA is aborting.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& c,
+                                           uint32_t role, int tile, bool honour_abort = true) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_slow(bar, parity, c, role, tile, honour_abort);
+}
+
+// Warp-uniform wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, int tile) {
+  const int lane = threadIdx.x & 31;
+  uint32_t ok = 1;
+  if (lane == 0) ok = wait_phase(bar, parity, c, kRoleSoftmax, tile) ? 1u : 0u;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0u;
+}
+
+// ------------------------------------------------------------- work and masks
+
+struct Task {
+  int b, h, bh;
+  int q0[2];
+  bool live[2];
+};
+
+// Task t -> (batch, head, pair of Q tiles). Causal: pairs in decreasing
+// length order across all heads (longest first); otherwise head-major so that
+// CTAs working at the same time share a head's K/V in L2.
+template <int MASK>
+__host__ __device__ __forceinline__ Task decode_task(int t, const KernelParams& p) {
+  const int BH = p.B * p.H;
+  int bh, qp;
+  if (MASK == kMaskCausal) {
+    bh = t % BH;
+    qp = p.n_qpairs - 1 - t / BH;
+  } else {
+    bh = t / p.n_qpairs;
+    qp = t - bh * p.n_qpairs;
+  }
+  Task k;
+  k.bh = bh;
+  k.b = bh / p.H;
+  k.h = bh - k.b * p.H;
+  k.q0[0] = qp * 2 * kBM;
+  k.q0[1] = k.q0[0] + kBM;
+  k.live[0] = k.q0[0] < p.Nq;
+  k.live[1] = k.q0[1] < p.Nq;
+  return k;
+}
+
+// Along one axis of length G with window w: does some query coordinate in
+// [c0, c1] have a window that meets the key coordinates [e0, e1]?
+template <bool WRAP>
+__host__ __device__ __forceinline__ bool axis_meets(int c0, int c1, int e0, int e1, int G, int w) {
+  const int half = w >> 1;
+  if (!WRAP) {
+    // clamped windows start at clamp(c - w/2, 0, G - w); starts grow with c
+    const int lo = min(max(c0 - half, 0), G - w);
+    const int hi = min(max(c1 - half, 0), G - w) + w - 1;
+    return hi >= e0 && lo <= e1;
+  }
+  const int span = c1 - c0 + w;  // positions covered, counted circularly
+  if (span >= G) return true;
+  int a = c0 - half;
+  if (a < 0) a += G;
+  const int b = a + span - 1;
+  if (b < G) return b >= e0 && a <= e1;
+  return a <= e1 || b - G >= e0;  // covered: [a, G-1] and [0, b-G]
+}
+
+// Does any query in rows [q0, q1) attend any key in [k0, k1)? Exact for
+// dilation 1: the Q and K ranges are cut into their grid-row segments.
+template <bool WRAP>
+__host__ __device__ __noinline__ bool na_tile_meets(int q0, int q1, int k0, int k1, const KernelParams& p) {
+  const int W = p.grid_w;
+  const int kr0 = k0 / W, kr1 = (k1 - 1) / W;
+  for (int qa = q0; qa < q1;) {
+    const int qr = qa / W;
+    const int qb = min(q1, (qr + 1) * W);
+    if (axis_meets<WRAP>(qr, qr, kr0, kr1, p.grid_h, p.window)) {
+      for (int ka = k0; ka < k1;) {
+        const int kr = ka / W;
+        const int kb = min(k1, (kr + 1) * W);
+        if (axis_meets<WRAP>(qr, qr, kr, kr, p.grid_h, p.window) &&
+            axis_meets<WRAP>(qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W, W,
+                             p.window))
+          return true;
+        ka = kb;
+      }
+    }
+    qa = qb;
+  }
+  return false;
+}
+
+// 0: no query of the tile attends any key of KV tile j (skip it);
+// 1: every (query, key) pair is allowed (no mask); 2: mask inside the tile.
+template <int MASK>
+__host__ __device__ __forceinline__ int tile_class(int q0, int j, const KernelParams& p) {
+  const int k0 = j * kBN;
+  const bool ragged = k0 + kBN > p.Nk;
+  if (MASK == kMaskNone) return ragged ? 2 : 1;
+  const int q1 = min(q0 + kBM, p.Nq);
+  if (MASK == kMaskCausal) {
+    if (k0 > q1 - 1) return 0;
+    return (!ragged && k0 + kBN - 1 <= q0) ? 1 : 2;
+  }
+  return na_tile_meets<MASK == kMaskNaWrap>(q0, q1, k0, min(k0 + kBN, p.Nk), p) ? 2 : 0;
+}
+
+template <int MASK>
+__host__ __device__ __forceinline__ bool tile_active(const Task& tk, int h, int j, const KernelParams& p) {
+  return tk.live[h] && tile_class<MASK>(tk.q0[h], j, p) != 0;
+}
+
+// Next KV tile after j that some live Q tile of the task needs (n_kv if none).
+template <int MASK>
+__host__ __device__ __forceinline__ int next_tile(const Task& tk, int j, const KernelParams& p) {
+  for (++j; j < p.n_kv; ++j)
+    if (tile_active<MASK>(tk, 0, j, p) || tile_active<MASK>(tk, 1, j, p)) return j;
+  return p.n_kv;
+}
+
+// ---------------------------------------------------------------- roles
+
+template <int D, int MASK>
+__device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& bars,
+                            const Ctl& ctl) {
+  using C = Cfg<D>;
+  uint32_t q_it = 0, k_it = 0, v_it = 0;
+  int q_armed = -1, k_armed[C::kKStages], v_armed[C::kVStages];
+  for (int s = 0; s < C::kKStages; ++s) k_armed[s] = -1;
+  for (int s = 0; s < C::kVStages; ++s) v_armed[s] = -1;
+  bool injected = false;
+  for (int t = blockIdx.x; t < p.n_tasks; t += gridDim.x) {
+    const Task tk = decode_task<MASK>(t, p);
+    if (!wait_phase(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, kRoleLoader, -1)) goto drain;
+    mbar_expect_tx(bars.q_full(), 2 * C::kTileBytes);
+    for (int h = 0; h < 2; ++h)
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d(sbase + C::kOffQ + h * C::kTileBytes + c * C::kChunkBytes, &p.tm_q,
+                    bars.q_full(), c * C::kBoxCols, tk.q0[h], tk.h, tk.b);
+    q_armed = static_cast<int>(q_it & 1u);
+    ++q_it;
+    int nth = 0;
+    for (int j = next_tile<MASK>(tk, -1, p); j < p.n_kv; j = next_tile<MASK>(tk, j, p), ++nth) {
+      const int ks = static_cast<int>(k_it % C::kKStages);
+      if (!wait_phase(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, kRoleLoader, j))
+        goto drain;
+      if (p.inject && !injected && nth == 1) {
+        injected = true;  // withhold this K tile: the MMA issuer's wait must run out
+      } else {
+        mbar_expect_tx(bars.k_full(ks), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sbase + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &p.tm_k,
+                      bars.k_full(ks), c * C::kBoxCols, j * kBN, tk.h, tk.b);
+        k_armed[ks] = static_cast<int>((k_it / C::kKStages) & 1u);
+      }
+      ++k_it;
+      const int vs = static_cast<int>(v_it % C::kVStages);
+      if (!wait_phase(bars.v_empty(vs), ((v_it / C::kVStages) & 1u) ^ 1u, ctl, kRoleLoader, j))
+        goto drain;
+      mbar_expect_tx(bars.v_full(vs), C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d(sbase + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &p.tm_v,
+                    bars.v_full(vs), c * C::kBoxCols, j * kBN, tk.h, tk.b);
+      v_armed[vs] = static_cast<int>((v_it / C::kVStages) & 1u);
+      ++v_it;
+    }
+  }
+drain:
+  // The last copy armed on each barrier must have landed before the CTA exits.
+  if (q_armed >= 0) wait_phase(bars.q_full(), q_armed, ctl, kRoleLoader, -1, false);
+  for (int s = 0; s < C::kKStages; ++s)
+    if (k_armed[s] >= 0) wait_phase(bars.k_full(s), k_armed[s], ctl, kRoleLoader, -1, false);
+  for (int s = 0; s < C::kVStages; ++s)
+    if (v_armed[s] >= 0) wait_phase(bars.v_full(s), v_armed[s], ctl, kRoleLoader, -1, false);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem, int h, uint32_t q_tile, uint32_t k_tile) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const int chunk = (ks * 16) / C::kBoxCols;
+    const uint32_t off = chunk * C::kChunkBytes + ((ks * 16) % C::kBoxCols) * 2;
+    const uint64_t a = smem_desc(q_tile + off, 16, 8 * C::kSwizzle, C::kLayout);
+    const uint64_t b = smem_desc(k_tile + off, 16, 8 * C::kSwizzle, C::kLayout);
+    mma_ss(tmem + C::tm_s(h), a, b, C::kIdescS, ks > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, bool accumulate) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int ks = 0; ks < kBN / 16; ++ks) {
+    // V is [key, d] with d contiguous: the B operand (K = keys, N = d) is MN-major.
+    // 16 keys = 16 rows of kSwizzle bytes; column chunks are kChunkBytes apart.
+    const uint64_t b = smem_desc(v_tile + ks * 16 * C::kSwizzle, C::kChunkBytes,
+                                 8 * C::kSwizzle, C::kLayout);
+    mma_ts(tmem + C::tm_o(h), tmem + C::tm_s(h) + ks * 8, b, C::kIdescO,
+           (accumulate || ks > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, int MASK>
+__device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars, uint32_t tmem,
+                         const Ctl& ctl) {
+  using C = Cfg<D>;
+  uint32_t q_it = 0, k_it = 0, v_it = 0;
+  uint32_t p_par[2] = {0, 0}, o_it[2] = {0, 0};
+  for (int t = blockIdx.x; t < p.n_tasks; t += gridDim.x) {
+    const Task tk = decode_task<MASK>(t, p);
+    if (!wait_phase(bars.q_full(), q_it & 1u, ctl, kRoleMma, -1)) goto drain;
+    ++q_it;
+    tc_fence_after();
+    bool o_ready[2] = {false, false};
+    int j = next_tile<MASK>(tk, -1, p);
+    if (j < p.n_kv) {
+      const int ks = static_cast<int>(k_it % C::kKStages);
+      if (!wait_phase(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, kRoleMma, j)) goto drain;
+      tc_fence_after();
+      for (int h = 0; h < 2; ++h)
+        if (tile_active<MASK>(tk, h, j, p)) {
+          issue_s<D>(tmem, h, sbase + C::kOffQ + h * C::kTileBytes,
+                     sbase + C::kOffK + ks * C::kTileBytes);
+          mma_commit(bars.s_full(h));
+        }
+      mma_commit(bars.k_empty(ks));
+      ++k_it;
+    }
+    while (j < p.n_kv) {
+      const int jn = next_tile<MASK>(tk, j, p);
+      const bool has_next = jn < p.n_kv;
+      if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
+      const int vs = static_cast<int>(v_it % C::kVStages);
+      if (!wait_phase(bars.v_full(vs), (v_it / C::kVStages) & 1u, ctl, kRoleMma, j)) goto drain;
+      tc_fence_after();
+      int ksn = -1;
+      for (int h = 0; h < 2; ++h) {
+        if (tile_active<MASK>(tk, h, j, p)) {
+          if (!wait_phase(bars.p_full(h), p_par[h], ctl, kRoleMma, j)) goto drain;
+          p_par[h] ^= 1u;
+          if (!o_ready[h]) {
+            if (!wait_phase(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, kRoleMma, j)) goto drain;
+          }
+          tc_fence_after();
+          issue_pv<D>(tmem, h, sbase + C::kOffV + vs * C::kTileBytes, o_ready[h]);
+          o_ready[h] = true;
+        }
+        if (has_next && tile_active<MASK>(tk, h, jn, p)) {
+          if (ksn < 0) {
+            ksn = static_cast<int>(k_it % C::kKStages);
+            if (!wait_phase(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, kRoleMma, jn))
+              goto drain;
+            tc_fence_after();
+          }
+          issue_s<D>(tmem, h, sbase + C::kOffQ + h * C::kTileBytes,
+                     sbase + C::kOffK + ksn * C::kTileBytes);
+          mma_commit(bars.s_full(h));
+        }
+      }
+      mma_commit(bars.v_empty(vs));
+      ++v_it;
+      if (ksn >= 0) {
+        mma_commit(bars.k_empty(ksn));
+        ++k_it;
+      }
+      j = jn;
+    }
+    for (int h = 0; h < 2; ++h) {
+      if (!tk.live[h]) continue;
+      if (!o_ready[h]) {  // keeps the o_empty phases in step even without a PV
+        if (!wait_phase(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, kRoleMma, -1)) goto drain;
+      }
+      mma_commit(bars.o_full(h));
+      ++o_it[h];
+    }
+  }
+drain:
+  // Every MMA this thread issued must be complete before TMEM is freed.
+  mma_commit(bars.done());
+  wait_phase(bars.done(), 0, ctl, kRoleMma, -1, false);
+}
+
+template <int D, int MASK>
+__device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t tmem,
+                             const Ctl& ctl) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hh = (warp - 2) >> 2;          // which Q tile of the pair
+  const int quarter = warp & 3;            // TMEM lanes this warp may access
+  const int row = quarter * 32 + lane;     // query row inside the Q tile
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const uint32_t t_s = lane_base + C::tm_s(hh);
+  const uint32_t t_o = lane_base + C::tm_o(hh);
+  const float c = p.c;
+  uint32_t s_par = 0, o_par = 0;
+
+  for (int t = blockIdx.x; t < p.n_tasks; t += gridDim.x) {
+    const Task tk = decode_task<MASK>(t, p);
+    if (!tk.live[hh]) continue;
+    const int q0 = tk.q0[hh];
+    const int q = q0 + row;
+    // neighbourhood: this query's grid coordinates and clamped window starts
+    int qy = 0, qx = 0, wy = 0, wx = 0;
+    if (MASK == kMaskNaClamp || MASK == kMaskNaWrap) {
+      qy = q / p.grid_w;
+      qx = q - qy * p.grid_w;
+      const int half = p.window >> 1;
+      wy = min(max(qy - half, 0), p.grid_h - p.window);
+      wx = min(max(qx - half, 0), p.grid_w - p.window);
+    }
+    float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
+    float l = 0.f;                // running row sum relative to m_ref
+    bool first = true;
+    for (int j = 0; j < p.n_kv; ++j) {
+      const int cls = tile_class<MASK>(q0, j, p);
+      if (cls == 0) continue;
+      if (!warp_wait(bars.s_full(hh), s_par, ctl, j)) return;
+      s_par ^= 1u;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128(t_s, sr);
+      float s[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+      if (cls == 2) {
+        const int k0 = j * kBN;
+        if (MASK == kMaskNone || MASK == kMaskCausal) {
+          int lim = p.Nk - 1 - k0;                       // last valid key column
+          if (MASK == kMaskCausal) lim = min(lim, q - k0);
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i > lim) s[i] = -CUDART_INF_F;
+        } else {
+          const int G_h = p.grid_h, G_w = p.grid_w, w = p.window, half = w >> 1;
+          int ky = k0 / G_w, kx = k0 - ky * G_w;
+          const int nvalid = p.Nk - k0;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            bool ok;
+            if (MASK == kMaskNaClamp) {
+              ok = static_cast<unsigned>(ky - wy) < static_cast<unsigned>(w) &&
+                   static_cast<unsigned>(kx - wx) < static_cast<unsigned>(w);
+            } else {
+              int dy = ky - qy + half;
+              dy += (dy < 0) ? G_h : 0;
+              dy -= (dy >= G_h) ? G_h : 0;
+              int dx = kx - qx + half;
+              dx += (dx < 0) ? G_w : 0;
+              dx -= (dx >= G_w) ? G_w : 0;
+              ok = dy < w && dx < w;
+            }
+            if (!ok || i >= nvalid) s[i] = -CUDART_INF_F;
+            if (++kx == G_w) {
+              kx = 0;
+              ++ky;
+            }
+          }
+        }
+      }
+      float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+      for (int i = 2; i < 128; i += 2) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+      }
+      const float mx = fmaxf(mx0, mx1);
+      const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * c;
+      const bool grow = m_tile > m_ref + kRescaleLog2;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = ex2(m_ref - m_tile);  // 0 while m_ref is still -inf
+        l *= alpha;
+        m_ref = m_tile;
+      }
+      const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2(fmaf(s[2 * i], c, neg_m));
+        const float p1 = ex2(fmaf(s[2 * i + 1], c, neg_m));
+        sum0 += p0;
+        sum1 += p1;
+        pk[i] = pack_bf16(p0, p1);
+      }
+      l += sum0 + sum1;
+      // O already holds the previous tiles' P V: bring it to the new maximum.
+      if (__any_sync(0xffffffffu, grow && !first)) {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t ov[32];
+          tmem_ld32(t_o + ch * 32, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(t_o + ch * 32, ov);
+        }
+      }
+      {
+        uint32_t lo[32], hi[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          lo[i] = pk[i];
+          hi[i] = pk[32 + i];
+        }
+        tmem_st32(t_s, lo);
+        tmem_st32(t_s + 32, hi);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.p_full(hh));
+      first = false;
+    }
+    // epilogue: O / l, bf16 store, log-sum-exp
+    if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return;
+    o_par ^= 1u;
+    tc_fence_after();
+    const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    const bool row_ok = q < p.Nq;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                          static_cast<int64_t>(q) * p.o_sn;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t ov[32];
+      tmem_ld32(t_o + ch * 32, ov);
+      if (ch == D / 32 - 1) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.o_empty(hh));
+      }
+      if (row_ok) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          packed[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l,
+                                __uint_as_float(ov[2 * i + 1]) * inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+    if (row_ok && p.lse != nullptr) {
+      const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
+      p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int D, int MASK>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KernelParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  Bars bars{sbase + C::kOffBar, C::kKStages, C::kVStages};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * bars.count());
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bars.q_full(), 1);
+    mbar_init(bars.q_empty(), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bars.s_full(h), 1);
+      mbar_init(bars.p_full(h), 4);   // one arrive per softmax warp
+      mbar_init(bars.o_full(h), 1);
+      mbar_init(bars.o_empty(h), 4);
+    }
+    mbar_init(bars.done(), 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(bars.k_full(s), 1);
+      mbar_init(bars.k_empty(s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(bars.v_full(s), 1);
+      mbar_init(bars.v_empty(s), 1);
+    }
+    *abort_flag = 0u;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tm_q);
+    prefetch_tmap(&p.tm_k);
+    prefetch_tmap(&p.tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) loader_role<D, MASK>(p, sbase, bars, ctl);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<D, MASK>(p, sbase, bars, tmem, ctl);
+    __syncwarp();
+  } else {
+    softmax_role<D, MASK>(p, bars, tmem, ctl);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- launch
+
+constexpr int kMinSmemBytes = 116 * 1024;  // more than half an SM: one CTA (and one TMEM owner) per SM
+
+template <int D>
+constexpr int smem_request() {
+  return Cfg<D>::kSmemBytes > kMinSmemBytes ? Cfg<D>::kSmemBytes : kMinSmemBytes;
+}
+
+template <int D, int MASK>
+cudaError_t launch_mask(const KernelParams& p, int grid, cudaStream_t s) {
+  auto kern = attn_fwd_kernel<D, MASK>;
+  const int smem = smem_request<D>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dim(const KernelParams& p, int mask, int grid, cudaStream_t s) {
+  switch (mask) {
+    case kMaskNone: return launch_mask<D, kMaskNone>(p, grid, s);
+    case kMaskCausal: return launch_mask<D, kMaskCausal>(p, grid, s);
+    case kMaskNaClamp: return launch_mask<D, kMaskNaClamp>(p, grid, s);
+    case kMaskNaWrap: return launch_mask<D, kMaskNaWrap>(p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace dev
+}  // namespace attn

@@ -1,0 +1,167 @@
+/*
+ * attn.h -- C ABI of libattn.so: the fused exact-attention forward pass for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Operation (one call):
+ *   O[b,h,i,:] = sum_{j in A(i)} softmax_j(scale * Q[b,h,i,:] . K[b,h,j,:]) V[b,h,j,:]
+ *   LSE[b,h,i] = ln sum_{j in A(i)} exp(scale * Q[b,h,i,:] . K[b,h,j,:])
+ * computed tile by tile with a running row maximum and row sum, the division
+ * by the row sum deferred to the end, so the Nq x Nk score matrix never
+ * reaches device memory.
+ *   - "Fused Self Attention" (AWS Neuron NKI tutorial), sections "Background"
+ *     (S = Q K^T, R = softmax(S) V), "Fusion to Save SBUF Space" (one strip of
+ *     query rows at a time) and "Softmax implementation" (row maximum, row
+ *     sum, division delayed until after the product with V).
+ *   - PhotoRoom / xformers memory-efficient attention post ("torch-permute"
+ *     copy): Q and K are read in tiles with a running softmax, and only the
+ *     end result is written to main GPU memory.
+ *   - "Profiling in PyTorch" part 3, "Deconstructing Naive Attention": scores
+ *     are scaled, masked positions are filled with -inf before the softmax;
+ *     "Introducing Scaled Dot Product Attention": is_causal=True.
+ *   - NATTEN issue #142 "circular windowed attention": 2-D neighbourhood
+ *     attention (each query attends the keys between its window start and
+ *     end), its circular "wrap" mode, and a float32 logsumexp output shaped
+ *     like q without its last dimension.
+ *
+ * Allowed sets A(i):
+ *   ATTN_MASK_NONE   every key j < Nk.
+ *   ATTN_MASK_CAUSAL j <= i (top-left alignment, also when Nq != Nk).
+ *   ATTN_MASK_NA2D   tokens are row-major on a grid_h x grid_w grid (Nq = Nk =
+ *                    grid_h * grid_w); per axis the window holds `window` (odd)
+ *                    positions: clamp mode (wrap = 0) shifts a full window
+ *                    inward at the borders, start = clamp(c - window/2, 0,
+ *                    G - window); wrap mode (wrap = 1) takes the positions
+ *                    (c + t) mod G, t in [-window/2, window/2].
+ *
+ * Data layout (device memory, owned and allocated by the caller):
+ *   q, o : bf16 [B, H, Nq, d]   k, v : bf16 [B, H, Nk, d]   (contiguous by
+ *          default; attn_fwd_ex accepts element strides for b, h and n, the
+ *          last dimension always contiguous, e.g. NATTEN's heads-last
+ *          [B, X, Y, heads, d] layout without a permute)
+ *   lse  : fp32 [B, H, Nq] contiguous, natural log; NULL = not written.
+ *   d in {32, 64, 128}. Pointers 16-byte aligned; element strides multiples
+ *   of 8 (16 bytes).
+ *
+ * Execution: every call only enqueues work on a CUDA stream (the one set by
+ * attn_set_stream for the calling thread, or attn_params_ex.stream) and
+ * returns; it launches exactly one kernel and allocates nothing per call. The
+ * library keeps one lazily allocated device status word per device.
+ * Device-side failures (a bounded wait that ran out) are reported by
+ * attn_get_device_status() after the caller synchronises the stream.
+ *
+ * Errors: every entry point returns ATTN_OK (0) or one of the codes below;
+ * argument checks happen on the host before any CUDA call, so an invalid call
+ * touches no device state. attn_last_error() gives a one-line message for
+ * the calling thread's last failure.
+ */
+#ifndef EXACT_ATTENTION_69_ATTN_H
+#define EXACT_ATTENTION_69_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ATTN_ABI_VERSION 1
+
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_NA2D = 2
+} attn_mask_kind;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,  /* sizes < 1, scale not finite or <= 0, even or
+                                oversized window, wrap without NA2D, NA2D with
+                                Nq != Nk or a non-square Nq and no grid, ... */
+  ATTN_ERR_UNSUPPORTED = 2,  /* d not in {32,64,128}; NA2D dilation > 1 */
+  ATTN_ERR_MISALIGNED = 3,   /* a pointer not 16-byte aligned, a stride not a
+                                multiple of 8 elements */
+  ATTN_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed; the
+                                message names it */
+  ATTN_ERR_TIMEOUT = 5       /* a device-side wait ran past its bound; the
+                                kernel stopped early, outputs are undefined */
+} attn_status;
+
+/* Full parameter block for attn_fwd_ex. Call attn_params_init first: it sets
+ * every field to its default (contiguous strides, dilation 1, no extras). */
+typedef struct attn_params_ex {
+  const void* q;   /* bf16, see layout above */
+  const void* k;
+  const void* v;
+  void* o;         /* bf16 output */
+  float* lse;      /* fp32 [B,H,Nq] output, or NULL */
+  int B, H, Nq, Nk, d;
+  float scale;     /* > 0 and finite, typically 1/sqrt(d) */
+  int mask_kind;   /* attn_mask_kind */
+  int window;      /* NA2D: odd window size; others: must be 0 */
+  int dilation;    /* NA2D: 1 (others must be 1) */
+  int wrap;        /* NA2D: 0 = clamp, 1 = wrap; others: must be 0 */
+  int grid_h, grid_w; /* NA2D token grid; 0,0 = square grid of side sqrt(Nq) */
+  /* element strides of dims (b, h, n); all zero = contiguous [B,H,N,d] */
+  int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
+  void* stream;    /* cudaStream_t; NULL = the calling thread's stream */
+  int num_ctas;    /* persistent CTAs; 0 = one per SM (smaller values are for tests) */
+  uint64_t timeout_ns; /* bound on every device-side wait; 0 = 2 seconds */
+  int inject;      /* test hook: 1 = the loader withholds one K tile so that
+                      the kernel's bounded wait runs out (ATTN_ERR_TIMEOUT);
+                      0 otherwise */
+  void* ev_start;  /* optional cudaEvent_t recorded right before the kernel */
+  void* ev_stop;   /* optional cudaEvent_t recorded right after the kernel */
+} attn_params_ex;
+
+/* Fill *p with defaults (zero pointers and sizes, dilation 1, contiguous). */
+void attn_params_init(attn_params_ex* p);
+
+/*
+ * attn_fwd: the fused forward pass over contiguous bf16 [B,H,N,d] tensors.
+ * q,k,v,o are device pointers, lse a device pointer or NULL. For
+ * ATTN_MASK_NA2D the token grid is square, side sqrt(Nq) (else
+ * ATTN_ERR_INVALID_ARG); use attn_fwd_ex for other grids and layouts.
+ * Returns an attn_status code. Asynchronous on the thread's stream.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int H, int Nq, int Nk, int d, float scale,
+             int mask_kind, int window, int dilation, int wrap);
+
+/* attn_fwd with every option (strides, grid, stream, events, test hooks). */
+int attn_fwd_ex(const attn_params_ex* p);
+
+/* Set the CUDA stream (a cudaStream_t, NULL = legacy default stream) used by
+ * the calling thread's later attn_fwd calls. Thread-local; always ATTN_OK. */
+int attn_set_stream(void* stream);
+
+/* Read and clear the current device's status word. Call after synchronising
+ * the stream of the calls in question. Returns ATTN_OK, ATTN_ERR_TIMEOUT, or
+ * ATTN_ERR_CUDA if the word could not be read. If detail is not NULL it
+ * receives 4 words: code, role (0 loader, 1 MMA issuer, 2 softmax), KV tile
+ * index, CTA index of the first failure. */
+int attn_get_device_status(uint32_t* detail);
+
+/* Static one-line description of a status code. */
+const char* attn_error_string(int code);
+
+/* One-line message about the calling thread's last failing call ("" if none). */
+const char* attn_last_error(void);
+
+/* Number of SMs the persistent grid would use on the current device, or a
+ * negative attn_status on failure. */
+int attn_device_sm_count(void);
+
+/* Free the library's per-device state (status words). Later calls re-create it. */
+void attn_shutdown(void);
+
+/* ATTN_ABI_VERSION of the built library. */
+int attn_abi_version(void);
+
+/* sizeof(attn_params_ex) in the built library (lets bindings check their
+ * copy of the struct layout). */
+int attn_params_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_69_ATTN_H */

@@ -1,0 +1,40 @@
+// Host build of the kernel's tile planning (which K/V tiles a Q tile visits,
+// and which of them need the in-tile mask), for CPU tests against the oracle.
+#include "attn_sm103.cuh"
+
+namespace {
+template <int MASK>
+int cls(int q0, int j, const attn::KernelParams& p) { return attn::dev::tile_class<MASK>(q0, j, p); }
+}
+
+extern "C" int tile_class_host(int mask, int q0, int j, int Nq, int Nk, int grid_h, int grid_w,
+                               int window) {
+  attn::KernelParams p{};
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.grid_h = grid_h;
+  p.grid_w = grid_w;
+  p.window = window;
+  p.n_kv = (Nk + attn::kBN - 1) / attn::kBN;
+  switch (mask) {
+    case attn::kMaskNone: return cls<attn::kMaskNone>(q0, j, p);
+    case attn::kMaskCausal: return cls<attn::kMaskCausal>(q0, j, p);
+    case attn::kMaskNaClamp: return cls<attn::kMaskNaClamp>(q0, j, p);
+    case attn::kMaskNaWrap: return cls<attn::kMaskNaWrap>(q0, j, p);
+    default: return -1;
+  }
+}
+
+// Task index -> (b, h, first row of Q tile 0), as the kernel decodes it.
+extern "C" void decode_task_host(int mask, int t, int B, int H, int Nq, int* out) {
+  attn::KernelParams p{};
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.n_qpairs = (Nq + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  attn::dev::Task k = mask == attn::kMaskCausal ? attn::dev::decode_task<attn::kMaskCausal>(t, p)
+                                                : attn::dev::decode_task<attn::kMaskNone>(t, p);
+  out[0] = k.b;
+  out[1] = k.h;
+  out[2] = k.q0[0];
+}

@@ -1,0 +1,83 @@
+"""Host build of the kernel's tile planning against the oracle's masks (CPU).
+
+For every Q tile (128 query rows) and K/V tile (128 keys) the kernel decides:
+skip (no allowed pair), unmasked (every pair allowed) or masked. Checked here
+exactly against the allowed-set matrix of the numpy oracle twin: a skipped
+tile holds no allowed pair, a visited one holds at least one (no wasted
+tiles), and an unmasked one holds only allowed pairs.
+"""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+from oracle import reference_np as twin
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+MASK_CODE = {"none": 0, "causal": 1, "clamp": 2, "wrap": 3}
+
+
+@pytest.fixture(scope="module")
+def plan(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    out = str(tmp_path_factory.mktemp("plan") / "tile_plan.so")
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O1", "-std=c++17",
+                    "-shared", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
+                    "-I", os.path.join(ROOT, "exact_attention_69_gb300", "csrc"),
+                    os.path.join(ROOT, "tests", "host", "tile_plan.cu"), "-o", out], check=True)
+    lib = ctypes.CDLL(out)
+    lib.tile_class_host.argtypes = [ctypes.c_int] * 8
+    lib.tile_class_host.restype = ctypes.c_int
+    lib.decode_task_host.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
+    return lib
+
+
+CASES = [
+    ("none", 300, 300, None, 0), ("none", 129, 1000, None, 0), ("none", 1, 1, None, 0),
+    ("causal", 700, 700, None, 0), ("causal", 300, 1000, None, 0), ("causal", 1000, 300, None, 0),
+    ("causal", 2048, 2048, None, 0),
+    ("clamp", 4096, 4096, (64, 64), 7), ("wrap", 4096, 4096, (64, 64), 7),
+    ("clamp", 25, 25, (5, 5), 3), ("wrap", 25, 25, (5, 5), 3),
+    ("clamp", 400, 400, (20, 20), 5), ("wrap", 400, 400, (20, 20), 5),
+    ("clamp", 1200, 1200, (24, 50), 7), ("wrap", 1200, 1200, (24, 50), 7),
+    ("clamp", 4800, 4800, (30, 160), 9), ("wrap", 4800, 4800, (30, 160), 9),
+    ("wrap", 1521, 1521, (39, 39), 39), ("clamp", 1521, 1521, (39, 39), 1),
+]
+
+
+@pytest.mark.parametrize("mask,Nq,Nk,grid,window", CASES)
+def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window):
+    allowed = twin.mask_matrix(Nq, Nk, mask, window, 1, grid)
+    gh, gw = grid if grid else (0, 0)
+    n_kv = -(-Nk // 128)
+    for q0 in range(0, Nq, 128):
+        rows = allowed[q0:min(q0 + 128, Nq)]
+        for j in range(n_kv):
+            block = rows[:, j * 128:min(j * 128 + 128, Nk)]
+            c = plan.tile_class_host(MASK_CODE[mask], q0, j, Nq, Nk, gh, gw, window)
+            assert c in (0, 1, 2)
+            assert (c != 0) == bool(block.any()), (q0, j, c)
+            if c == 1:
+                assert block.all() and block.shape[1] == 128, (q0, j)
+
+
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_tasks_cover_every_q_tile_once(plan, mask):
+    B, H, Nq = 3, 5, 1000
+    n_qpairs = -(-Nq // 256)
+    seen = set()
+    out = (ctypes.c_int * 3)()
+    for t in range(B * H * n_qpairs):
+        plan.decode_task_host(MASK_CODE[mask], t, B, H, Nq, out)
+        key = (out[0], out[1], out[2])
+        assert key not in seen
+        seen.add(key)
+    assert seen == {(b, h, 256 * p) for b in range(B) for h in range(H) for p in range(n_qpairs)}
+    if mask == "causal":  # longest pairs (largest row offset) come first
+        plan.decode_task_host(1, 0, B, H, Nq, out)
+        assert out[2] == 256 * (n_qpairs - 1)
