@@ -67,11 +67,14 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
     p.num_ctas = int(num_ctas)
     p.timeout_ns = int(timeout_ns)
     p.inject = int(inject)
-    if events is not None:
-        p.ev_start = events[0].cuda_event
-        p.ev_stop = events[1].cuda_event
     with torch.cuda.device(q.device):
+        # torch events bracket the single launch on the same stream (events
+        # recorded inside the library would be invisible to torch)
+        if events is not None:
+            events[0].record(stream)
         _lib.check(_lib.fwd_ex(p), "attn_fwd")
+        if events is not None:
+            events[1].record(stream)
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
