@@ -10,7 +10,12 @@ namespace attn {
 
 constexpr int kBM = 128;        // query rows per Q tile: one TMEM lane and one softmax thread per row
 constexpr int kBN = 128;        // keys per K/V tile
-constexpr int kWarps = 10;      // warp 0 loader, warp 1 MMA issuer, warps 2-5 / 6-9 softmax of Q tile 0 / 1
+constexpr int kWarps = 12;      // warpgroup 0: warp 0 loader, warp 1 MMA issuer (warps 2-3 idle);
+                                // warpgroups 1 / 2: softmax of Q tile 0 / 1
+constexpr int kRegsControl = 72;   // registers per thread of warpgroup 0 after setmaxnreg
+constexpr int kRegsSoftmax = 216;  // registers per thread of warpgroups 1-2 after setmaxnreg
+// 128 * kRegsControl + 256 * kRegsSoftmax must not exceed 384 * 168 (the launch's registers)
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale row maximum until the true one exceeds it by 2^8
 

@@ -10,11 +10,15 @@
 //   warp 1      MMA issuer (one thread): S_h = Q_h K_j^T into TMEM
 //               (tcgen05.mma, both operands in shared memory), then
 //               O_h += P_h V_j (A operand P_h read from TMEM)
-//   warps 2-5   softmax of Q tile 0, warps 6-9 softmax of Q tile 1: one thread
+//   warps 2-3   idle (they complete warpgroup 0, which gives its registers
+//               to the softmax warpgroups with setmaxnreg)
+//   warps 4-7   softmax of Q tile 0, warps 8-11 softmax of Q tile 1: one thread
 //               per query row reads its S row from TMEM, applies the mask,
 //               keeps the running maximum and row sum, writes P as bf16 back
-//               over S, rescales O when the maximum grew, and finally divides
-//               O by the row sum and stores O and the log-sum-exp.
+//               over S in two halves of 64 keys (each announced on its own
+//               barrier so that P V starts on the first half while the second
+//               is computed), rescales O when the maximum grew, and finally
+//               divides O by the row sum and stores O and the log-sum-exp.
 //
 // The method: "Fused Self Attention" (NKI tutorial) -- one strip of query rows
 // at a time ("Fusion to Save SBUF Space"), row maxima and row sums with the
@@ -158,6 +162,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Per-warpgroup register budget (all threads of the warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void set_max_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void set_max_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -176,6 +190,13 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
@@ -235,15 +256,16 @@ struct Bars {
   __device__ uint32_t q_full() const { return base; }
   __device__ uint32_t q_empty() const { return base + 8; }
   __device__ uint32_t s_full(int h) const { return base + 16 + 8 * h; }
-  __device__ uint32_t p_full(int h) const { return base + 32 + 8 * h; }
-  __device__ uint32_t o_full(int h) const { return base + 48 + 8 * h; }
-  __device__ uint32_t o_empty(int h) const { return base + 64 + 8 * h; }
-  __device__ uint32_t done() const { return base + 80; }
-  __device__ uint32_t k_full(int s) const { return base + 88 + 8 * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 88 + 8 * (kst + s); }
-  __device__ uint32_t v_full(int s) const { return base + 88 + 8 * (2 * kst + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 88 + 8 * (2 * kst + vst + s); }
-  __device__ int count() const { return 11 + 2 * kst + 2 * vst; }
+  // P of Q tile h, keys [64 * part, 64 * part + 64) written to TMEM
+  __device__ uint32_t p_full(int h, int part) const { return base + 32 + 8 * (2 * h + part); }
+  __device__ uint32_t o_full(int h) const { return base + 64 + 8 * h; }
+  __device__ uint32_t o_empty(int h) const { return base + 80 + 8 * h; }
+  __device__ uint32_t done() const { return base + 96; }
+  __device__ uint32_t k_full(int s) const { return base + 104 + 8 * s; }
+  __device__ uint32_t k_empty(int s) const { return base + 104 + 8 * (kst + s); }
+  __device__ uint32_t v_full(int s) const { return base + 104 + 8 * (2 * kst + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 104 + 8 * (2 * kst + vst + s); }
+  __device__ int count() const { return 13 + 2 * kst + 2 * vst; }
 };
 
 // ------------------------------------------------------------- bounded waits
@@ -254,7 +276,7 @@ struct Ctl {
   uint64_t timeout_ns;
 };
 
-static __device__ __noinline__ void report_timeout(const Ctl& c, uint32_t role, int tile) {
+static __device__ __forceinline__ void report_timeout(const Ctl& c, uint32_t role, int tile) {
   if (atomicCAS(c.status, 0u, kStatusTimeout) == 0u) {
     c.status[1] = role;
     c.status[2] = static_cast<uint32_t>(tile);
@@ -264,7 +286,7 @@ static __device__ __noinline__ void report_timeout(const Ctl& c, uint32_t role, 
   *c.abort = 1u;
 }
 
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t role,
+static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t role,
                                        int tile, bool honour_abort) {
   const uint64_t t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
@@ -350,7 +372,7 @@ __host__ __device__ __forceinline__ bool axis_meets(int c0, int c1, int e0, int 
 // Does any query in rows [q0, q1) attend any key in [k0, k1)? Exact for
 // dilation 1: the Q and K ranges are cut into their grid-row segments.
 template <bool WRAP>
-__host__ __device__ __noinline__ bool na_tile_meets(int q0, int q1, int k0, int k1, const KernelParams& p) {
+__host__ __device__ __forceinline__ bool na_tile_meets(int q0, int q1, int k0, int k1, const KernelParams& p) {
   const int W = p.grid_w;
   const int kr0 = k0 / W, kr1 = (k1 - 1) / W;
   for (int qa = q0; qa < q1;) {
@@ -456,30 +478,45 @@ drain:
     if (v_armed[s] >= 0) wait_phase(bars.v_full(s), v_armed[s], ctl, kRoleLoader, -1, false);
 }
 
-template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tmem, int h, uint32_t q_tile, uint32_t k_tile) {
-  using C = Cfg<D>;
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    const int chunk = (ks * 16) / C::kBoxCols;
-    const uint32_t off = chunk * C::kChunkBytes + ((ks * 16) % C::kBoxCols) * 2;
-    const uint64_t a = smem_desc(q_tile + off, 16, 8 * C::kSwizzle, C::kLayout);
-    const uint64_t b = smem_desc(k_tile + off, 16, 8 * C::kSwizzle, C::kLayout);
-    mma_ss(tmem + C::tm_s(h), a, b, C::kIdescS, ks > 0 ? 1u : 0u);
-  }
+// Descriptors of consecutive k-steps differ only in the start address field
+// (bits 0-13, address >> 4), and no step carries out of it (shared memory is
+// below 256 KB): each step adds a compile-time offset to one base descriptor.
+// The MMA issuer runs with few registers: an opaque copy of an address keeps
+// the compiler from hoisting every per-step descriptor out of the tile loop.
+__device__ __forceinline__ uint32_t opaque(uint32_t x) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(x));
+  return x;
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, bool accumulate) {
+__device__ __forceinline__ void issue_s(uint32_t tmem, int h, uint32_t q_tile, uint32_t k_tile) {
   using C = Cfg<D>;
+  q_tile = opaque(q_tile);
+  k_tile = opaque(k_tile);
+  const uint64_t a0 = smem_desc(q_tile, 16, 8 * C::kSwizzle, C::kLayout);
+  const uint64_t b0 = smem_desc(k_tile, 16, 8 * C::kSwizzle, C::kLayout);
 #pragma unroll
-  for (int ks = 0; ks < kBN / 16; ++ks) {
-    // V is [key, d] with d contiguous: the B operand (K = keys, N = d) is MN-major.
-    // 16 keys = 16 rows of kSwizzle bytes; column chunks are kChunkBytes apart.
-    const uint64_t b = smem_desc(v_tile + ks * 16 * C::kSwizzle, C::kChunkBytes,
-                                 8 * C::kSwizzle, C::kLayout);
-    mma_ts(tmem + C::tm_o(h), tmem + C::tm_s(h) + ks * 8, b, C::kIdescO,
-           (accumulate || ks > 0) ? 1u : 0u);
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t off = ((ks * 16) / C::kBoxCols) * C::kChunkBytes + ((ks * 16) % C::kBoxCols) * 2;
+    mma_ss(tmem + C::tm_s(h), a0 + (off >> 4), b0 + (off >> 4), C::kIdescS, ks > 0 ? 1u : 0u);
+  }
+}
+
+// O_h += P_h[:, keys of `part`] V_j[keys of `part`, :], part 0 = keys 0-63, 1 = keys 64-127.
+// V is [key, d] with d contiguous: the B operand (K = keys, N = d) is MN-major;
+// 16 keys = 16 rows of kSwizzle bytes; column chunks are kChunkBytes apart.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, bool accumulate,
+                                         int part) {
+  using C = Cfg<D>;
+  v_tile = opaque(v_tile);
+  const uint64_t b0 = smem_desc(v_tile, C::kChunkBytes, 8 * C::kSwizzle, C::kLayout);
+  const uint32_t t_o = tmem + C::tm_o(h), t_p = tmem + C::tm_s(h);
+#pragma unroll
+  for (int k = 0; k < kBN / 32; ++k) {
+    const int ks = part * (kBN / 32) + k;
+    mma_ts(t_o, t_p + ks * 8, b0 + ((ks * 16 * C::kSwizzle) >> 4), C::kIdescO,
+           (accumulate || k > 0) ? 1u : 0u);
   }
 }
 
@@ -519,13 +556,16 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       int ksn = -1;
       for (int h = 0; h < 2; ++h) {
         if (tile_active<MASK>(tk, h, j, p)) {
-          if (!wait_phase(bars.p_full(h), p_par[h], ctl, kRoleMma, j)) goto drain;
-          p_par[h] ^= 1u;
           if (!o_ready[h]) {
             if (!wait_phase(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, kRoleMma, j)) goto drain;
           }
-          tc_fence_after();
-          issue_pv<D>(tmem, h, sbase + C::kOffV + vs * C::kTileBytes, o_ready[h]);
+          for (int part = 0; part < 2; ++part) {
+            if (!wait_phase(bars.p_full(h, part), p_par[h], ctl, kRoleMma, j)) goto drain;
+            tc_fence_after();
+            issue_pv<D>(tmem, h, sbase + C::kOffV + vs * C::kTileBytes, o_ready[h] || part > 0,
+                        part);
+          }
+          p_par[h] ^= 1u;
           o_ready[h] = true;
         }
         if (has_next && tile_active<MASK>(tk, h, jn, p)) {
@@ -568,7 +608,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
                              const Ctl& ctl) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hh = (warp - 2) >> 2;          // which Q tile of the pair
+  const int hh = (warp - 4) >> 2;          // which Q tile of the pair
   const int quarter = warp & 3;            // TMEM lanes this warp may access
   const int row = quarter * 32 + lane;     // query row inside the Q tile
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -640,13 +680,16 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
           }
         }
       }
-      float mx0 = s[0], mx1 = s[1];
+      // row maximum: 8 independent chains of 3-input max
+      float mx8[8];
 #pragma unroll
-      for (int i = 2; i < 128; i += 2) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
+      for (int ch = 0; ch < 8; ++ch) {
+        mx8[ch] = fmaxf(s[ch], s[ch + 8]);
+#pragma unroll
+        for (int i = 16; i < 128; i += 16) mx8[ch] = fmax3(mx8[ch], s[ch + i], s[ch + i + 8]);
       }
-      const float mx = fmaxf(mx0, mx1);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
       const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * c;
       const bool grow = m_tile > m_ref + kRescaleLog2;
       float alpha = 1.f;
@@ -655,19 +698,8 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
         l *= alpha;
         m_ref = m_tile;
       }
-      const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
-      float sum0 = 0.f, sum1 = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2(fmaf(s[2 * i], c, neg_m));
-        const float p1 = ex2(fmaf(s[2 * i + 1], c, neg_m));
-        sum0 += p0;
-        sum1 += p1;
-        pk[i] = pack_bf16(p0, p1);
-      }
-      l += sum0 + sum1;
-      // O already holds the previous tiles' P V: bring it to the new maximum.
+      // O already holds the previous tiles' P V (their MMAs completed before
+      // this S was committed): bring it to the new maximum before the next P V.
       if (__any_sync(0xffffffffu, grow && !first)) {
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
@@ -678,20 +710,31 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
           tmem_st32(t_o + ch * 32, ov);
         }
       }
-      {
-        uint32_t lo[32], hi[32];
+      const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
+      float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
+      // p = 2^(s c - m) in two halves of 64 keys; each half goes to TMEM and is
+      // announced on its own barrier so that P V can start on the first half.
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          lo[i] = pk[i];
-          hi[i] = pk[32 + i];
+          const int e = 64 * part + 2 * i;
+          const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
+          const float2 pe = make_float2(ex2(x.x), ex2(x.y));
+          sum4[i & 3] = __fadd2_rn(sum4[i & 3], pe);
+          pk[i] = pack_bf16(pe.x, pe.y);
         }
-        tmem_st32(t_s, lo);
-        tmem_st32(t_s + 32, hi);
+        tmem_st32(t_s + 32 * part, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.p_full(hh, part));
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.p_full(hh));
+      const float2 sa = __fadd2_rn(sum4[0], sum4[1]), sb = __fadd2_rn(sum4[2], sum4[3]);
+      l += (sa.x + sa.y) + (sb.x + sb.y);
       first = false;
     }
     // epilogue: O / l, bf16 store, log-sum-exp
@@ -750,7 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(bars.q_empty(), 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(bars.s_full(h), 1);
-      mbar_init(bars.p_full(h), 4);   // one arrive per softmax warp
+      mbar_init(bars.p_full(h, 0), 4);   // one arrive per softmax warp
+      mbar_init(bars.p_full(h, 1), 4);
       mbar_init(bars.o_full(h), 1);
       mbar_init(bars.o_empty(h), 4);
     }
@@ -781,13 +825,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
 
-  if (warp == 0) {
-    if (lane == 0) loader_role<D, MASK>(p, sbase, bars, ctl);
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) mma_role<D, MASK>(p, sbase, bars, tmem, ctl);
-    __syncwarp();
+  if (warp < 4) {
+    // warpgroup 0 needs few registers; the softmax warpgroups take them
+    set_max_regs_dec<kRegsControl>();
+    if (warp == 0) {
+      if (lane == 0) loader_role<D, MASK>(p, sbase, bars, ctl);
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) mma_role<D, MASK>(p, sbase, bars, tmem, ctl);
+      __syncwarp();
+    }
   } else {
+    set_max_regs_inc<kRegsSoftmax>();
     softmax_role<D, MASK>(p, bars, tmem, ctl);
   }
 
