@@ -58,6 +58,9 @@ class AttnParamsEx(ctypes.Structure):
         ("inject", ctypes.c_int),
         ("ev_start", ctypes.c_void_p),
         ("ev_stop", ctypes.c_void_p),
+        ("schedule", ctypes.c_int),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_uint64),
     ]
 
 
@@ -105,6 +108,8 @@ def load(path: str = LIB_PATH):
         lib.attn_abi_version.restype = i
         lib.attn_params_size.argtypes = []
         lib.attn_params_size.restype = i
+        lib.attn_workspace_bytes.argtypes = [ctypes.POINTER(AttnParamsEx)]
+        lib.attn_workspace_bytes.restype = ctypes.c_int64
         size = lib.attn_params_size()
         if size != ctypes.sizeof(AttnParamsEx):
             raise ImportError(f"attn_params_ex layout mismatch: library {size} bytes, "

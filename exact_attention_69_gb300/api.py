@@ -44,7 +44,7 @@ def _check_dev(*ts):
 
 
 def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, grid,
-            layout, num_ctas, timeout_ns, inject, events, stream):
+            layout, num_ctas, timeout_ns, inject, events, stream, schedule=0, workspace=None):
     p = _lib.params()
     p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
     p.lse = lse.data_ptr() if lse is not None else None
@@ -67,6 +67,10 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
     p.num_ctas = int(num_ctas)
     p.timeout_ns = int(timeout_ns)
     p.inject = int(inject)
+    p.schedule = int(schedule)
+    if workspace is not None:
+        p.workspace = workspace.data_ptr()
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(q.device):
         # torch events bracket the single launch on the same stream (events
         # recorded inside the library would be invisible to torch)
@@ -81,13 +85,18 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
              mask: str = "none", window: int = 0, dilation: int = 1, grid=None,
              out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
              return_lse: bool = True, num_ctas: int = 0, timeout_ns: int = 0, inject: int = 0,
-             events=None, stream=None):
+             events=None, stream=None, schedule: int = 0,
+             workspace: torch.Tensor | None = None):
     """Fused exact attention forward over [B, H, N, d] bf16 tensors.
 
     mask: 'none' | 'causal' | 'clamp' | 'wrap' (the last two: 2-D neighbourhood
     attention with an odd `window` over a grid_h x grid_w token grid, square
     by default). Returns (o, lse) or o. CPU inputs are copied to the current
     CUDA device, and the results back to the CPU (the end-to-end path).
+    schedule: 0 automatic, 1 whole tasks per CTA, 2 equal shares of K/V tiles
+    with cut tasks merged (unmasked only). workspace: optional zero-filled
+    device tensor for schedule 2 (see workspace_bytes); default: the
+    library's own.
     """
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("expected [B, H, N, d] tensors")
@@ -107,8 +116,25 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
         raise ValueError("lse must be a contiguous float32 [B, H, Nq] tensor")
     _launch(q, k, v, out, lse, B=B, H=H, Nq=Nq, Nk=Nk, d=d, scale=scale, mask=mask,
             window=window, dilation=dilation, grid=grid, layout="bhnd", num_ctas=num_ctas,
-            timeout_ns=timeout_ns, inject=inject, events=events, stream=stream)
+            timeout_ns=timeout_ns, inject=inject, events=events, stream=stream,
+            schedule=schedule, workspace=workspace)
     return (out, lse) if return_lse else out
+
+
+def workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, *, mask: str = "none",
+                    num_ctas: int = 0, schedule: int = 0) -> int:
+    """Bytes of workspace an attn_fwd call of this shape needs on the current device."""
+    p = _lib.params()
+    p.q = p.k = p.v = p.o = 256  # placeholders: only the shape is examined
+    p.B, p.H, p.Nq, p.Nk, p.d = B, H, Nq, Nk, d
+    p.scale = 1.0
+    p.mask_kind = _MASKS[mask]
+    p.num_ctas = int(num_ctas)
+    p.schedule = int(schedule)
+    n = _lib.load().attn_workspace_bytes(p)
+    if n < 0:
+        _lib.check(int(-n), "attn_workspace_bytes")
+    return int(n)
 
 
 def _host_roundtrip(q, k, v, *, return_lse, **kw):

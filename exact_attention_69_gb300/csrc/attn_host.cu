@@ -2,8 +2,9 @@
 //
 // Host work per call: validate the arguments (before any CUDA call), encode
 // the three TMA tensor maps, pick the kernel specialisation, launch once on
-// the caller's stream. The only device memory the library owns is one status
-// word per device, allocated on first use.
+// the caller's stream. The device memory the library owns: one status word
+// per device, and a workspace for split schedules, both allocated on first
+// use (the workspace grows when a call needs more).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -28,6 +29,9 @@ thread_local char t_err[512] = {0};
 struct DeviceState {
   uint32_t* status = nullptr;  // 4 x u32 device status word
   int sm_count = 0;
+  void* ws = nullptr;          // workspace of split schedules (zero-filled when allocated)
+  size_t ws_bytes = 0;
+  uint32_t epoch = 0;          // tag of the last split call
 };
 
 std::mutex g_mu;
@@ -44,6 +48,39 @@ int fail(int code, const char* fmt, ...) {
 
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(ATTN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
+
+// How a call's work is laid out over the persistent CTAs.
+struct Plan {
+  int grid = 0;
+  int split = 0;
+  int n_qpairs = 0, n_kv = 0, n_tasks = 0;
+  int64_t units = 0;
+  size_t part_bytes = 0, count_bytes = 0;
+  size_t ws_bytes() const { return split ? align256(part_bytes) + align256(count_bytes) : 0; }
+};
+
+int make_plan(const attn_params_ex* p, int sm_count, Plan* pl) {
+  pl->n_qpairs = (p->Nq + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  pl->n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
+  pl->n_tasks = p->B * p->H * pl->n_qpairs;
+  pl->units = static_cast<int64_t>(pl->n_tasks) * pl->n_kv;
+  int ctas = sm_count;
+  if (p->num_ctas > 0 && p->num_ctas < ctas) ctas = p->num_ctas;
+  if (p->schedule == 2 && p->mask_kind != ATTN_MASK_NONE)
+    return fail(ATTN_ERR_INVALID_ARG, "schedule 2 applies to ATTN_MASK_NONE only");
+  pl->split = p->schedule == 2 ||
+              (p->schedule == 0 && p->mask_kind == ATTN_MASK_NONE && pl->n_tasks % ctas != 0);
+  if (pl->split) {
+    pl->grid = static_cast<int>(pl->units < ctas ? pl->units : ctas);
+    pl->part_bytes = static_cast<size_t>(pl->grid) * 2 * 2 * 128 * (p->d + 2) * sizeof(float);
+    pl->count_bytes = static_cast<size_t>(pl->n_tasks) * 2 * 4 * sizeof(unsigned long long);
+  } else {
+    pl->grid = pl->n_tasks < ctas ? pl->n_tasks : ctas;
+  }
+  return ATTN_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -135,6 +172,13 @@ int validate(const attn_params_ex* p, Checked* c) {
     return fail(ATTN_ERR_MISALIGNED, "lse must be 4-byte aligned");
   if (p->num_ctas < 0) return fail(ATTN_ERR_INVALID_ARG, "num_ctas must be >= 0");
   if (p->inject != 0 && p->inject != 1) return fail(ATTN_ERR_INVALID_ARG, "inject must be 0 or 1");
+  if (p->schedule < 0 || p->schedule > 2)
+    return fail(ATTN_ERR_INVALID_ARG, "schedule must be 0, 1 or 2");
+  if (p->workspace && !aligned16(p->workspace))
+    return fail(ATTN_ERR_MISALIGNED, "workspace must be 16-byte aligned");
+  if (static_cast<int64_t>(p->B) * p->H * ((p->Nq + 255) / 256) * ((p->Nk + 127) / 128) >=
+      (int64_t{1} << 40))
+    return fail(ATTN_ERR_INVALID_ARG, "problem too large");
   int rc;
   if ((rc = check_strides(p->q_stride, c->qs, p->Nq, p->H, p->d, "q")) != ATTN_OK) return rc;
   if ((rc = check_strides(p->k_stride, c->ks, p->Nk, p->H, p->d, "k")) != ATTN_OK) return rc;
@@ -205,6 +249,42 @@ int encode_map(CUtensorMap* m, const void* base, int d, int N, int H, int B, con
   return ATTN_OK;
 }
 
+// Device pointers of the call's workspace: the caller's, or the library's own
+// (grown, and zero-filled, when too small). Also hands out the call's epoch.
+int acquire_workspace(const attn_params_ex* p, const Plan& pl, DeviceState* ds, void** ws,
+                      uint32_t* epoch) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (++ds->epoch == 0) ds->epoch = 1;
+  *epoch = ds->epoch;
+  const size_t need = pl.ws_bytes();
+  if (p->workspace) {
+    if (p->workspace_bytes < need)
+      return fail(ATTN_ERR_INVALID_ARG, "workspace of %llu bytes, this call needs %zu",
+                  static_cast<unsigned long long>(p->workspace_bytes), need);
+    *ws = p->workspace;
+    return ATTN_OK;
+  }
+  if (ds->ws_bytes < need) {
+    cudaError_t e;
+    if (ds->ws) {
+      if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+      cudaFree(ds->ws);
+      ds->ws = nullptr;
+      ds->ws_bytes = 0;
+    }
+    void* ptr = nullptr;
+    if ((e = cudaMalloc(&ptr, need)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    if ((e = cudaMemset(ptr, 0, need)) != cudaSuccess) {
+      cudaFree(ptr);
+      return cuda_fail(e, "cudaMemset(workspace)");
+    }
+    ds->ws = ptr;
+    ds->ws_bytes = need;
+  }
+  *ws = ds->ws;
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -245,9 +325,20 @@ int attn_fwd_ex(const attn_params_ex* p) {
   kp.grid_h = c.grid_h;
   kp.grid_w = c.grid_w;
   kp.window = p->window;
-  kp.n_qpairs = (p->Nq + 2 * attn::kBM - 1) / (2 * attn::kBM);
-  kp.n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
-  kp.n_tasks = p->B * p->H * kp.n_qpairs;
+  Plan pl;
+  if ((rc = make_plan(p, ds->sm_count, &pl)) != ATTN_OK) return rc;
+  kp.n_qpairs = pl.n_qpairs;
+  kp.n_kv = pl.n_kv;
+  kp.n_tasks = pl.n_tasks;
+  kp.split = pl.split;
+  kp.units = pl.units;
+  if (pl.split) {
+    void* ws = nullptr;
+    if ((rc = acquire_workspace(p, pl, ds, &ws, &kp.epoch)) != ATTN_OK) return rc;
+    kp.ws_part = static_cast<float*>(ws);
+    kp.ws_count = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) +
+                                                         align256(pl.part_bytes));
+  }
   kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
   kp.inject = p->inject;
   kp.status = ds->status;
@@ -256,9 +347,7 @@ int attn_fwd_ex(const attn_params_ex* p) {
   if (p->mask_kind == ATTN_MASK_CAUSAL) mask = attn::kMaskCausal;
   if (p->mask_kind == ATTN_MASK_NA2D) mask = p->wrap ? attn::kMaskNaWrap : attn::kMaskNaClamp;
 
-  int grid = ds->sm_count;
-  if (p->num_ctas > 0 && p->num_ctas < grid) grid = p->num_ctas;
-  if (grid > kp.n_tasks) grid = kp.n_tasks;
+  const int grid = pl.grid;
 
   cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
   cudaError_t e;
@@ -347,14 +436,31 @@ void attn_shutdown(void) {
     if (g_dev[i].status) {
       int prev = 0;
       cudaGetDevice(&prev);
-      if (cudaSetDevice(i) == cudaSuccess) cudaFree(g_dev[i].status);
+      if (cudaSetDevice(i) == cudaSuccess) {
+        cudaFree(g_dev[i].status);
+        if (g_dev[i].ws) cudaFree(g_dev[i].ws);
+      }
       cudaSetDevice(prev);
       g_dev[i].status = nullptr;
+      g_dev[i].ws = nullptr;
+      g_dev[i].ws_bytes = 0;
     }
   }
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+int64_t attn_workspace_bytes(const attn_params_ex* p) {
+  t_err[0] = 0;
+  Checked c;
+  int rc = validate(p, &c);
+  if (rc != ATTN_OK) return -rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return -rc;
+  Plan pl;
+  if ((rc = make_plan(p, ds->sm_count, &pl)) != ATTN_OK) return -rc;
+  return static_cast<int64_t>(pl.ws_bytes());
+}
 
 int attn_params_size(void) { return static_cast<int>(sizeof(attn_params_ex)); }
 

@@ -38,6 +38,16 @@ struct KernelParams {
   int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head
   int n_kv;                     // ceil(Nk / 128)
   int n_tasks;                  // B * H * n_qpairs
+  // Work split. split == 0: whole tasks, round robin over the CTAs. split == 1
+  // (unmasked only): the tasks' K/V tiles form one sequence of `units`
+  // (task-major) and CTA c takes units [c*units/G, (c+1)*units/G); a task cut
+  // between CTAs leaves partial results in the workspace and the last part to
+  // finish merges them.
+  int split;
+  int64_t units;
+  float* ws_part;               // per CTA 2 slots x 2 Q tiles x 128 rows x (d + 2) fp32
+  unsigned long long* ws_count; // per (task, Q tile, 32-row quarter): epoch << 32 | parts arrived
+  uint32_t epoch;               // this call's tag in ws_count (never 0)
   uint64_t timeout_ns;          // bound on every mbarrier wait
   int inject;                   // 1: loader withholds one K tile (tests the bounded wait)
   uint32_t* status;             // device status word: code, role, tile, CTA

@@ -7,7 +7,7 @@
 //
 //   warp 0      loader: TMA of Q (once per task) and of K_j, V_j into
 //               multi-stage shared-memory rings (mbarrier full/empty pairs)
-//   warp 1      MMA issuer (one thread): S_h = Q_h K_j^T into TMEM
+//   warp 1      MMA issuer (one elected lane of the converged warp): S_h = Q_h K_j^T into TMEM
 //               (tcgen05.mma, both operands in shared memory), then
 //               O_h += P_h V_j (A operand P_h read from TMEM)
 //   warps 2-3   idle (they complete warpgroup 0, which gives its registers
@@ -48,6 +48,7 @@ namespace attn {
 namespace dev {
 
 constexpr uint32_t kStatusTimeout = 5;  // same value as ATTN_ERR_TIMEOUT in attn.h
+constexpr uint32_t kSleepHintNs = 200000;  // longest park per try_wait (also the abort latency)
 
 // ------------------------------------------------------------------ PTX wrappers
 
@@ -66,10 +67,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
       : "memory");
 }
 
+// The loader and MMA warps run converged: every lane executes the same
+// instruction stream and `elect.sync` picks the one lane that acts. (Issued
+// from a lone diverged lane, each tcgen05.mma costs ~190 cycles of issue
+// instead of running back to back at the tensor core's rate.)
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "{\n\t.reg .b64 st;\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
       "r"(bytes)
       : "memory");
 }
@@ -83,6 +89,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_test, but lets the hardware park the thread until the phase
+// completes or `hint_ns` passes, instead of returning at once: waiting
+// threads then take no issue slots from the warps that share their scheduler.
+__device__ __forceinline__ bool mbar_test_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -102,12 +123,14 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// 4-D tiled TMA load into shared memory, completion counted on `bar`.
+// 4-D tiled TMA load into shared memory, completion counted on `bar`
+// (warp-wide; one elected lane issues it).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int c0, int c1, int c2, int c3) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
@@ -133,33 +156,38 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D (TMEM) = A (smem) * B (smem) [+ D]
+// D (TMEM) = A (smem) * B (smem) [+ D]   (warp-wide; one elected lane issues it)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// D (TMEM) = A (TMEM) * B (smem) [+ D]
+// D (TMEM) = A (TMEM) * B (smem) [+ D]   (warp-wide; one elected lane issues it)
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// One arrive on `bar` once every tcgen05 operation this thread issued so far is complete.
+// One arrive on `bar` once every tcgen05 operation issued so far by the
+// elected lane is complete (warp-wide; the same lane that issued the MMAs).
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 // Per-warpgroup register budget (all threads of the warpgroup execute it).
@@ -261,11 +289,14 @@ struct Bars {
   __device__ uint32_t o_full(int h) const { return base + 64 + 8 * h; }
   __device__ uint32_t o_empty(int h) const { return base + 80 + 8 * h; }
   __device__ uint32_t done() const { return base + 96; }
-  __device__ uint32_t k_full(int s) const { return base + 104 + 8 * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 104 + 8 * (kst + s); }
-  __device__ uint32_t v_full(int s) const { return base + 104 + 8 * (2 * kst + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 104 + 8 * (2 * kst + vst + s); }
-  __device__ int count() const { return 13 + 2 * kst + 2 * vst; }
+  // turn(h): softmax warpgroup h may start the exponentials of its next tile
+  // that both Q tiles use (arrived by the other warpgroup's 4 warps)
+  __device__ uint32_t turn(int h) const { return base + 104 + 8 * h; }
+  __device__ uint32_t k_full(int s) const { return base + 120 + 8 * s; }
+  __device__ uint32_t k_empty(int s) const { return base + 120 + 8 * (kst + s); }
+  __device__ uint32_t v_full(int s) const { return base + 120 + 8 * (2 * kst + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 120 + 8 * (2 * kst + vst + s); }
+  __device__ int count() const { return 15 + 2 * kst + 2 * vst; }
 };
 
 // ------------------------------------------------------------- bounded waits
@@ -290,9 +321,9 @@ static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, 
                                        int tile, bool honour_abort) {
   const uint64_t t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test_sleep(bar, parity, kSleepHintNs)) return true;
     if (honour_abort && *c.abort) return false;
-    if ((n & 63u) == 0u) {
+    if ((n & 3u) == 0u) {
       if (global_ns() - t0 > c.timeout_ns || n >= (1u << 28)) {
         report_timeout(c, role, tile);
         return false;
@@ -308,12 +339,25 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   return wait_slow(bar, parity, c, role, tile, honour_abort);
 }
 
-// Warp-uniform wait: lane 0 polls, the verdict is broadcast.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, int tile) {
-  const int lane = threadIdx.x & 31;
-  uint32_t ok = 1;
-  if (lane == 0) ok = wait_phase(bar, parity, c, kRoleSoftmax, tile) ? 1u : 0u;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0u;
+// Warp-uniform wait: every lane polls the barrier and warp votes make each
+// decision (done, abort, time out) the same for all lanes, so the warp never
+// diverges. (Polling from one lane while the others wait at a shuffle costs
+// the warps that share the scheduler measurably.)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, int tile,
+                                          uint32_t role = kRoleSoftmax, bool honour_abort = true) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    const bool ok = mbar_test_sleep(bar, parity, kSleepHintNs);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if (honour_abort && __any_sync(0xffffffffu, *c.abort != 0u)) return false;
+    if ((n & 3u) == 0u &&
+        __any_sync(0xffffffffu, global_ns() - t0 > c.timeout_ns || n >= (1u << 28))) {
+      if ((threadIdx.x & 31) == 0) report_timeout(c, role, tile);
+      __syncwarp();
+      return false;
+    }
+  }
 }
 
 // ------------------------------------------------------------- work and masks
@@ -415,12 +459,70 @@ __host__ __device__ __forceinline__ bool tile_active(const Task& tk, int h, int 
 }
 
 // Next KV tile after j that some live Q tile of the task needs (n_kv if none).
+// Next KV tile after j and before `end` that some live Q tile of the task
+// needs (`end` if none).
 template <int MASK>
-__host__ __device__ __forceinline__ int next_tile(const Task& tk, int j, const KernelParams& p) {
-  for (++j; j < p.n_kv; ++j)
+__host__ __device__ __forceinline__ int next_tile(const Task& tk, int j, int end,
+                                                  const KernelParams& p) {
+  for (++j; j < end; ++j)
     if (tile_active<MASK>(tk, 0, j, p) || tile_active<MASK>(tk, 1, j, p)) return j;
-  return p.n_kv;
+  return end;
 }
+
+// ------------------------------------------------------------- work split
+
+// A segment: KV tiles [kv0, kv1) of task t; `head` marks the CTA's first one.
+struct Seg {
+  int t, kv0, kv1;
+  bool head;
+};
+
+// First unit of CTA c when the units are split evenly over `ctas` CTAs.
+__host__ __device__ __forceinline__ int64_t unit_lo(int64_t units, int ctas, int c) {
+  return static_cast<int64_t>(c) * units / ctas;
+}
+
+// The CTA whose unit range holds unit u.
+__host__ __device__ __forceinline__ int cta_of_unit(int64_t units, int ctas, int64_t u) {
+  int c = static_cast<int>(u * ctas / units);
+  while (c > 0 && unit_lo(units, ctas, c) > u) --c;
+  while (c + 1 < ctas && unit_lo(units, ctas, c + 1) <= u) ++c;
+  return c;
+}
+
+template <int MASK>
+struct SegIter {
+  int64_t u, hi;
+  int t_rr;
+  bool first;
+  __device__ __forceinline__ explicit SegIter(const KernelParams& p) : first(true) {
+    if (MASK == kMaskNone && p.split) {
+      u = unit_lo(p.units, gridDim.x, blockIdx.x);
+      hi = unit_lo(p.units, gridDim.x, blockIdx.x + 1);
+    } else {
+      t_rr = blockIdx.x;
+    }
+  }
+  __device__ __forceinline__ bool next(const KernelParams& p, Seg& s) {
+    if (MASK == kMaskNone && p.split) {
+      if (u >= hi) return false;
+      s.t = static_cast<int>(u / p.n_kv);
+      s.kv0 = static_cast<int>(u - static_cast<int64_t>(s.t) * p.n_kv);
+      const int64_t len = min(static_cast<int64_t>(p.n_kv - s.kv0), hi - u);
+      s.kv1 = s.kv0 + static_cast<int>(len);
+      u += len;
+    } else {
+      if (t_rr >= p.n_tasks) return false;
+      s.t = t_rr;
+      s.kv0 = 0;
+      s.kv1 = p.n_kv;
+      t_rr += gridDim.x;
+    }
+    s.head = first;
+    first = false;
+    return true;
+  }
+};
 
 // ---------------------------------------------------------------- roles
 
@@ -433,9 +535,11 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
   for (int s = 0; s < C::kKStages; ++s) k_armed[s] = -1;
   for (int s = 0; s < C::kVStages; ++s) v_armed[s] = -1;
   bool injected = false;
-  for (int t = blockIdx.x; t < p.n_tasks; t += gridDim.x) {
-    const Task tk = decode_task<MASK>(t, p);
-    if (!wait_phase(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, kRoleLoader, -1)) goto drain;
+  SegIter<MASK> it(p);
+  Seg sg;
+  while (it.next(p, sg)) {
+    const Task tk = decode_task<MASK>(sg.t, p);
+    if (!warp_wait(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, -1, kRoleLoader)) goto drain;
     mbar_expect_tx(bars.q_full(), 2 * C::kTileBytes);
     for (int h = 0; h < 2; ++h)
       for (int c = 0; c < C::kChunks; ++c)
@@ -444,9 +548,10 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
     q_armed = static_cast<int>(q_it & 1u);
     ++q_it;
     int nth = 0;
-    for (int j = next_tile<MASK>(tk, -1, p); j < p.n_kv; j = next_tile<MASK>(tk, j, p), ++nth) {
+    for (int j = next_tile<MASK>(tk, sg.kv0 - 1, sg.kv1, p); j < sg.kv1;
+         j = next_tile<MASK>(tk, j, sg.kv1, p), ++nth) {
       const int ks = static_cast<int>(k_it % C::kKStages);
-      if (!wait_phase(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, kRoleLoader, j))
+      if (!warp_wait(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
         goto drain;
       if (p.inject && !injected && nth == 1) {
         injected = true;  // withhold this K tile: the MMA issuer's wait must run out
@@ -459,7 +564,7 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
       }
       ++k_it;
       const int vs = static_cast<int>(v_it % C::kVStages);
-      if (!wait_phase(bars.v_empty(vs), ((v_it / C::kVStages) & 1u) ^ 1u, ctl, kRoleLoader, j))
+      if (!warp_wait(bars.v_empty(vs), ((v_it / C::kVStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
         goto drain;
       mbar_expect_tx(bars.v_full(vs), C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
@@ -471,11 +576,11 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
   }
 drain:
   // The last copy armed on each barrier must have landed before the CTA exits.
-  if (q_armed >= 0) wait_phase(bars.q_full(), q_armed, ctl, kRoleLoader, -1, false);
+  if (q_armed >= 0) warp_wait(bars.q_full(), q_armed, ctl, -1, kRoleLoader, false);
   for (int s = 0; s < C::kKStages; ++s)
-    if (k_armed[s] >= 0) wait_phase(bars.k_full(s), k_armed[s], ctl, kRoleLoader, -1, false);
+    if (k_armed[s] >= 0) warp_wait(bars.k_full(s), k_armed[s], ctl, -1, kRoleLoader, false);
   for (int s = 0; s < C::kVStages; ++s)
-    if (v_armed[s] >= 0) wait_phase(bars.v_full(s), v_armed[s], ctl, kRoleLoader, -1, false);
+    if (v_armed[s] >= 0) warp_wait(bars.v_full(s), v_armed[s], ctl, -1, kRoleLoader, false);
 }
 
 // Descriptors of consecutive k-steps differ only in the start address field
@@ -526,16 +631,18 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
   using C = Cfg<D>;
   uint32_t q_it = 0, k_it = 0, v_it = 0;
   uint32_t p_par[2] = {0, 0}, o_it[2] = {0, 0};
-  for (int t = blockIdx.x; t < p.n_tasks; t += gridDim.x) {
-    const Task tk = decode_task<MASK>(t, p);
-    if (!wait_phase(bars.q_full(), q_it & 1u, ctl, kRoleMma, -1)) goto drain;
+  SegIter<MASK> it(p);
+  Seg sg;
+  while (it.next(p, sg)) {
+    const Task tk = decode_task<MASK>(sg.t, p);
+    if (!warp_wait(bars.q_full(), q_it & 1u, ctl, -1, kRoleMma)) goto drain;
     ++q_it;
     tc_fence_after();
     bool o_ready[2] = {false, false};
-    int j = next_tile<MASK>(tk, -1, p);
-    if (j < p.n_kv) {
+    int j = next_tile<MASK>(tk, sg.kv0 - 1, sg.kv1, p);
+    if (j < sg.kv1) {
       const int ks = static_cast<int>(k_it % C::kKStages);
-      if (!wait_phase(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, kRoleMma, j)) goto drain;
+      if (!warp_wait(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
       for (int h = 0; h < 2; ++h)
         if (tile_active<MASK>(tk, h, j, p)) {
@@ -546,21 +653,21 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       mma_commit(bars.k_empty(ks));
       ++k_it;
     }
-    while (j < p.n_kv) {
-      const int jn = next_tile<MASK>(tk, j, p);
-      const bool has_next = jn < p.n_kv;
+    while (j < sg.kv1) {
+      const int jn = next_tile<MASK>(tk, j, sg.kv1, p);
+      const bool has_next = jn < sg.kv1;
       if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
       const int vs = static_cast<int>(v_it % C::kVStages);
-      if (!wait_phase(bars.v_full(vs), (v_it / C::kVStages) & 1u, ctl, kRoleMma, j)) goto drain;
+      if (!warp_wait(bars.v_full(vs), (v_it / C::kVStages) & 1u, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
       int ksn = -1;
       for (int h = 0; h < 2; ++h) {
         if (tile_active<MASK>(tk, h, j, p)) {
           if (!o_ready[h]) {
-            if (!wait_phase(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, kRoleMma, j)) goto drain;
+            if (!warp_wait(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, j, kRoleMma)) goto drain;
           }
           for (int part = 0; part < 2; ++part) {
-            if (!wait_phase(bars.p_full(h, part), p_par[h], ctl, kRoleMma, j)) goto drain;
+            if (!warp_wait(bars.p_full(h, part), p_par[h], ctl, j, kRoleMma)) goto drain;
             tc_fence_after();
             issue_pv<D>(tmem, h, sbase + C::kOffV + vs * C::kTileBytes, o_ready[h] || part > 0,
                         part);
@@ -571,7 +678,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
         if (has_next && tile_active<MASK>(tk, h, jn, p)) {
           if (ksn < 0) {
             ksn = static_cast<int>(k_it % C::kKStages);
-            if (!wait_phase(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, kRoleMma, jn))
+            if (!warp_wait(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, jn, kRoleMma))
               goto drain;
             tc_fence_after();
           }
@@ -591,7 +698,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
     for (int h = 0; h < 2; ++h) {
       if (!tk.live[h]) continue;
       if (!o_ready[h]) {  // keeps the o_empty phases in step even without a PV
-        if (!wait_phase(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, kRoleMma, -1)) goto drain;
+        if (!warp_wait(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, -1, kRoleMma)) goto drain;
       }
       mma_commit(bars.o_full(h));
       ++o_it[h];
@@ -600,7 +707,127 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
 drain:
   // Every MMA this thread issued must be complete before TMEM is freed.
   mma_commit(bars.done());
-  wait_phase(bars.done(), 0, ctl, kRoleMma, -1, false);
+  warp_wait(bars.done(), 0, ctl, -1, kRoleMma, false);
+}
+
+// ------------------------------------------------------------- partial results
+
+// One arrival on a (task, Q tile) word tagged with this call's epoch; returns
+// the number of parts arrived so far in this call, or 0 if the CAS loop ran
+// past its bound (recorded as a timeout).
+__device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t epoch,
+                                                const Ctl& c) {
+  unsigned long long old = atomicAdd(w, 0ull);
+  for (int n = 0; n < (1 << 20); ++n) {
+    const unsigned long long assumed = old;
+    const uint32_t cnt = static_cast<uint32_t>(assumed >> 32) == epoch
+                             ? static_cast<uint32_t>(assumed) : 0u;
+    const unsigned long long nv = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    old = atomicCAS(w, assumed, nv);
+    if (old == assumed) return cnt + 1u;
+  }
+  report_timeout(c, kRoleSoftmax, -2);
+  return 0u;
+}
+
+// Epilogue of a task cut between CTAs. Each warp handles its 32 rows on its
+// own: write this part (unnormalised O, the running maximum m in log2 units,
+// the row sum l), count the part on the rows' arrival word, and if it is the
+// last part of those rows, merge all parts:
+//   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
+//   LSE = ln 2 (M + log2 L).
+// No CTA waits for another: the last part to finish does the merge.
+// False: the CTA is aborting.
+template <int D>
+__device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars& bars, const Seg& sg,
+                                 const Task& tk, int hh, int row, uint32_t t_o, float m_ref,
+                                 float l, const Ctl& ctl) {
+  const int lane = threadIdx.x & 31;
+  const int quarter = row >> 5;
+  auto slot_of = [&](int cta, bool head) {
+    return p.ws_part +
+           static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2);
+  };
+  float* mine = slot_of(blockIdx.x, sg.head);
+#pragma unroll
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t ov[32];
+    tmem_ld32(t_o + ch * 32, ov);
+    if (ch == D / 32 - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.o_empty(hh));
+    }
+    float4* dst = reinterpret_cast<float4*>(mine + row * D + ch * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                           __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+  }
+  mine[128 * D + row] = m_ref;
+  mine[128 * D + 128 + row] = l;
+  __threadfence();
+  __syncwarp();
+  const int64_t t_first = static_cast<int64_t>(sg.t) * p.n_kv;
+  const int c_lo = cta_of_unit(p.units, gridDim.x, t_first);
+  const int c_hi = cta_of_unit(p.units, gridDim.x, t_first + p.n_kv - 1);
+  uint32_t n = 0;
+  if (lane == 0)
+    n = arrive_part(p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter, p.epoch, ctl);
+  n = __shfl_sync(0xffffffffu, n, 0);
+  if (n != static_cast<uint32_t>(c_hi - c_lo + 1)) return !*ctl.abort;
+  __threadfence();
+  const int q = tk.q0[hh] + row;
+  float M = -CUDART_INF_F;
+  for (int c = c_lo; c <= c_hi; ++c) {
+    const float* sl = slot_of(c, unit_lo(p.units, gridDim.x, c) >= t_first);
+    M = fmaxf(M, __ldcg(sl + 128 * D + row));
+  }
+  float L = 0.f;
+  for (int c = c_lo; c <= c_hi; ++c) {
+    const float* sl = slot_of(c, unit_lo(p.units, gridDim.x, c) >= t_first);
+    const float mi = __ldcg(sl + 128 * D + row);
+    if (mi != -CUDART_INF_F) L += ex2(mi - M) * __ldcg(sl + 128 * D + 128 + row);
+  }
+  const float inv_L = L > 0.f ? 1.f / L : 0.f;
+  const bool row_ok = q < p.Nq;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                        static_cast<int64_t>(q) * p.o_sn;
+#pragma unroll 1
+  for (int ch = 0; ch < D / 16; ++ch) {
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 1
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const float* sl = slot_of(c, unit_lo(p.units, gridDim.x, c) >= t_first);
+      const float mi = __ldcg(sl + 128 * D + row);
+      const float w = mi == -CUDART_INF_F ? 0.f : ex2(mi - M);
+      const float4* src = reinterpret_cast<const float4*>(sl + row * D + ch * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 v = __ldcg(src + i);
+        acc[4 * i] += w * v.x;
+        acc[4 * i + 1] += w * v.y;
+        acc[4 * i + 2] += w * v.z;
+        acc[4 * i + 3] += w * v.w;
+      }
+    }
+    if (row_ok) {
+      uint32_t packed[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) packed[i] = pack_bf16(acc[2 * i] * inv_L, acc[2 * i + 1] * inv_L);
+      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 16);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    }
+  }
+  if (row_ok && p.lse != nullptr) {
+    const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
+    p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
+  }
+  return !*ctl.abort;
 }
 
 template <int D, int MASK>
@@ -616,9 +843,13 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
   const uint32_t t_o = lane_base + C::tm_o(hh);
   const float c = p.c;
   uint32_t s_par = 0, o_par = 0;
+  uint32_t n_pair = 0;  // tiles both Q tiles used so far: the exp2 phases of the
+                        // two warpgroups alternate on them (0 first, then 1)
 
-  for (int t = blockIdx.x; t < p.n_tasks; t += gridDim.x) {
-    const Task tk = decode_task<MASK>(t, p);
+  SegIter<MASK> it(p);
+  Seg sg;
+  while (it.next(p, sg)) {
+    const Task tk = decode_task<MASK>(sg.t, p);
     if (!tk.live[hh]) continue;
     const int q0 = tk.q0[hh];
     const int q = q0 + row;
@@ -634,7 +865,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
-    for (int j = 0; j < p.n_kv; ++j) {
+    for (int j = sg.kv0; j < sg.kv1; ++j) {
       const int cls = tile_class<MASK>(q0, j, p);
       if (cls == 0) continue;
       if (!warp_wait(bars.s_full(hh), s_par, ctl, j)) return;
@@ -710,6 +941,16 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
           tmem_st32(t_o + ch * 32, ov);
         }
       }
+      // Alternate with the other warpgroup: on tiles that both Q tiles use,
+      // warpgroup 0 runs its exponentials first, then warpgroup 1, then
+      // warpgroup 0 on the next such tile. The two then never compete for
+      // the exp unit, and the tensor core works on one Q tile while the
+      // other's softmax runs.
+      const bool paired = tk.live[1 - hh] && tile_class<MASK>(tk.q0[1 - hh], j, p) != 0;
+      if (paired && (hh == 1 || n_pair > 0)) {
+        const uint32_t par = hh == 1 ? (n_pair & 1u) : ((n_pair - 1u) & 1u);
+        if (!warp_wait(bars.turn(hh), par, ctl, j)) return;
+      }
       const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
       const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
       float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
@@ -733,6 +974,10 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.p_full(hh, part));
       }
+      if (paired) {
+        if (lane == 0) mbar_arrive(bars.turn(1 - hh));
+        ++n_pair;
+      }
       const float2 sa = __fadd2_rn(sum4[0], sum4[1]), sb = __fadd2_rn(sum4[2], sum4[3]);
       l += (sa.x + sa.y) + (sb.x + sb.y);
       first = false;
@@ -741,6 +986,10 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return;
     o_par ^= 1u;
     tc_fence_after();
+    if (MASK == kMaskNone && p.split && (sg.kv0 > 0 || sg.kv1 < p.n_kv)) {
+      if (!partial_epilogue<D>(p, bars, sg, tk, hh, row, t_o, m_ref, l, ctl)) return;
+      continue;
+    }
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     const bool row_ok = q < p.Nq;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
@@ -799,6 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bars.o_empty(h), 4);
     }
     mbar_init(bars.done(), 1);
+    mbar_init(bars.turn(0), 4);
+    mbar_init(bars.turn(1), 4);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bars.k_full(s), 1);
       mbar_init(bars.k_empty(s), 1);
@@ -829,12 +1080,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // warpgroup 0 needs few registers; the softmax warpgroups take them
     set_max_regs_dec<kRegsControl>();
     if (warp == 0) {
-      if (lane == 0) loader_role<D, MASK>(p, sbase, bars, ctl);
-      __syncwarp();
+      loader_role<D, MASK>(p, sbase, bars, ctl);    // whole warp, elected lane issues
     } else if (warp == 1) {
-      if (lane == 0) mma_role<D, MASK>(p, sbase, bars, tmem, ctl);
-      __syncwarp();
+      mma_role<D, MASK>(p, sbase, bars, tmem, ctl);  // whole warp, elected lane issues
     }
+    __syncwarp();
   } else {
     set_max_regs_inc<kRegsSoftmax>();
     softmax_role<D, MASK>(p, bars, tmem, ctl);

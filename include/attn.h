@@ -44,8 +44,13 @@
  *
  * Execution: every call only enqueues work on a CUDA stream (the one set by
  * attn_set_stream for the calling thread, or attn_params_ex.stream) and
- * returns; it launches exactly one kernel and allocates nothing per call. The
- * library keeps one lazily allocated device status word per device.
+ * returns; it launches exactly one kernel. The library keeps one lazily
+ * allocated device status word per device, and for unmasked problems whose
+ * work is split across CTAs (see attn_params_ex.schedule) a workspace for
+ * partial results: the caller's (attn_params_ex.workspace) or else one per
+ * device, allocated on first need and grown when a larger one is needed.
+ * Calls that use the library's workspace must not overlap on the device
+ * (e.g. on two streams at once); give each concurrent stream its own.
  * Device-side failures (a bounded wait that ran out) are reported by
  * attn_get_device_status() after the caller synchronises the stream.
  *
@@ -63,7 +68,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 typedef enum {
   ATTN_MASK_NONE = 0,
@@ -110,6 +115,14 @@ typedef struct attn_params_ex {
                       0 otherwise */
   void* ev_start;  /* optional cudaEvent_t recorded right before the kernel */
   void* ev_stop;   /* optional cudaEvent_t recorded right after the kernel */
+  int schedule;    /* work split over the persistent CTAs: 0 = automatic,
+                      1 = whole (batch, head, 256-query) tasks round robin,
+                      2 = equal shares of K/V tiles, a task cut between CTAs
+                          merged by its last part (ATTN_MASK_NONE only) */
+  void* workspace; /* optional device buffer for schedule 2, zero-filled
+                      before its first use (later calls leave it reusable);
+                      NULL = the library's own */
+  uint64_t workspace_bytes; /* size of `workspace` */
 } attn_params_ex;
 
 /* Fill *p with defaults (zero pointers and sizes, dilation 1, contiguous). */
@@ -149,6 +162,10 @@ const char* attn_last_error(void);
 /* Number of SMs the persistent grid would use on the current device, or a
  * negative attn_status on failure. */
 int attn_device_sm_count(void);
+
+/* Bytes of workspace the call described by *p needs on the current device (0
+ * if its schedule splits no task), or a negative attn_status. */
+int64_t attn_workspace_bytes(const attn_params_ex* p);
 
 /* Free the library's per-device state (status words). Later calls re-create it. */
 void attn_shutdown(void);

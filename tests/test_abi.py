@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.attn_params_size() == ctypes.sizeof(_lib.AttnParamsEx)
-    assert lib.attn_abi_version() == 1
+    assert lib.attn_abi_version() == 2
 
 
 def test_error_strings(lib):
@@ -70,6 +70,8 @@ BAD = [
     ("misaligned_k", dict(k=(1 << 20) + 8), _lib.ATTN_ERR_MISALIGNED),
     ("misaligned_lse", dict(lse=(1 << 20) + 2), _lib.ATTN_ERR_MISALIGNED),
     ("neg_ctas", dict(num_ctas=-1), _lib.ATTN_ERR_INVALID_ARG),
+    ("schedule3", dict(schedule=3), _lib.ATTN_ERR_INVALID_ARG),
+    ("misaligned_ws", dict(workspace=(1 << 20) + 4), _lib.ATTN_ERR_MISALIGNED),
 ]
 
 

@@ -220,3 +220,64 @@ def test_bounded_wait_reports_timeout(E):
     _status_ok(E)
     ref_o, ref_lse = oracle.attention(to_f64(q), to_f64(k), to_f64(v), scale=0.125)
     check(o, lse, ref_o, ref_lse)
+
+
+@pytest.mark.parametrize("num_ctas", [2, 3, 5, 13, 0])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("N", [300, 1000])
+def test_split_schedule(E, num_ctas, d, N):
+    """Equal shares of K/V tiles per CTA: tasks cut between CTAs are merged by
+    their last part (ragged Nk included: 300 and 1000 are not multiples of 128)."""
+    q, k, v = make_qkv(1, 3, N, N, d, 1.0, 20 + num_ctas + d)
+    o, lse = E.attn_fwd(q.cuda(), k.cuda(), v.cuda(), num_ctas=num_ctas, schedule=2)
+    _status_ok(E)
+    ref_o, ref_lse = oracle.attention(to_f64(q), to_f64(k), to_f64(v), scale=1 / math.sqrt(d))
+    check(o, lse, ref_o, ref_lse)
+
+
+def test_split_many_parts_per_task(E):
+    """One head, two Q pairs over many CTAs: every task is cut into ~10 parts."""
+    q, k, v = make_qkv(1, 1, 512, 4096, 64, 1.0, 31)
+    o, lse = E.attn_fwd(q.cuda(), k.cuda(), v.cuda(), num_ctas=20, schedule=2)
+    _status_ok(E)
+    ref_o, ref_lse = oracle.attention(to_f64(q), to_f64(k), to_f64(v), scale=0.125)
+    check(o, lse, ref_o, ref_lse)
+
+
+def test_split_repeated_calls_reuse_workspace(E):
+    """Consecutive calls share the library's workspace; per-call tags keep the
+    arrival counts of one call from leaking into the next."""
+    q, k, v = (t.cuda() for t in make_qkv(2, 2, 700, 700, 64, 1.0, 32))
+    ref = None
+    for _ in range(5):
+        o, lse = E.attn_fwd(q, k, v, num_ctas=7, schedule=2)
+        _status_ok(E)
+        if ref is None:
+            ref = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o, ref[0]) and torch.equal(lse, ref[1])
+    ref_o, ref_lse = oracle.attention(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()),
+                                      scale=0.125)
+    check(ref[0], ref[1], ref_o, ref_lse)
+
+
+def test_split_caller_workspace(E):
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 777, 900, 128, 1.0, 33))
+    nbytes = E.workspace_bytes(1, 2, 777, 900, 128, num_ctas=5, schedule=2)
+    assert nbytes > 0
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        o, lse = E.attn_fwd(q, k, v, num_ctas=5, schedule=2, workspace=ws)
+        _status_ok(E)
+    ref_o, ref_lse = oracle.attention(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()),
+                                      scale=1 / math.sqrt(128))
+    check(o, lse, ref_o, ref_lse)
+
+
+def test_split_and_whole_schedules_agree(E):
+    q, k, v = (t.cuda() for t in make_qkv(2, 5, 4096, 4096, 64, 0.5, 34))
+    o1, l1 = E.attn_fwd(q, k, v, schedule=1)
+    o2, l2 = E.attn_fwd(q, k, v, schedule=2)
+    _status_ok(E)
+    assert (o1.float() - o2.float()).abs().max().item() <= 1e-2
+    assert (l1 - l2).abs().max().item() <= 1e-3
