@@ -110,6 +110,8 @@ def load(path: str = LIB_PATH):
         lib.attn_params_size.restype = i
         lib.attn_workspace_bytes.argtypes = [ctypes.POINTER(AttnParamsEx)]
         lib.attn_workspace_bytes.restype = ctypes.c_int64
+        lib.attn_fwd_noalloc.argtypes = [ctypes.POINTER(AttnParamsEx)]
+        lib.attn_fwd_noalloc.restype = i
         size = lib.attn_params_size()
         if size != ctypes.sizeof(AttnParamsEx):
             raise ImportError(f"attn_params_ex layout mismatch: library {size} bytes, "

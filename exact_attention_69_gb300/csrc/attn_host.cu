@@ -465,3 +465,135 @@ int64_t attn_workspace_bytes(const attn_params_ex* p) {
 int attn_params_size(void) { return static_cast<int>(sizeof(attn_params_ex)); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-alloc entry point
+//
+// attn_fwd_noalloc: for callers that cannot allocate device memory at all --
+// code running where cudaMalloc is forbidden or unavailable (inside a memory
+// pool's own bookkeeping, a custom allocator, an embedded runtime that owns
+// every allocation), or that must not allocate lazily on a first call. It
+// runs the split-schedule unmasked forward pass with all of its scratch (the
+// partial results of cut tasks, their arrival words and the device status
+// word) in one fixed, file-scope device array, so it calls no cudaMalloc,
+// cudaFree or other allocating routine.
+namespace {
+
+// Fixed scratch of the no-alloc entry point. Every GPU on which the library's
+// device code is loaded holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t{48} << 20;
+constexpr size_t kNoAllocStatusBytes = 256;  // device status word at the front
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sm_count = 0;
+  uint32_t epoch = 0;                // tag of the last call on this device
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: the device address of the
+// scratch array (the symbol name itself is only a host-side stand-in).
+int noalloc_setup(NoAllocDevice** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (d.scratch == nullptr) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(ATTN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                  dev, major, minor);
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    d.sm_count = sms;
+    d.scratch = static_cast<unsigned char*>(ptr);
+  }
+  *out = &d;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const attn_params_ex* p) {
+  t_err[0] = 0;
+  Checked c;
+  int rc = validate(p, &c);
+  if (rc != ATTN_OK) return rc;
+  if (p->mask_kind != ATTN_MASK_NONE)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_noalloc computes unmasked attention only");
+  if (p->workspace != nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_fwd_noalloc uses its own fixed scratch; workspace must be NULL");
+  if ((rc = get_encoder()) != ATTN_OK) return rc;
+  NoAllocDevice* nd = nullptr;
+  if ((rc = noalloc_setup(&nd)) != ATTN_OK) return rc;
+
+  attn_params_ex split = *p;
+  split.schedule = 2;
+  Plan pl;
+  if ((rc = make_plan(&split, nd->sm_count, &pl)) != ATTN_OK) return rc;
+  const size_t need = kNoAllocStatusBytes + pl.ws_bytes();
+  if (need > kNoAllocScratchBytes)
+    return fail(ATTN_ERR_INVALID_ARG,
+                "this problem needs %zu bytes of scratch; attn_fwd_noalloc has %zu (use attn_fwd_ex)",
+                need, kNoAllocScratchBytes);
+
+  attn::KernelParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  const int box_cols = p->d >= 64 ? 64 : 32;
+  const CUtensorMapSwizzle swz = p->d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if ((rc = encode_map(&kp.tm_q, p->q, p->d, p->Nq, p->H, p->B, c.qs, box_cols, swz, "q")) != ATTN_OK ||
+      (rc = encode_map(&kp.tm_k, p->k, p->d, p->Nk, p->H, p->B, c.ks, box_cols, swz, "k")) != ATTN_OK ||
+      (rc = encode_map(&kp.tm_v, p->v, p->d, p->Nk, p->H, p->B, c.vs, box_cols, swz, "v")) != ATTN_OK)
+    return rc;
+  kp.o = p->o;
+  kp.lse = p->lse;
+  kp.o_sb = c.os[0];
+  kp.o_sh = c.os[1];
+  kp.o_sn = c.os[2];
+  kp.B = p->B;
+  kp.H = p->H;
+  kp.Nq = p->Nq;
+  kp.Nk = p->Nk;
+  kp.c = p->scale * 1.4426950408889634f;
+  kp.n_qpairs = pl.n_qpairs;
+  kp.n_kv = pl.n_kv;
+  kp.n_tasks = pl.n_tasks;
+  kp.split = pl.split;
+  kp.units = pl.units;
+  kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
+  kp.inject = p->inject;
+  // Layout of the scratch: status word, partial results, arrival words. The
+  // arrival words carry each call's tag, so nothing has to be cleared between
+  // calls (the array starts zeroed, and tag 0 is never used).
+  kp.status = reinterpret_cast<uint32_t*>(nd->scratch);
+  if (pl.split) {
+    kp.ws_part = reinterpret_cast<float*>(nd->scratch + kNoAllocStatusBytes);
+    kp.ws_count = reinterpret_cast<unsigned long long*>(nd->scratch + kNoAllocStatusBytes +
+                                                         align256(pl.part_bytes));
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (++nd->epoch == 0) nd->epoch = 1;
+    kp.epoch = nd->epoch;
+  }
+  cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
+  cudaError_t e;
+  if (p->ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_start), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(start)");
+  switch (p->d) {
+    case 32: e = attn::launch_d32(kp, attn::kMaskNone, pl.grid, s); break;
+    case 64: e = attn::launch_d64(kp, attn::kMaskNone, pl.grid, s); break;
+    default: e = attn::launch_d128(kp, attn::kMaskNone, pl.grid, s); break;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (p->ev_stop && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_stop), s)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord(stop)");
+  return ATTN_OK;
+}

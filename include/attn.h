@@ -177,6 +177,32 @@ int attn_abi_version(void);
  * copy of the struct layout). */
 int attn_params_size(void);
 
+/*
+ * attn_fwd_noalloc: attn_fwd_ex for callers that cannot allocate device
+ * memory -- code that runs where cudaMalloc is forbidden or unavailable (an
+ * allocator's or memory pool's own internals, an embedded runtime that owns
+ * every allocation) or that must never allocate lazily on a first call. The
+ * pages describe no such entry point; it has no counterpart there.
+ *
+ * Computes the unmasked forward pass (mask_kind must be ATTN_MASK_NONE,
+ * workspace NULL) with the split schedule, keeping every piece of scratch in
+ * one fixed 48 MiB device array inside the library, which each GPU that loads
+ * the library holds until the process exits. It calls no cudaMalloc,
+ * cudaFree or other allocating routine. The caller passes inputs and outputs
+ * as for attn_fwd_ex.
+ *  - The first call on a device looks up the array's device address for that
+ *    device (cudaGetSymbolAddress); make that first call before any stream
+ *    capture.
+ *  - A problem that needs more scratch than the array holds is rejected with
+ *    ATTN_ERR_INVALID_ARG and a message giving both sizes.
+ *  - All calls on a device share its array and each overwrites what the last
+ *    one left. Calls that overlap on the GPU (e.g. on two streams at once)
+ *    race and give wrong results: serialise them.
+ *  - A device-side wait that runs out is recorded only in the array's own
+ *    status word, which attn_get_device_status does not read.
+ */
+int attn_fwd_noalloc(const attn_params_ex* p);
+
 #ifdef __cplusplus
 }
 #endif
