@@ -52,6 +52,8 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
 
+constexpr int64_t kMinSplitUnits = 4;
+
 // How a call's work is laid out over the persistent CTAs.
 struct Plan {
   int grid = 0;
@@ -74,7 +76,10 @@ int make_plan(const attn_params_ex* p, int sm_count, Plan* pl) {
   pl->split = p->schedule == 2 ||
               (p->schedule == 0 && p->mask_kind == ATTN_MASK_NONE && pl->n_tasks % ctas != 0);
   if (pl->split) {
-    pl->grid = static_cast<int>(pl->units < ctas ? pl->units : ctas);
+    // at least kMinSplitUnits K/V tiles per CTA: fewer, larger parts to merge
+    const int64_t by_units = (pl->units + kMinSplitUnits - 1) / kMinSplitUnits;
+    pl->grid = static_cast<int>(by_units < ctas ? by_units : ctas);
+    if (pl->grid > attn::kMaxSplitCtas) pl->grid = attn::kMaxSplitCtas;
     pl->part_bytes = static_cast<size_t>(pl->grid) * 2 * 2 * 128 * (p->d + 2) * sizeof(float);
     pl->count_bytes = static_cast<size_t>(pl->n_tasks) * 2 * 4 * sizeof(unsigned long long);
   } else {

@@ -17,7 +17,8 @@ constexpr int kRegsSoftmax = 216;  // registers per thread of warpgroups 1-2 aft
 // 128 * kRegsControl + 256 * kRegsSoftmax must not exceed 384 * 168 (the launch's registers)
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
 constexpr int kThreads = kWarps * 32;
-constexpr float kRescaleLog2 = 8.0f;  // keep a stale row maximum until the true one exceeds it by 2^8
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kMaxSplitCtas = 256;  // largest grid of the split schedule (its range table lives in shared memory)  // keep a stale row maximum until the true one exceeds it by 2^8
 
 // Mask specialisations (the C-ABI's NA2D splits into clamp and wrap here).
 enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskNaClamp = 2, kMaskNaWrap = 3 };

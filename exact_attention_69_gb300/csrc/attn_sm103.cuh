@@ -268,7 +268,10 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kBarBytes = 512;
-  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  // first unit of every CTA of a split schedule (kMaxSplitCtas + 1 int64)
+  static constexpr int kOffTbl = kOffBar + kBarBytes;
+  static constexpr int kTblBytes = 8 * (kMaxSplitCtas + 1);
+  static constexpr int kSmemBytes = kOffTbl + kTblBytes + 1024;  // + alignment slack
   static constexpr uint32_t kLayout = D >= 64 ? 2u : 4u;
   static constexpr uint32_t kIdescS = make_idesc(kBM, kBN, false);
   static constexpr uint32_t kIdescO = make_idesc(kBM, D, true);
@@ -482,12 +485,15 @@ __host__ __device__ __forceinline__ int64_t unit_lo(int64_t units, int ctas, int
   return static_cast<int64_t>(c) * units / ctas;
 }
 
-// The CTA whose unit range holds unit u.
-__host__ __device__ __forceinline__ int cta_of_unit(int64_t units, int ctas, int64_t u) {
-  int c = static_cast<int>(u * ctas / units);
-  while (c > 0 && unit_lo(units, ctas, c) > u) --c;
-  while (c + 1 < ctas && unit_lo(units, ctas, c + 1) <= u) ++c;
-  return c;
+// The CTA whose unit range holds unit u, given the table lo[c] = first unit of
+// CTA c (lo[ctas] = units): a binary search, no 64-bit division.
+__device__ __forceinline__ int cta_of_unit(const int64_t* lo, int ctas, int64_t u) {
+  int a = 0, b = ctas - 1;  // lo[a] <= u < lo[b + 1]
+  while (a < b) {
+    const int m = (a + b + 1) >> 1;
+    if (lo[m] <= u) a = m; else b = m - 1;
+  }
+  return a;
 }
 
 template <int MASK>
@@ -495,10 +501,10 @@ struct SegIter {
   int64_t u, hi;
   int t_rr;
   bool first;
-  __device__ __forceinline__ explicit SegIter(const KernelParams& p) : first(true) {
+  __device__ __forceinline__ SegIter(const KernelParams& p, const int64_t* lo) : first(true) {
     if (MASK == kMaskNone && p.split) {
-      u = unit_lo(p.units, gridDim.x, blockIdx.x);
-      hi = unit_lo(p.units, gridDim.x, blockIdx.x + 1);
+      u = lo[blockIdx.x];
+      hi = lo[blockIdx.x + 1];
     } else {
       t_rr = blockIdx.x;
     }
@@ -524,18 +530,86 @@ struct SegIter {
   }
 };
 
+// Grid coordinates of query token q and the starts of its clamped window.
+__host__ __device__ __forceinline__ void na_query_coords(const KernelParams& p, int q, int& qy,
+                                                         int& qx, int& wy, int& wx) {
+  qy = q / p.grid_w;
+  qx = q - qy * p.grid_w;
+  const int half = p.window >> 1;
+  wy = min(max(qy - half, 0), p.grid_h - p.window);
+  wx = min(max(qx - half, 0), p.grid_w - p.window);
+}
+
+// Sets bits [lo, hi) (0 <= lo <= hi <= 128) of a 128-bit mask.
+__host__ __device__ __forceinline__ void set_bits(uint32_t (&bits)[4], int lo, int hi) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int a = max(lo - 32 * w, 0), b = min(hi - 32 * w, 32);
+    if (a < b) {
+      const uint32_t upto = b >= 32 ? 0xffffffffu : ((1u << b) - 1u);
+      bits[w] |= upto & ~((1u << a) - 1u);
+    }
+  }
+}
+
+// Allowed keys of query (qy, qx) in the K/V tile starting at key k0, as bits
+// of a 128-bit mask (bit i: key k0 + i). Clamp: rows [wy, wy + w), columns
+// [wx, wx + w). Wrap: rows and columns (c - w/2 + t) mod G, t in [0, w).
+template <bool WRAP>
+__host__ __device__ __forceinline__ void na_tile_bits(const KernelParams& p, int k0, int qy, int qx, int wy,
+                                             int wx, uint32_t (&bits)[4]) {
+  const int G_h = p.grid_h, G_w = p.grid_w, w = p.window, half = w >> 1;
+  bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+  const int nvalid = min(kBN, p.Nk - k0);
+  int ky = k0 / G_w;
+  int kx0 = k0 - ky * G_w;
+  // circular column window: [ca, ca + w) mod G_w
+  int ca = qx - half;
+  if (ca < 0) ca += G_w;
+  for (int i = 0; i < nvalid; ++ky) {
+    const int len = min(G_w - kx0, nvalid - i);  // this row's columns [kx0, kx0 + len)
+    bool row_ok;
+    if (!WRAP) {
+      row_ok = static_cast<unsigned>(ky - wy) < static_cast<unsigned>(w);
+    } else {
+      int dy = ky - qy + half;
+      dy += dy < 0 ? G_h : 0;
+      dy -= dy >= G_h ? G_h : 0;
+      row_ok = dy < w;
+    }
+    if (row_ok) {
+      const int base = i - kx0;  // bit of column 0 of this row
+      if (!WRAP) {
+        const int lo = max(wx, kx0), hi = min(wx + w, kx0 + len);
+        if (lo < hi) set_bits(bits, base + lo, base + hi);
+      } else {
+        const int e1 = min(ca + w, G_w);
+        int lo = max(ca, kx0), hi = min(e1, kx0 + len);
+        if (lo < hi) set_bits(bits, base + lo, base + hi);
+        if (ca + w > G_w) {  // the window wraps past the last column
+          lo = kx0;
+          hi = min(ca + w - G_w, kx0 + len);
+          if (lo < hi) set_bits(bits, base + lo, base + hi);
+        }
+      }
+    }
+    i += len;
+    kx0 = 0;
+  }
+}
+
 // ---------------------------------------------------------------- roles
 
 template <int D, int MASK>
 __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& bars,
-                            const Ctl& ctl) {
+                            const int64_t* cta_lo, const Ctl& ctl) {
   using C = Cfg<D>;
   uint32_t q_it = 0, k_it = 0, v_it = 0;
   int q_armed = -1, k_armed[C::kKStages], v_armed[C::kVStages];
   for (int s = 0; s < C::kKStages; ++s) k_armed[s] = -1;
   for (int s = 0; s < C::kVStages; ++s) v_armed[s] = -1;
   bool injected = false;
-  SegIter<MASK> it(p);
+  SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
@@ -627,11 +701,11 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, 
 
 template <int D, int MASK>
 __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars, uint32_t tmem,
-                         const Ctl& ctl) {
+                         const int64_t* cta_lo, const Ctl& ctl) {
   using C = Cfg<D>;
   uint32_t q_it = 0, k_it = 0, v_it = 0;
   uint32_t p_par[2] = {0, 0}, o_it[2] = {0, 0};
-  SegIter<MASK> it(p);
+  SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
@@ -737,18 +811,23 @@ __device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t 
 //   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
 //   LSE = ln 2 (M + log2 L).
 // No CTA waits for another: the last part to finish does the merge.
+// A part is stored column-group major ([d/4][128 rows] of float4, then m[128],
+// l[128]) so that every warp access is one contiguous 512-byte run.
 // False: the CTA is aborting.
 template <int D>
 __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars& bars, const Seg& sg,
-                                 const Task& tk, int hh, int row, uint32_t t_o, float m_ref,
-                                 float l, const Ctl& ctl) {
+                                              const Task& tk, int hh, int row, uint32_t t_o,
+                                              float m_ref, float l, const int64_t* cta_lo,
+                                              const Ctl& ctl) {
   const int lane = threadIdx.x & 31;
   const int quarter = row >> 5;
+  const int ctas = gridDim.x;
   auto slot_of = [&](int cta, bool head) {
     return p.ws_part +
            static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2);
   };
   float* mine = slot_of(blockIdx.x, sg.head);
+  float4* mine4 = reinterpret_cast<float4*>(mine);
 #pragma unroll
   for (int ch = 0; ch < D / 32; ++ch) {
     uint32_t ov[32];
@@ -758,19 +837,19 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
       __syncwarp();
       if (lane == 0) mbar_arrive(bars.o_empty(hh));
     }
-    float4* dst = reinterpret_cast<float4*>(mine + row * D + ch * 32);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      dst[i] = make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                           __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+      mine4[(ch * 8 + i) * 128 + row] =
+          make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                      __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
   }
   mine[128 * D + row] = m_ref;
   mine[128 * D + 128 + row] = l;
   __threadfence();
   __syncwarp();
   const int64_t t_first = static_cast<int64_t>(sg.t) * p.n_kv;
-  const int c_lo = cta_of_unit(p.units, gridDim.x, t_first);
-  const int c_hi = cta_of_unit(p.units, gridDim.x, t_first + p.n_kv - 1);
+  const int c_lo = cta_of_unit(cta_lo, ctas, t_first);
+  const int c_hi = cta_of_unit(cta_lo, ctas, t_first + p.n_kv - 1);
   uint32_t n = 0;
   if (lane == 0)
     n = arrive_part(p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter, p.epoch, ctl);
@@ -778,48 +857,72 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   if (n != static_cast<uint32_t>(c_hi - c_lo + 1)) return !*ctl.abort;
   __threadfence();
   const int q = tk.q0[hh] + row;
+  // a part of CTA c is that CTA's first segment iff its range starts in this task
+  auto part = [&](int c) -> const float* { return slot_of(c, cta_lo[c] >= t_first); };
   float M = -CUDART_INF_F;
-  for (int c = c_lo; c <= c_hi; ++c) {
-    const float* sl = slot_of(c, unit_lo(p.units, gridDim.x, c) >= t_first);
-    M = fmaxf(M, __ldcg(sl + 128 * D + row));
+  for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
+    float mi[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      mi[u] = c0 + u <= c_hi ? __ldcg(part(c0 + u) + 128 * D + row) : -CUDART_INF_F;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) M = fmaxf(M, mi[u]);
   }
   float L = 0.f;
-  for (int c = c_lo; c <= c_hi; ++c) {
-    const float* sl = slot_of(c, unit_lo(p.units, gridDim.x, c) >= t_first);
-    const float mi = __ldcg(sl + 128 * D + row);
-    if (mi != -CUDART_INF_F) L += ex2(mi - M) * __ldcg(sl + 128 * D + 128 + row);
+  for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
+    float mi[8], li[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = c0 + u <= c_hi;
+      const float* sl = part(in ? c0 + u : c_hi);
+      mi[u] = in ? __ldcg(sl + 128 * D + row) : -CUDART_INF_F;
+      li[u] = in ? __ldcg(sl + 128 * D + 128 + row) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (mi[u] != -CUDART_INF_F) L += ex2(mi[u] - M) * li[u];
   }
   const float inv_L = L > 0.f ? 1.f / L : 0.f;
   const bool row_ok = q < p.Nq;
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
                         static_cast<int64_t>(q) * p.o_sn;
+  // O in chunks of 32 columns; four parts' rows are loaded together.
 #pragma unroll 1
-  for (int ch = 0; ch < D / 16; ++ch) {
-    float acc[16];
+  for (int ch = 0; ch < D / 32; ++ch) {
+    float acc[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
 #pragma unroll 1
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const float* sl = slot_of(c, unit_lo(p.units, gridDim.x, c) >= t_first);
-      const float mi = __ldcg(sl + 128 * D + row);
-      const float w = mi == -CUDART_INF_F ? 0.f : ex2(mi - M);
-      const float4* src = reinterpret_cast<const float4*>(sl + row * D + ch * 16);
+    for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
+      float4 v[4][8];
+      float wgt[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 v = __ldcg(src + i);
-        acc[4 * i] += w * v.x;
-        acc[4 * i + 1] += w * v.y;
-        acc[4 * i + 2] += w * v.z;
-        acc[4 * i + 3] += w * v.w;
+      for (int u = 0; u < 4; ++u) {
+        const bool in = c0 + u <= c_hi;
+        const float* sl = part(in ? c0 + u : c_hi);
+        const float mi = __ldcg(sl + 128 * D + row);
+        wgt[u] = (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
+        const float4* src = reinterpret_cast<const float4*>(sl);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 128 + row);
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[4 * i] += wgt[u] * v[u][i].x;
+          acc[4 * i + 1] += wgt[u] * v[u][i].y;
+          acc[4 * i + 2] += wgt[u] * v[u][i].z;
+          acc[4 * i + 3] += wgt[u] * v[u][i].w;
+        }
     }
     if (row_ok) {
-      uint32_t packed[8];
+      uint32_t packed[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) packed[i] = pack_bf16(acc[2 * i] * inv_L, acc[2 * i + 1] * inv_L);
-      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 16);
+      for (int i = 0; i < 16; ++i) packed[i] = pack_bf16(acc[2 * i] * inv_L, acc[2 * i + 1] * inv_L);
+      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+      for (int i = 0; i < 4; ++i)
         dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
     }
   }
@@ -832,7 +935,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
 
 template <int D, int MASK>
 __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t tmem,
-                             const Ctl& ctl) {
+                             const int64_t* cta_lo, const Ctl& ctl) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hh = (warp - 4) >> 2;          // which Q tile of the pair
@@ -846,7 +949,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
   uint32_t n_pair = 0;  // tiles both Q tiles used so far: the exp2 phases of the
                         // two warpgroups alternate on them (0 first, then 1)
 
-  SegIter<MASK> it(p);
+  SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
@@ -855,13 +958,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     const int q = q0 + row;
     // neighbourhood: this query's grid coordinates and clamped window starts
     int qy = 0, qx = 0, wy = 0, wx = 0;
-    if (MASK == kMaskNaClamp || MASK == kMaskNaWrap) {
-      qy = q / p.grid_w;
-      qx = q - qy * p.grid_w;
-      const int half = p.window >> 1;
-      wy = min(max(qy - half, 0), p.grid_h - p.window);
-      wx = min(max(qx - half, 0), p.grid_w - p.window);
-    }
+    if (MASK == kMaskNaClamp || MASK == kMaskNaWrap) na_query_coords(p, q, qy, qx, wy, wx);
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
@@ -885,30 +982,15 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
           for (int i = 0; i < 128; ++i)
             if (i > lim) s[i] = -CUDART_INF_F;
         } else {
-          const int G_h = p.grid_h, G_w = p.grid_w, w = p.window, half = w >> 1;
-          int ky = k0 / G_w, kx = k0 - ky * G_w;
-          const int nvalid = p.Nk - k0;
+          // The window is a product of a row set and a column set, and a K/V
+          // tile covers whole grid-row segments: build the tile's allowed
+          // keys as a 128-bit mask, one column interval per row segment,
+          // then clear the rest with independent selects.
+          uint32_t bits[4];
+          na_tile_bits<MASK == kMaskNaWrap>(p, k0, qy, qx, wy, wx, bits);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            bool ok;
-            if (MASK == kMaskNaClamp) {
-              ok = static_cast<unsigned>(ky - wy) < static_cast<unsigned>(w) &&
-                   static_cast<unsigned>(kx - wx) < static_cast<unsigned>(w);
-            } else {
-              int dy = ky - qy + half;
-              dy += (dy < 0) ? G_h : 0;
-              dy -= (dy >= G_h) ? G_h : 0;
-              int dx = kx - qx + half;
-              dx += (dx < 0) ? G_w : 0;
-              dx -= (dx >= G_w) ? G_w : 0;
-              ok = dy < w && dx < w;
-            }
-            if (!ok || i >= nvalid) s[i] = -CUDART_INF_F;
-            if (++kx == G_w) {
-              kx = 0;
-              ++ky;
-            }
-          }
+          for (int i = 0; i < 128; ++i)
+            if (((bits[i >> 5] >> (i & 31)) & 1u) == 0u) s[i] = -CUDART_INF_F;
         }
       }
       // row maximum: 8 independent chains of 3-input max
@@ -987,7 +1069,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     o_par ^= 1u;
     tc_fence_after();
     if (MASK == kMaskNone && p.split && (sg.kv0 > 0 || sg.kv1 < p.n_kv)) {
-      if (!partial_epilogue<D>(p, bars, sg, tk, hh, row, t_o, m_ref, l, ctl)) return;
+      if (!partial_epilogue<D>(p, bars, sg, tk, hh, row, t_o, m_ref, l, cta_lo, ctl)) return;
       continue;
     }
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
@@ -1036,6 +1118,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   Bars bars{sbase + C::kOffBar, C::kKStages, C::kVStages};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * bars.count());
   volatile uint32_t* abort_flag = tmem_slot + 1;
+  int64_t* cta_lo = reinterpret_cast<int64_t*>(smem + C::kOffTbl);
+  if (MASK == kMaskNone && p.split)
+    for (int c = threadIdx.x; c <= static_cast<int>(gridDim.x); c += blockDim.x)
+      cta_lo[c] = unit_lo(p.units, gridDim.x, c);  // ordered by the __syncthreads below
 
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full(), 1);
@@ -1080,14 +1166,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // warpgroup 0 needs few registers; the softmax warpgroups take them
     set_max_regs_dec<kRegsControl>();
     if (warp == 0) {
-      loader_role<D, MASK>(p, sbase, bars, ctl);    // whole warp, elected lane issues
+      loader_role<D, MASK>(p, sbase, bars, cta_lo, ctl);    // whole warp, elected lane issues
     } else if (warp == 1) {
-      mma_role<D, MASK>(p, sbase, bars, tmem, ctl);  // whole warp, elected lane issues
+      mma_role<D, MASK>(p, sbase, bars, tmem, cta_lo, ctl);  // whole warp, elected lane issues
     }
     __syncwarp();
   } else {
     set_max_regs_inc<kRegsSoftmax>();
-    softmax_role<D, MASK>(p, bars, tmem, ctl);
+    softmax_role<D, MASK>(p, bars, tmem, cta_lo, ctl);
   }
 
   tc_fence_before();

@@ -38,3 +38,20 @@ extern "C" void decode_task_host(int mask, int t, int B, int H, int Nq, int* out
   out[1] = k.h;
   out[2] = k.q0[0];
 }
+
+// The in-tile neighbourhood mask of query q for the K/V tile starting at key
+// k0: bit i set iff key k0 + i is allowed.
+extern "C" void na_bits_host(int wrap, int q, int k0, int N, int grid_h, int grid_w, int window,
+                             unsigned* out) {
+  attn::KernelParams p{};
+  p.Nq = p.Nk = N;
+  p.grid_h = grid_h;
+  p.grid_w = grid_w;
+  p.window = window;
+  int qy, qx, wy, wx;
+  attn::dev::na_query_coords(p, q, qy, qx, wy, wx);
+  uint32_t bits[4];
+  if (wrap) attn::dev::na_tile_bits<true>(p, k0, qy, qx, wy, wx, bits);
+  else attn::dev::na_tile_bits<false>(p, k0, qy, qx, wy, wx, bits);
+  for (int i = 0; i < 4; ++i) out[i] = bits[i];
+}

@@ -34,6 +34,7 @@ def plan(tmp_path_factory):
     lib.tile_class_host.argtypes = [ctypes.c_int] * 8
     lib.tile_class_host.restype = ctypes.c_int
     lib.decode_task_host.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
+    lib.na_bits_host.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_uint)]
     return lib
 
 
@@ -81,3 +82,25 @@ def test_tasks_cover_every_q_tile_once(plan, mask):
     if mask == "causal":  # longest pairs (largest row offset) come first
         plan.decode_task_host(1, 0, B, H, Nq, out)
         assert out[2] == 256 * (n_qpairs - 1)
+
+
+@pytest.mark.parametrize("mode,gh,gw,window", [
+    ("clamp", 64, 64, 7), ("wrap", 64, 64, 7), ("clamp", 5, 5, 3), ("wrap", 5, 5, 3),
+    ("clamp", 13, 29, 7), ("wrap", 13, 29, 7), ("wrap", 24, 50, 9), ("clamp", 30, 160, 9),
+    ("wrap", 39, 39, 39), ("clamp", 12, 20, 1)])
+def test_in_tile_mask_bits_match_oracle_mask(plan, mode, gh, gw, window):
+    """The kernel's in-tile neighbourhood mask, bit for bit, against the oracle
+    twin's allowed-set matrix, for every query and every K/V tile."""
+    N = gh * gw
+    allowed = twin.mask_matrix(N, N, mode, window, 1, (gh, gw))
+    out = (ctypes.c_uint * 4)()
+    rng = np.random.default_rng(0)
+    queries = range(N) if N <= 1600 else rng.choice(N, 400, replace=False)
+    for q in queries:
+        for k0 in range(0, N, 128):
+            plan.na_bits_host(1 if mode == "wrap" else 0, int(q), k0, N, gh, gw, window, out)
+            bits = np.array([(out[i >> 5] >> (i & 31)) & 1 for i in range(128)], dtype=bool)
+            ref = np.zeros(128, dtype=bool)
+            n = min(128, N - k0)
+            ref[:n] = allowed[q, k0:k0 + n]
+            assert np.array_equal(bits, ref), (q, k0)
