@@ -95,6 +95,31 @@ def count_flops(w):
     return per_pair * 128 * 128 * float(tiles), per_pair * float(m.sum())
 
 
+# ------------------------------------------------------------------ multi-rank
+
+def max_over_ranks(ms: float, dist_mod, device) -> float:
+    """The slowest rank's time (every rank gets it); `ms` itself on one rank."""
+    if dist_mod is None or not dist_mod.is_available() or not dist_mod.is_initialized():
+        return ms
+    if dist_mod.get_world_size() == 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, steps: int, ms_total: float) -> float:
+    """All ranks' work (each rank runs its own instance: weak scaling) over the
+    slowest rank's time."""
+    return world * flops_per_rank_step * steps / (ms_total * 1e-3) / 1e12
+
+
+def rank_seed(w, rank: int) -> int:
+    """Each rank draws its own instance of the workload."""
+    return w.seed + 1000 * rank
+
+
 # ------------------------------------------------------------------ environment
 
 def load_peaks():
@@ -292,7 +317,7 @@ def ours_arm(args, w):
     flops_tile, flops_exact = count_flops(w)
     set_bytes = 2 * (2 * w.B * w.H * w.Nq * w.d + 2 * w.B * w.H * w.Nk * w.d) + 4 * w.B * w.H * w.Nq
     n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes))
-    q, k, v = make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.sigma, w.seed + 1000 * rank)
+    q, k, v = make_qkv(w.B, w.H, w.Nq, w.Nk, w.d, w.sigma, rank_seed(w, rank))
     sets = []
     for i in range(n_sets):
         # distinct device buffers per set (same values): no step hits L2 from the last
@@ -355,12 +380,9 @@ def ours_arm(args, w):
         step(i, events=kev[i])
     torch.cuda.synchronize()
     k_ms = [a.elapsed_time(b) for a, b in kev]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist if world > 1 else None, dev)
     ms_step = ms_total / args.steps
-    value = world * flops_tile * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_tile, args.steps, ms_total)
 
     # end to end through the public API: pinned host inputs in, host outputs back
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
@@ -387,13 +409,10 @@ def ours_arm(args, w):
     e1.record(stream)
     torch.cuda.synchronize()
     e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e_ms, dist if world > 1 else None, dev)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
-    e2e = {"value": world * flops_tile * e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+    e2e = {"value": whole_job_tflops(world, flops_tile, e_steps, e_ms), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
 
     if rank != 0:
