@@ -268,6 +268,7 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kBarBytes = 512;
+  static_assert(8 * (13 + 2 * kKStages + 2 * kVStages) + 8 <= kBarBytes, "barrier area");
   // first unit of every CTA of a split schedule (kMaxSplitCtas + 1 int64)
   static constexpr int kOffTbl = kOffBar + kBarBytes;
   static constexpr int kTblBytes = 8 * (kMaxSplitCtas + 1);
@@ -276,7 +277,9 @@ struct Cfg {
   static constexpr uint32_t kIdescS = make_idesc(kBM, kBN, false);
   static constexpr uint32_t kIdescO = make_idesc(kBM, D, true);
   static constexpr uint32_t kTmemCols = 512;
+  // S of Q tile h, its bf16 P (written over the first 64 columns of S) and O.
   __host__ __device__ static constexpr uint32_t tm_s(int h) { return 128u * h; }
+  __host__ __device__ static constexpr uint32_t tm_p(int h) { return tm_s(h); }
   __host__ __device__ static constexpr uint32_t tm_o(int h) { return 256u + static_cast<uint32_t>(D) * h; }
 };
 
@@ -292,14 +295,11 @@ struct Bars {
   __device__ uint32_t o_full(int h) const { return base + 64 + 8 * h; }
   __device__ uint32_t o_empty(int h) const { return base + 80 + 8 * h; }
   __device__ uint32_t done() const { return base + 96; }
-  // turn(h): softmax warpgroup h may start the exponentials of its next tile
-  // that both Q tiles use (arrived by the other warpgroup's 4 warps)
-  __device__ uint32_t turn(int h) const { return base + 104 + 8 * h; }
-  __device__ uint32_t k_full(int s) const { return base + 120 + 8 * s; }
-  __device__ uint32_t k_empty(int s) const { return base + 120 + 8 * (kst + s); }
-  __device__ uint32_t v_full(int s) const { return base + 120 + 8 * (2 * kst + s); }
-  __device__ uint32_t v_empty(int s) const { return base + 120 + 8 * (2 * kst + vst + s); }
-  __device__ int count() const { return 15 + 2 * kst + 2 * vst; }
+  __device__ uint32_t k_full(int s) const { return base + 104 + 8 * s; }
+  __device__ uint32_t k_empty(int s) const { return base + 104 + 8 * (kst + s); }
+  __device__ uint32_t v_full(int s) const { return base + 104 + 8 * (2 * kst + s); }
+  __device__ uint32_t v_empty(int s) const { return base + 104 + 8 * (2 * kst + vst + s); }
+  __device__ int count() const { return 13 + 2 * kst + 2 * vst; }
 };
 
 // ------------------------------------------------------------- bounded waits
@@ -690,7 +690,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, 
   using C = Cfg<D>;
   v_tile = opaque(v_tile);
   const uint64_t b0 = smem_desc(v_tile, C::kChunkBytes, 8 * C::kSwizzle, C::kLayout);
-  const uint32_t t_o = tmem + C::tm_o(h), t_p = tmem + C::tm_s(h);
+  const uint32_t t_o = tmem + C::tm_o(h), t_p = tmem + C::tm_p(h);
 #pragma unroll
   for (int k = 0; k < kBN / 32; ++k) {
     const int ks = part * (kBN / 32) + k;
@@ -699,6 +699,9 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, 
   }
 }
 
+// One warp issues both products. P_h overwrites the first half of S_h, so
+// S_h of the next tile follows P V of this one: per tile, P V_h(j) then
+// S_h(j + 1) for each Q tile.
 template <int D, int MASK>
 __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars, uint32_t tmem,
                          const int64_t* cta_lo, const Ctl& ctl) {
@@ -933,6 +936,57 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   return !*ctl.abort;
 }
 
+// Keys of a partial tile (class 2) that the query may not see become -inf.
+template <int MASK>
+__device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams& p, int j, int q,
+                                          int qy, int qx, int wy, int wx) {
+  const uint32_t neg_inf = __float_as_uint(-CUDART_INF_F);
+  const int k0 = j * kBN;
+  if (MASK == kMaskNone || MASK == kMaskCausal) {
+    int lim = p.Nk - 1 - k0;                       // last valid key column
+    if (MASK == kMaskCausal) lim = min(lim, q - k0);
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+      if (i > lim) s[i] = neg_inf;
+  } else {
+    // The window is a product of a row set and a column set, and a K/V
+    // tile covers whole grid-row segments: build the tile's allowed
+    // keys as a 128-bit mask, one column interval per row segment,
+    // then clear the rest with independent selects.
+    uint32_t bits[4];
+    na_tile_bits<MASK == kMaskNaWrap>(p, k0, qy, qx, wy, wx, bits);
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+      if (((bits[i >> 5] >> (i & 31)) & 1u) == 0u) s[i] = neg_inf;
+  }
+}
+
+// Row maximum of a tile (fp32 bit patterns): 8 independent chains of 3-input max.
+__device__ __forceinline__ float row_max128(const uint32_t (&s)[128]) {
+  float mx8[8];
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    mx8[ch] = fmaxf(__uint_as_float(s[ch]), __uint_as_float(s[ch + 8]));
+#pragma unroll
+    for (int i = 16; i < 128; i += 16)
+      mx8[ch] = fmax3(mx8[ch], __uint_as_float(s[ch + i]), __uint_as_float(s[ch + i + 8]));
+  }
+  return fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+}
+
+// O row *= alpha (the accumulated P V of earlier tiles, brought to a new maximum).
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha) {
+#pragma unroll
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t ov[32];
+    tmem_ld32(t_o + ch * 32, ov);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+    tmem_st32(t_o + ch * 32, ov);
+  }
+}
+
 template <int D, int MASK>
 __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t tmem,
                              const int64_t* cta_lo, const Ctl& ctl) {
@@ -944,10 +998,9 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const uint32_t t_s = lane_base + C::tm_s(hh);
   const uint32_t t_o = lane_base + C::tm_o(hh);
+  const uint32_t t_p = lane_base + C::tm_p(hh);
   const float c = p.c;
   uint32_t s_par = 0, o_par = 0;
-  uint32_t n_pair = 0;  // tiles both Q tiles used so far: the exp2 phases of the
-                        // two warpgroups alternate on them (0 first, then 1)
 
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
@@ -962,6 +1015,8 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
+    // P overwrites the first half of S, and each half of P is announced on
+    // its own so that P V starts on the first.
     for (int j = sg.kv0; j < sg.kv1; ++j) {
       const int cls = tile_class<MASK>(q0, j, p);
       if (cls == 0) continue;
@@ -970,39 +1025,11 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(t_s, sr);
+      if (cls == 2) mask_tile<MASK>(sr, p, j, q, qy, qx, wy, wx);
+      const float mx = row_max128(sr);
       float s[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
-      if (cls == 2) {
-        const int k0 = j * kBN;
-        if (MASK == kMaskNone || MASK == kMaskCausal) {
-          int lim = p.Nk - 1 - k0;                       // last valid key column
-          if (MASK == kMaskCausal) lim = min(lim, q - k0);
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i > lim) s[i] = -CUDART_INF_F;
-        } else {
-          // The window is a product of a row set and a column set, and a K/V
-          // tile covers whole grid-row segments: build the tile's allowed
-          // keys as a 128-bit mask, one column interval per row segment,
-          // then clear the rest with independent selects.
-          uint32_t bits[4];
-          na_tile_bits<MASK == kMaskNaWrap>(p, k0, qy, qx, wy, wx, bits);
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (((bits[i >> 5] >> (i & 31)) & 1u) == 0u) s[i] = -CUDART_INF_F;
-        }
-      }
-      // row maximum: 8 independent chains of 3-input max
-      float mx8[8];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        mx8[ch] = fmaxf(s[ch], s[ch + 8]);
-#pragma unroll
-        for (int i = 16; i < 128; i += 16) mx8[ch] = fmax3(mx8[ch], s[ch + i], s[ch + i + 8]);
-      }
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                             fmaxf(mx8[6], mx8[7]));
       const float m_tile = (mx == -CUDART_INF_F) ? -CUDART_INF_F : mx * c;
       const bool grow = m_tile > m_ref + kRescaleLog2;
       float alpha = 1.f;
@@ -1011,34 +1038,13 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
         l *= alpha;
         m_ref = m_tile;
       }
-      // O already holds the previous tiles' P V (their MMAs completed before
-      // this S was committed): bring it to the new maximum before the next P V.
-      if (__any_sync(0xffffffffu, grow && !first)) {
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t ov[32];
-          tmem_ld32(t_o + ch * 32, ov);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32(t_o + ch * 32, ov);
-        }
-      }
-      // Alternate with the other warpgroup: on tiles that both Q tiles use,
-      // warpgroup 0 runs its exponentials first, then warpgroup 1, then
-      // warpgroup 0 on the next such tile. The two then never compete for
-      // the exp unit, and the tensor core works on one Q tile while the
-      // other's softmax runs.
-      const bool paired = tk.live[1 - hh] && tile_class<MASK>(tk.q0[1 - hh], j, p) != 0;
-      if (paired && (hh == 1 || n_pair > 0)) {
-        const uint32_t par = hh == 1 ? (n_pair & 1u) : ((n_pair - 1u) & 1u);
-        if (!warp_wait(bars.turn(hh), par, ctl, j)) return;
-      }
+      // O holds the previous tiles' P V, whose MMAs completed before this S
+      // was committed: bring it to the new maximum before the next P V.
+      if (__any_sync(0xffffffffu, grow && !first)) rescale_o<D>(t_o, alpha);
       const float neg_m = (m_ref == -CUDART_INF_F) ? 0.f : -m_ref;
       const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
       float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
-      // p = 2^(s c - m) in two halves of 64 keys; each half goes to TMEM and is
-      // announced on its own barrier so that P V can start on the first half.
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t pk[32];
@@ -1050,15 +1056,11 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
           sum4[i & 3] = __fadd2_rn(sum4[i & 3], pe);
           pk[i] = pack_bf16(pe.x, pe.y);
         }
-        tmem_st32(t_s + 32 * part, pk);
+        tmem_st32(t_p + 32 * part, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.p_full(hh, part));
-      }
-      if (paired) {
-        if (lane == 0) mbar_arrive(bars.turn(1 - hh));
-        ++n_pair;
       }
       const float2 sa = __fadd2_rn(sum4[0], sum4[1]), sb = __fadd2_rn(sum4[2], sum4[3]);
       l += (sa.x + sa.y) + (sb.x + sb.y);
@@ -1134,8 +1136,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bars.o_empty(h), 4);
     }
     mbar_init(bars.done(), 1);
-    mbar_init(bars.turn(0), 4);
-    mbar_init(bars.turn(1), 4);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bars.k_full(s), 1);
       mbar_init(bars.k_empty(s), 1);
