@@ -789,19 +789,24 @@ drain:
 
 // ------------------------------------------------------------- partial results
 
+// Orders this thread's earlier global writes before, or its later global
+// reads after, a flag observed by another CTA (release / acquire, GPU scope).
+__device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // One arrival on a (task, Q tile) word tagged with this call's epoch; returns
 // the number of parts arrived so far in this call, or 0 if the CAS loop ran
-// past its bound (recorded as a timeout).
+// past its bound (recorded as a timeout). The first attempt assumes this is
+// the call's first arrival, which saves a round trip for the first part.
 __device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t epoch,
                                                 const Ctl& c) {
-  unsigned long long old = atomicAdd(w, 0ull);
+  unsigned long long assumed = static_cast<unsigned long long>(epoch) << 32;
   for (int n = 0; n < (1 << 20); ++n) {
-    const unsigned long long assumed = old;
     const uint32_t cnt = static_cast<uint32_t>(assumed >> 32) == epoch
                              ? static_cast<uint32_t>(assumed) : 0u;
     const unsigned long long nv = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
-    old = atomicCAS(w, assumed, nv);
+    const unsigned long long old = atomicCAS(w, assumed, nv);
     if (old == assumed) return cnt + 1u;
+    assumed = old;
   }
   report_timeout(c, kRoleSoftmax, -2);
   return 0u;
@@ -813,7 +818,9 @@ __device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t 
 // last part of those rows, merge all parts:
 //   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
 //   LSE = ln 2 (M + log2 L).
-// No CTA waits for another: the last part to finish does the merge.
+// No CTA waits for another: the last part to finish does the merge, reading
+// its own O from TMEM (o_empty is arrived only at the end, which costs
+// nothing: the next task's first P V also needs this warpgroup's next P).
 // A part is stored column-group major ([d/4][128 rows] of float4, then m[128],
 // l[128]) so that every warp access is one contiguous 512-byte run.
 // False: the CTA is aborting.
@@ -829,17 +836,17 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     return p.ws_part +
            static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2);
   };
+  auto release_o = [&]() {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars.o_empty(hh));
+  };
   float* mine = slot_of(blockIdx.x, sg.head);
   float4* mine4 = reinterpret_cast<float4*>(mine);
 #pragma unroll
   for (int ch = 0; ch < D / 32; ++ch) {
     uint32_t ov[32];
     tmem_ld32(t_o + ch * 32, ov);
-    if (ch == D / 32 - 1) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars.o_empty(hh));
-    }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       mine4[(ch * 8 + i) * 128 + row] =
@@ -848,7 +855,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   }
   mine[128 * D + row] = m_ref;
   mine[128 * D + 128 + row] = l;
-  __threadfence();
+  fence_gpu();
   __syncwarp();
   const int64_t t_first = static_cast<int64_t>(sg.t) * p.n_kv;
   const int c_lo = cta_of_unit(cta_lo, ctas, t_first);
@@ -857,52 +864,68 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   if (lane == 0)
     n = arrive_part(p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter, p.epoch, ctl);
   n = __shfl_sync(0xffffffffu, n, 0);
-  if (n != static_cast<uint32_t>(c_hi - c_lo + 1)) return !*ctl.abort;
-  __threadfence();
+  if (n != static_cast<uint32_t>(c_hi - c_lo + 1)) {
+    release_o();
+    return !*ctl.abort;
+  }
+  fence_gpu();
   const int q = tk.q0[hh] + row;
   // a part of CTA c is that CTA's first segment iff its range starts in this task
   auto part = [&](int c) -> const float* { return slot_of(c, cta_lo[c] >= t_first); };
-  float M = -CUDART_INF_F;
-  for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
-    float mi[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u)
-      mi[u] = c0 + u <= c_hi ? __ldcg(part(c0 + u) + 128 * D + row) : -CUDART_INF_F;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) M = fmaxf(M, mi[u]);
-  }
-  float L = 0.f;
+  const int me = blockIdx.x;
+  // M and L over all parts, online: m and l of up to 8 other parts per round.
+  // Every load reads a valid part (this CTA's stands in for the unused
+  // slots) so that all of a round's loads are in flight together.
+  float M = m_ref;
+  float L = l;
   for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
     float mi[8], li[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const bool in = c0 + u <= c_hi;
-      const float* sl = part(in ? c0 + u : c_hi);
-      mi[u] = in ? __ldcg(sl + 128 * D + row) : -CUDART_INF_F;
-      li[u] = in ? __ldcg(sl + 128 * D + 128 + row) : 0.f;
+      const int c = c0 + u;
+      const float* sl = part(c <= c_hi ? c : me);
+      mi[u] = __ldcg(sl + 128 * D + row);
+      li[u] = __ldcg(sl + 128 * D + 128 + row);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (mi[u] != -CUDART_INF_F) L += ex2(mi[u] - M) * li[u];
+    for (int u = 0; u < 8; ++u) {
+      const int c = c0 + u;
+      if (c > c_hi || c == me) mi[u] = -CUDART_INF_F;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (mi[u] == -CUDART_INF_F) continue;
+      if (mi[u] > M) {
+        L = (M == -CUDART_INF_F) ? 0.f : L * ex2(M - mi[u]);
+        M = mi[u];
+      }
+      L += li[u] * ex2(mi[u] - M);
+    }
   }
   const float inv_L = L > 0.f ? 1.f / L : 0.f;
+  const float w_me = (m_ref == -CUDART_INF_F) ? 0.f : ex2(m_ref - M);
   const bool row_ok = q < p.Nq;
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
                         static_cast<int64_t>(q) * p.o_sn;
-  // O in chunks of 32 columns; four parts' rows are loaded together.
+  // O in chunks of 32 columns: this part's from TMEM, four other parts' rows per round.
 #pragma unroll 1
   for (int ch = 0; ch < D / 32; ++ch) {
     float acc[32];
+    {
+      uint32_t ov[32];
+      tmem_ld32(t_o + ch * 32, ov);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+      for (int i = 0; i < 32; ++i) acc[i] = w_me * __uint_as_float(ov[i]);
+    }
 #pragma unroll 1
     for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
       float4 v[4][8];
       float wgt[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const bool in = c0 + u <= c_hi;
-        const float* sl = part(in ? c0 + u : c_hi);
+        const int c = c0 + u;
+        const bool in = c <= c_hi && c != me;
+        const float* sl = part(c <= c_hi ? c : me);
         const float mi = __ldcg(sl + 128 * D + row);
         wgt[u] = (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
         const float4* src = reinterpret_cast<const float4*>(sl);
@@ -929,6 +952,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
         dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
     }
   }
+  release_o();
   if (row_ok && p.lse != nullptr) {
     const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
     p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
