@@ -166,8 +166,6 @@ int validate(const attn_params_ex* p, Checked* c) {
     if (span > c->grid_h || span > c->grid_w)
       return fail(ATTN_ERR_INVALID_ARG, "window*dilation=%lld exceeds the grid side",
                   static_cast<long long>(span));
-    if (p->dilation > 1)
-      return fail(ATTN_ERR_UNSUPPORTED, "NA2D dilation > 1 is not implemented on the GPU");
   }
   if (!p->q || !p->k || !p->v || !p->o)
     return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
@@ -330,6 +328,7 @@ int attn_fwd_ex(const attn_params_ex* p) {
   kp.grid_h = c.grid_h;
   kp.grid_w = c.grid_w;
   kp.window = p->window;
+  kp.dilation = p->mask_kind == ATTN_MASK_NA2D ? p->dilation : 1;
   Plan pl;
   if ((rc = make_plan(p, ds->sm_count, &pl)) != ATTN_OK) return rc;
   kp.n_qpairs = pl.n_qpairs;
@@ -350,7 +349,10 @@ int attn_fwd_ex(const attn_params_ex* p) {
 
   int mask = attn::kMaskNone;
   if (p->mask_kind == ATTN_MASK_CAUSAL) mask = attn::kMaskCausal;
-  if (p->mask_kind == ATTN_MASK_NA2D) mask = p->wrap ? attn::kMaskNaWrap : attn::kMaskNaClamp;
+  if (p->mask_kind == ATTN_MASK_NA2D) {
+    if (p->dilation > 1) mask = p->wrap ? attn::kMaskNaWrapDil : attn::kMaskNaClampDil;
+    else mask = p->wrap ? attn::kMaskNaWrap : attn::kMaskNaClamp;
+  }
 
   const int grid = pl.grid;
 

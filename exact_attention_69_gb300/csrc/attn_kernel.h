@@ -21,7 +21,19 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSplitCtas = 256;  // largest grid of the split schedule (its range table lives in shared memory)  // keep a stale row maximum until the true one exceeds it by 2^8
 
 // Mask specialisations (the C-ABI's NA2D splits into clamp and wrap here).
-enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskNaClamp = 2, kMaskNaWrap = 3 };
+// Kernel variants. The neighbourhood masks come with and without dilation:
+// dilation 1 keeps its interval arithmetic, free of the strided case.
+enum MaskKind : int {
+  kMaskNone = 0,
+  kMaskCausal = 1,
+  kMaskNaClamp = 2,
+  kMaskNaWrap = 3,
+  kMaskNaClampDil = 4,
+  kMaskNaWrapDil = 5
+};
+__host__ __device__ constexpr bool mask_is_na(int m) { return m >= kMaskNaClamp; }
+__host__ __device__ constexpr bool mask_na_wrap(int m) { return m == kMaskNaWrap || m == kMaskNaWrapDil; }
+__host__ __device__ constexpr bool mask_na_dilated(int m) { return m == kMaskNaClampDil || m == kMaskNaWrapDil; }
 
 // Roles recorded in the device status word when a bounded wait runs out.
 enum Role : uint32_t { kRoleLoader = 0, kRoleMma = 1, kRoleSoftmax = 2 };
@@ -36,6 +48,7 @@ struct KernelParams {
   int B, H, Nq, Nk;
   float c;                      // scale * log2(e): scores enter exp2 in log2 units
   int grid_h, grid_w, window;   // neighbourhood masks only
+  int dilation;                 // neighbourhood masks: key stride along each axis (>= 1)
   int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head
   int n_kv;                     // ceil(Nk / 128)
   int n_tasks;                  // B * H * n_qpairs

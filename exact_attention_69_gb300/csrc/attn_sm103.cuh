@@ -416,22 +416,53 @@ __host__ __device__ __forceinline__ bool axis_meets(int c0, int c1, int e0, int 
   return a <= e1 || b - G >= e0;  // covered: [a, G-1] and [0, b-G]
 }
 
-// Does any query in rows [q0, q1) attend any key in [k0, k1)? Exact for
-// dilation 1: the Q and K ranges are cut into their grid-row segments.
+// As axis_meets for a dilated window (stride dl > 1). Every key coordinate
+// of a dilated window lies within dl * (w - 1) of its query (clamp; the window
+// holds the query) or dl * (w / 2) circularly (wrap): the test is whether
+// that neighbourhood of [c0, c1] meets [e0, e1], a superset of the exact
+// answer. A tile it keeps that no window touches is fully masked: wasted
+// work, never a wrong result.
 template <bool WRAP>
+__host__ __device__ __forceinline__ bool axis_meets_dilated(int c0, int c1, int e0, int e1, int G,
+                                                            int w, int dl) {
+  if (!WRAP) {
+    const int lo = max(c0 - dl * (w - 1), 0), hi = min(c1 + dl * (w - 1), G - 1);
+    return hi >= e0 && lo <= e1;
+  }
+  const int reach = dl * (w >> 1);
+  const int span = c1 - c0 + 1 + 2 * reach;
+  if (span >= G) return true;
+  int a = c0 - reach;
+  if (a < 0) a += G;
+  const int b = a + span - 1;
+  if (b < G) return b >= e0 && a <= e1;
+  return a <= e1 || b - G >= e0;
+}
+
+template <bool WRAP, bool DIL>
+__host__ __device__ __forceinline__ bool axis_meets_nd(int c0, int c1, int e0, int e1, int G, int w,
+                                                       int dl) {
+  if (DIL) return axis_meets_dilated<WRAP>(c0, c1, e0, e1, G, w, dl);
+  return axis_meets<WRAP>(c0, c1, e0, e1, G, w);
+}
+
+// Does any query in rows [q0, q1) attend any key in [k0, k1)? The Q and K
+// ranges are cut into their grid-row segments; exact for dilation 1, a
+// superset for dilation > 1 (see axis_meets_dilated).
+template <bool WRAP, bool DIL>
 __host__ __device__ __forceinline__ bool na_tile_meets(int q0, int q1, int k0, int k1, const KernelParams& p) {
   const int W = p.grid_w;
   const int kr0 = k0 / W, kr1 = (k1 - 1) / W;
   for (int qa = q0; qa < q1;) {
     const int qr = qa / W;
     const int qb = min(q1, (qr + 1) * W);
-    if (axis_meets<WRAP>(qr, qr, kr0, kr1, p.grid_h, p.window)) {
+    if (axis_meets_nd<WRAP, DIL>(qr, qr, kr0, kr1, p.grid_h, p.window, p.dilation)) {
       for (int ka = k0; ka < k1;) {
         const int kr = ka / W;
         const int kb = min(k1, (kr + 1) * W);
-        if (axis_meets<WRAP>(qr, qr, kr, kr, p.grid_h, p.window) &&
-            axis_meets<WRAP>(qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W, W,
-                             p.window))
+        if (axis_meets_nd<WRAP, DIL>(qr, qr, kr, kr, p.grid_h, p.window, p.dilation) &&
+            axis_meets_nd<WRAP, DIL>(qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W, W,
+                                p.window, p.dilation))
           return true;
         ka = kb;
       }
@@ -453,7 +484,8 @@ __host__ __device__ __forceinline__ int tile_class(int q0, int j, const KernelPa
     if (k0 > q1 - 1) return 0;
     return (!ragged && k0 + kBN - 1 <= q0) ? 1 : 2;
   }
-  return na_tile_meets<MASK == kMaskNaWrap>(q0, q1, k0, min(k0 + kBN, p.Nk), p) ? 2 : 0;
+  return na_tile_meets<mask_na_wrap(MASK), mask_na_dilated(MASK)>(q0, q1, k0, min(k0 + kBN, p.Nk), p)
+             ? 2 : 0;
 }
 
 template <int MASK>
@@ -530,14 +562,45 @@ struct SegIter {
   }
 };
 
-// Grid coordinates of query token q and the starts of its clamped window.
+// First key coordinate of the window of query coordinate c on an axis of
+// length G (window w odd, dilation dl): the window's keys are f + dl * t,
+// t in [0, w) (modulo G for wrap). Clamp: the keys share c's residue modulo
+// dl, and inside that residue class the w-wide window is centred on c and
+// shifted inward at the borders. Wrap: centred on c, circular.
+template <bool WRAP, bool DIL>
+__host__ __device__ __forceinline__ int na_window_first(int c, int G, int w, int dl) {
+  const int half = w >> 1;
+  if (!DIL) dl = 1;
+  if (WRAP) {
+    const int f = c - dl * half;  // > -G since dl * w <= G
+    return f < 0 ? f + G : f;
+  }
+  if (dl == 1) return min(max(c - half, 0), G - w);
+  const int r = c % dl;
+  const int len = (G - r + dl - 1) / dl;  // positions of residue r
+  const int start = min(max(c / dl - half, 0), len - w);
+  return r + dl * start;
+}
+
+// Grid coordinates of query token q and the first key coordinates of its
+// window along each axis.
+template <bool WRAP, bool DIL>
 __host__ __device__ __forceinline__ void na_query_coords(const KernelParams& p, int q, int& qy,
                                                          int& qx, int& wy, int& wx) {
   qy = q / p.grid_w;
   qx = q - qy * p.grid_w;
-  const int half = p.window >> 1;
-  wy = min(max(qy - half, 0), p.grid_h - p.window);
-  wx = min(max(qx - half, 0), p.grid_w - p.window);
+  wy = na_window_first<WRAP, DIL>(qy, p.grid_h, p.window, p.dilation);
+  wx = na_window_first<WRAP, DIL>(qx, p.grid_w, p.window, p.dilation);
+}
+
+// Is key coordinate k in the window that starts at f (stride dl, w keys)?
+template <bool WRAP, bool DIL>
+__host__ __device__ __forceinline__ bool na_in_window(int k, int f, int G, int w, int dl) {
+  int d = k - f;
+  if (WRAP) d += d < 0 ? G : 0;
+  if (d < 0) return false;
+  if (!DIL) return d < w;
+  return d % dl == 0 && d / dl < w;
 }
 
 // Sets bits [lo, hi) (0 <= lo <= hi <= 128) of a 128-bit mask.
@@ -553,43 +616,39 @@ __host__ __device__ __forceinline__ void set_bits(uint32_t (&bits)[4], int lo, i
 }
 
 // Allowed keys of query (qy, qx) in the K/V tile starting at key k0, as bits
-// of a 128-bit mask (bit i: key k0 + i). Clamp: rows [wy, wy + w), columns
-// [wx, wx + w). Wrap: rows and columns (c - w/2 + t) mod G, t in [0, w).
-template <bool WRAP>
+// of a 128-bit mask (bit i: key k0 + i). The window's rows are wy + dl * t and
+// its columns wx + dl * t, t in [0, w) (modulo the grid side for wrap). With
+// dilation 1 a row's allowed columns form one interval (two when a wrapped
+// window crosses the last column); with dilation > 1 they are set one by one.
+template <bool WRAP, bool DIL>
 __host__ __device__ __forceinline__ void na_tile_bits(const KernelParams& p, int k0, int qy, int qx, int wy,
                                              int wx, uint32_t (&bits)[4]) {
-  const int G_h = p.grid_h, G_w = p.grid_w, w = p.window, half = w >> 1;
+  const int G_h = p.grid_h, G_w = p.grid_w, w = p.window, dl = p.dilation;
   bits[0] = bits[1] = bits[2] = bits[3] = 0u;
   const int nvalid = min(kBN, p.Nk - k0);
   int ky = k0 / G_w;
   int kx0 = k0 - ky * G_w;
-  // circular column window: [ca, ca + w) mod G_w
-  int ca = qx - half;
-  if (ca < 0) ca += G_w;
   for (int i = 0; i < nvalid; ++ky) {
     const int len = min(G_w - kx0, nvalid - i);  // this row's columns [kx0, kx0 + len)
-    bool row_ok;
-    if (!WRAP) {
-      row_ok = static_cast<unsigned>(ky - wy) < static_cast<unsigned>(w);
-    } else {
-      int dy = ky - qy + half;
-      dy += dy < 0 ? G_h : 0;
-      dy -= dy >= G_h ? G_h : 0;
-      row_ok = dy < w;
-    }
-    if (row_ok) {
+    if (na_in_window<WRAP, DIL>(ky, wy, G_h, w, dl)) {
       const int base = i - kx0;  // bit of column 0 of this row
-      if (!WRAP) {
-        const int lo = max(wx, kx0), hi = min(wx + w, kx0 + len);
+      if (!DIL) {
+        const int e1 = min(wx + w, G_w);
+        int lo = max(wx, kx0), hi = min(e1, kx0 + len);
         if (lo < hi) set_bits(bits, base + lo, base + hi);
-      } else {
-        const int e1 = min(ca + w, G_w);
-        int lo = max(ca, kx0), hi = min(e1, kx0 + len);
-        if (lo < hi) set_bits(bits, base + lo, base + hi);
-        if (ca + w > G_w) {  // the window wraps past the last column
+        if (WRAP && wx + w > G_w) {  // the window wraps past the last column
           lo = kx0;
-          hi = min(ca + w - G_w, kx0 + len);
+          hi = min(wx + w - G_w, kx0 + len);
           if (lo < hi) set_bits(bits, base + lo, base + hi);
+        }
+      } else {
+        for (int t = 0; t < w; ++t) {
+          int cx = wx + dl * t;
+          if (WRAP && cx >= G_w) cx -= G_w;
+          if (cx >= kx0 && cx < kx0 + len) {
+            const int bit = base + cx;
+            bits[bit >> 5] |= 1u << (bit & 31);
+          }
         }
       }
     }
@@ -978,7 +1037,7 @@ __device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams
     // keys as a 128-bit mask, one column interval per row segment,
     // then clear the rest with independent selects.
     uint32_t bits[4];
-    na_tile_bits<MASK == kMaskNaWrap>(p, k0, qy, qx, wy, wx, bits);
+    na_tile_bits<mask_na_wrap(MASK), mask_na_dilated(MASK)>(p, k0, qy, qx, wy, wx, bits);
 #pragma unroll
     for (int i = 0; i < 128; ++i)
       if (((bits[i >> 5] >> (i & 31)) & 1u) == 0u) s[i] = neg_inf;
@@ -1035,7 +1094,8 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     const int q = q0 + row;
     // neighbourhood: this query's grid coordinates and clamped window starts
     int qy = 0, qx = 0, wy = 0, wx = 0;
-    if (MASK == kMaskNaClamp || MASK == kMaskNaWrap) na_query_coords(p, q, qy, qx, wy, wx);
+    if (mask_is_na(MASK))
+      na_query_coords<mask_na_wrap(MASK), mask_na_dilated(MASK)>(p, q, qy, qx, wy, wx);
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
@@ -1234,6 +1294,8 @@ cudaError_t launch_dim(const KernelParams& p, int mask, int grid, cudaStream_t s
     case kMaskCausal: return launch_mask<D, kMaskCausal>(p, grid, s);
     case kMaskNaClamp: return launch_mask<D, kMaskNaClamp>(p, grid, s);
     case kMaskNaWrap: return launch_mask<D, kMaskNaWrap>(p, grid, s);
+    case kMaskNaClampDil: return launch_mask<D, kMaskNaClampDil>(p, grid, s);
+    case kMaskNaWrapDil: return launch_mask<D, kMaskNaWrapDil>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

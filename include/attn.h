@@ -31,7 +31,11 @@
  *                    positions: clamp mode (wrap = 0) shifts a full window
  *                    inward at the borders, start = clamp(c - window/2, 0,
  *                    G - window); wrap mode (wrap = 1) takes the positions
- *                    (c + t) mod G, t in [-window/2, window/2].
+ *                    (c + t) mod G, t in [-window/2, window/2]. With dilation
+ *                    dl > 1 (NATTEN's convention): clamp keeps the keys of
+ *                    c's residue class modulo dl and applies the rule above
+ *                    to the index inside that class; wrap takes
+ *                    (c + dl * t) mod G. window * dl <= each grid side.
  *
  * Data layout (device memory, owned and allocated by the caller):
  *   q, o : bf16 [B, H, Nq, d]   k, v : bf16 [B, H, Nk, d]   (contiguous by
@@ -81,7 +85,7 @@ typedef enum {
   ATTN_ERR_INVALID_ARG = 1,  /* sizes < 1, scale not finite or <= 0, even or
                                 oversized window, wrap without NA2D, NA2D with
                                 Nq != Nk or a non-square Nq and no grid, ... */
-  ATTN_ERR_UNSUPPORTED = 2,  /* d not in {32,64,128}; NA2D dilation > 1 */
+  ATTN_ERR_UNSUPPORTED = 2,  /* d not in {32,64,128} */
   ATTN_ERR_MISALIGNED = 3,   /* a pointer not 16-byte aligned, a stride not a
                                 multiple of 8 elements */
   ATTN_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed; the
@@ -102,7 +106,7 @@ typedef struct attn_params_ex {
   float scale;     /* > 0 and finite, typically 1/sqrt(d) */
   int mask_kind;   /* attn_mask_kind */
   int window;      /* NA2D: odd window size; others: must be 0 */
-  int dilation;    /* NA2D: 1 (others must be 1) */
+  int dilation;    /* NA2D: key stride >= 1 along each axis; others: must be 1 */
   int wrap;        /* NA2D: 0 = clamp, 1 = wrap; others: must be 0 */
   int grid_h, grid_w; /* NA2D token grid; 0,0 = square grid of side sqrt(Nq) */
   /* element strides of dims (b, h, n); all zero = contiguous [B,H,N,d] */

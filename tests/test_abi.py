@@ -65,7 +65,8 @@ BAD = [
     ("na_q_ne_k", dict(mask_kind=2, window=3, Nq=256, Nk=289), _lib.ATTN_ERR_INVALID_ARG),
     ("na_window_too_big", dict(mask_kind=2, window=17), _lib.ATTN_ERR_INVALID_ARG),
     ("na_bad_grid", dict(mask_kind=2, window=3, grid_h=10, grid_w=20), _lib.ATTN_ERR_INVALID_ARG),
-    ("na_dilation2", dict(mask_kind=2, window=3, dilation=2), _lib.ATTN_ERR_UNSUPPORTED),
+    ("na_dilation0", dict(mask_kind=2, window=3, dilation=0), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_dilated_window_too_big", dict(mask_kind=2, window=3, dilation=6), _lib.ATTN_ERR_INVALID_ARG),
     ("null_q", dict(q=None), _lib.ATTN_ERR_INVALID_ARG),
     ("misaligned_k", dict(k=(1 << 20) + 8), _lib.ATTN_ERR_MISALIGNED),
     ("misaligned_lse", dict(lse=(1 << 20) + 2), _lib.ATTN_ERR_MISALIGNED),

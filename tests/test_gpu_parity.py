@@ -50,14 +50,15 @@ def check(o, lse, ref_o, ref_lse, rows=None):
 
 
 def run(E, B, H, Nq, Nk, d, mask="none", window=0, grid=None, sigma=1.0, seed=1, rows=None,
-        num_ctas=0, scale=None):
+        num_ctas=0, scale=None, dilation=1):
     q, k, v = make_qkv(B, H, Nq, Nk, d, sigma, seed)
     scale = scale if scale is not None else 1.0 / math.sqrt(d)
     o, lse = E.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, mask=mask, window=window,
-                        grid=grid, num_ctas=num_ctas)
+                        dilation=dilation, grid=grid, num_ctas=num_ctas)
     _status_ok(E)
     ref_o, ref_lse = oracle.attention_rows(to_f64(q), to_f64(k), to_f64(v), rows, scale=scale,
-                                           mask_kind=mask, window=window, grid=grid)
+                                           mask_kind=mask, window=window, dilation=dilation,
+                                           grid=grid)
     return check(o, lse, ref_o, ref_lse, rows)
 
 
@@ -86,6 +87,25 @@ NA_GRIDS = [(5, 5, 3), (8, 8, 3), (16, 16, 5), (20, 12, 5), (13, 29, 7), (64, 64
 @pytest.mark.parametrize("d", [32, 64, 128])
 def test_neighbourhood(E, mode, gh, gw, win, d):
     run(E, 1, 2, gh * gw, gh * gw, d, mode, window=win, grid=(gh, gw), seed=gh * gw + win)
+
+
+# dilated neighbourhoods: (grid_h, grid_w, window, dilation), window * dilation <= each side
+NA_DILATED = [(8, 8, 3, 2), (16, 16, 5, 3), (20, 12, 3, 4), (13, 29, 3, 4), (24, 50, 5, 4),
+              (64, 64, 7, 2), (64, 64, 7, 9), (21, 21, 7, 3)]
+
+
+@pytest.mark.parametrize("mode", ["clamp", "wrap"])
+@pytest.mark.parametrize("gh,gw,win,dil", NA_DILATED)
+@pytest.mark.parametrize("d", [32, 64])
+def test_neighbourhood_dilated(E, mode, gh, gw, win, dil, d):
+    run(E, 1, 2, gh * gw, gh * gw, d, mode, window=win, dilation=dil, grid=(gh, gw),
+        seed=gh * gw + 31 * win + dil)
+
+
+def test_neighbourhood_dilated_d128_and_persistent(E):
+    run(E, 2, 1, 1024, 1024, 128, "wrap", window=5, dilation=3, grid=(32, 32), seed=77)
+    run(E, 1, 3, 1024, 1024, 32, "clamp", window=5, dilation=2, grid=(32, 32), num_ctas=2,
+        seed=78)
 
 
 def test_issue142_wrap_example_on_gpu(E):

@@ -2,9 +2,10 @@
 
 For every Q tile (128 query rows) and K/V tile (128 keys) the kernel decides:
 skip (no allowed pair), unmasked (every pair allowed) or masked. Checked here
-exactly against the allowed-set matrix of the numpy oracle twin: a skipped
-tile holds no allowed pair, a visited one holds at least one (no wasted
-tiles), and an unmasked one holds only allowed pairs.
+against the allowed-set matrix of the numpy oracle twin: a skipped tile holds
+no allowed pair and an unmasked one holds only allowed pairs; with dilation 1
+a visited tile also holds at least one (no wasted tiles), while dilated
+neighbourhoods may visit a few fully masked tiles (a superset test).
 """
 import ctypes
 import os
@@ -31,10 +32,10 @@ def plan(tmp_path_factory):
                     "-I", os.path.join(ROOT, "exact_attention_69_gb300", "csrc"),
                     os.path.join(ROOT, "tests", "host", "tile_plan.cu"), "-o", out], check=True)
     lib = ctypes.CDLL(out)
-    lib.tile_class_host.argtypes = [ctypes.c_int] * 8
+    lib.tile_class_host.argtypes = [ctypes.c_int] * 9
     lib.tile_class_host.restype = ctypes.c_int
     lib.decode_task_host.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
-    lib.na_bits_host.argtypes = [ctypes.c_int] * 7 + [ctypes.POINTER(ctypes.c_uint)]
+    lib.na_bits_host.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_uint)]
     return lib
 
 
@@ -51,20 +52,37 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("mask,Nq,Nk,grid,window", CASES)
-def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window):
-    allowed = twin.mask_matrix(Nq, Nk, mask, window, 1, grid)
+DILATED = [
+    ("clamp", 4096, 4096, (64, 64), 7, 2), ("wrap", 4096, 4096, (64, 64), 7, 3),
+    ("clamp", 400, 400, (20, 20), 3, 4), ("wrap", 400, 400, (20, 20), 5, 4),
+    ("clamp", 1200, 1200, (24, 50), 3, 7), ("wrap", 1200, 1200, (24, 50), 5, 4),
+    ("clamp", 64, 64, (8, 8), 3, 2), ("wrap", 64, 64, (8, 8), 3, 2),
+]
+
+
+@pytest.mark.parametrize("mask,Nq,Nk,grid,window,dilation",
+                         [c + (1,) for c in CASES] + DILATED)
+def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window, dilation):
+    allowed = twin.mask_matrix(Nq, Nk, mask, window, dilation, grid)
     gh, gw = grid if grid else (0, 0)
     n_kv = -(-Nk // 128)
+    visited = wasted = 0
     for q0 in range(0, Nq, 128):
         rows = allowed[q0:min(q0 + 128, Nq)]
         for j in range(n_kv):
             block = rows[:, j * 128:min(j * 128 + 128, Nk)]
-            c = plan.tile_class_host(MASK_CODE[mask], q0, j, Nq, Nk, gh, gw, window)
+            c = plan.tile_class_host(MASK_CODE[mask], q0, j, Nq, Nk, gh, gw, window, dilation)
             assert c in (0, 1, 2)
-            assert (c != 0) == bool(block.any()), (q0, j, c)
+            if c == 0:
+                assert not block.any(), (q0, j)
+            else:
+                visited += 1
+                wasted += not block.any()
+            if dilation == 1:
+                assert (c != 0) == bool(block.any()), (q0, j, c)
             if c == 1:
                 assert block.all() and block.shape[1] == 128, (q0, j)
+    assert wasted <= visited // 2 + 1, (visited, wasted)
 
 
 @pytest.mark.parametrize("mask", ["none", "causal"])
@@ -84,21 +102,25 @@ def test_tasks_cover_every_q_tile_once(plan, mask):
         assert out[2] == 256 * (n_qpairs - 1)
 
 
-@pytest.mark.parametrize("mode,gh,gw,window", [
-    ("clamp", 64, 64, 7), ("wrap", 64, 64, 7), ("clamp", 5, 5, 3), ("wrap", 5, 5, 3),
-    ("clamp", 13, 29, 7), ("wrap", 13, 29, 7), ("wrap", 24, 50, 9), ("clamp", 30, 160, 9),
-    ("wrap", 39, 39, 39), ("clamp", 12, 20, 1)])
-def test_in_tile_mask_bits_match_oracle_mask(plan, mode, gh, gw, window):
+@pytest.mark.parametrize("mode,gh,gw,window,dilation", [
+    ("clamp", 64, 64, 7, 1), ("wrap", 64, 64, 7, 1), ("clamp", 5, 5, 3, 1), ("wrap", 5, 5, 3, 1),
+    ("clamp", 13, 29, 7, 1), ("wrap", 13, 29, 7, 1), ("wrap", 24, 50, 9, 1),
+    ("clamp", 30, 160, 9, 1), ("wrap", 39, 39, 39, 1), ("clamp", 12, 20, 1, 1),
+    ("clamp", 8, 8, 3, 2), ("wrap", 8, 8, 3, 2), ("clamp", 20, 20, 5, 3), ("wrap", 20, 20, 5, 4),
+    ("clamp", 13, 29, 3, 4), ("wrap", 13, 29, 3, 4), ("clamp", 64, 64, 7, 2), ("wrap", 64, 64, 7, 9),
+    ("wrap", 21, 21, 7, 3), ("clamp", 21, 35, 3, 7)])
+def test_in_tile_mask_bits_match_oracle_mask(plan, mode, gh, gw, window, dilation):
     """The kernel's in-tile neighbourhood mask, bit for bit, against the oracle
     twin's allowed-set matrix, for every query and every K/V tile."""
     N = gh * gw
-    allowed = twin.mask_matrix(N, N, mode, window, 1, (gh, gw))
+    allowed = twin.mask_matrix(N, N, mode, window, dilation, (gh, gw))
     out = (ctypes.c_uint * 4)()
     rng = np.random.default_rng(0)
     queries = range(N) if N <= 1600 else rng.choice(N, 400, replace=False)
     for q in queries:
         for k0 in range(0, N, 128):
-            plan.na_bits_host(1 if mode == "wrap" else 0, int(q), k0, N, gh, gw, window, out)
+            plan.na_bits_host(1 if mode == "wrap" else 0, int(q), k0, N, gh, gw, window, dilation,
+                              out)
             bits = np.array([(out[i >> 5] >> (i & 31)) & 1 for i in range(128)], dtype=bool)
             ref = np.zeros(128, dtype=bool)
             n = min(128, N - k0)
