@@ -31,12 +31,15 @@
  *   1 CAUSAL : j <= i (top-left alignment, as is_causal=True).
  *   2 NA2D   : tokens are laid out row-major on a grid_h x grid_w grid;
  *              query (qy, qx), key (ky, kx); the key is allowed iff both axes
- *              are allowed by the one-axis rule below (window k odd, dilation).
- *     clamp (wrap = 0): the window keeps its full size k and is shifted inward
- *              at the borders. With dilation delta, keys share the query's
- *              residue modulo delta, and the dilation-1 rule is applied to the
- *              index inside that residue class.
- *     wrap  (wrap = 1): the keys are (q + delta*t) mod G for t in [-k/2, k/2].
+ *              are allowed by the one-axis rule below, each axis with its own
+ *              window size (odd) and its own choice of clamp or wrap; one
+ *              dilation for both. A grid with one row and a window of 1 along
+ *              it is 1-D neighbourhood attention.
+ *     clamp: the window keeps its full size k and is shifted inward at the
+ *              borders. With dilation delta, keys share the query's residue
+ *              modulo delta, and the dilation-1 rule is applied to the index
+ *              inside that residue class.
+ *     wrap : the keys are (q + delta*t) mod G for t in [-k/2, k/2].
  *   A row whose allowed set is empty gets o = 0 and lse = -inf (the
  *   NaN-guarding convention of a "safe" softmax).
  */
@@ -55,7 +58,7 @@
 typedef struct {
   int Nq, Nk, d;
   double scale;
-  int mask_kind, window, dilation, wrap, grid_h, grid_w;
+  int mask_kind, window_h, window_w, dilation, wrap_h, wrap_w, grid_h, grid_w;
 } problem_t;
 
 /* One axis of the clamped neighbourhood: is key coordinate kc in the window of
@@ -94,11 +97,11 @@ static int allowed(const problem_t* p, int i, int j) {
     case ORACLE_MASK_NA2D: {
       int qy = i / p->grid_w, qx = i % p->grid_w;
       int ky = j / p->grid_w, kx = j % p->grid_w;
-      if (p->wrap)
-        return axis_allowed_wrap(qy, ky, p->grid_h, p->window, p->dilation) &&
-               axis_allowed_wrap(qx, kx, p->grid_w, p->window, p->dilation);
-      return axis_allowed_clamp(qy, ky, p->grid_h, p->window, p->dilation) &&
-             axis_allowed_clamp(qx, kx, p->grid_w, p->window, p->dilation);
+      const int row_ok = p->wrap_h ? axis_allowed_wrap(qy, ky, p->grid_h, p->window_h, p->dilation)
+                                   : axis_allowed_clamp(qy, ky, p->grid_h, p->window_h, p->dilation);
+      const int col_ok = p->wrap_w ? axis_allowed_wrap(qx, kx, p->grid_w, p->window_w, p->dilation)
+                                   : axis_allowed_clamp(qx, kx, p->grid_w, p->window_w, p->dilation);
+      return row_ok && col_ok;
     }
     default:
       return 0;
@@ -112,8 +115,10 @@ static int check_args(const problem_t* p, int B, int H) {
   if (p->mask_kind == ORACLE_MASK_NA2D) {
     if (p->grid_h < 1 || p->grid_w < 1) return -1;
     if (p->grid_h * p->grid_w != p->Nq || p->Nq != p->Nk) return -1;
-    if (p->window < 1 || p->window % 2 == 0 || p->dilation < 1) return -1;
-    if (p->window * p->dilation > p->grid_h || p->window * p->dilation > p->grid_w) return -1;
+    if (p->window_h < 1 || p->window_h % 2 == 0 || p->window_w < 1 || p->window_w % 2 == 0)
+      return -1;
+    if (p->dilation < 1) return -1;
+    if (p->window_h * p->dilation > p->grid_h || p->window_w * p->dilation > p->grid_w) return -1;
   }
   return 0;
 }
@@ -162,14 +167,17 @@ static void one_row(const problem_t* p, const double* q, const double* k,
  * q: [B,H,Nq,d], k,v: [B,H,Nk,d], all fp64 contiguous.
  * rows == NULL: every row; o is [B,H,Nq,d], lse is [B,H,Nq].
  * rows != NULL: nrows flat row indices in [0, B*H*Nq); o is [nrows,d], lse [nrows].
+ * window_h / window_w and wrap_h / wrap_w: the row (grid_h) and column (grid_w)
+ * axes of NA2D; ignored for the other masks.
  * nthreads <= 0 leaves the OpenMP default.
  */
 int oracle_attn_rows(const double* q, const double* k, const double* v,
                      double* o, double* lse, int B, int H, int Nq, int Nk, int d,
-                     double scale, int mask_kind, int window, int dilation,
-                     int wrap, int grid_h, int grid_w, const int64_t* rows,
+                     double scale, int mask_kind, int window_h, int window_w, int dilation,
+                     int wrap_h, int wrap_w, int grid_h, int grid_w, const int64_t* rows,
                      int64_t nrows, int nthreads) {
-  problem_t p = {Nq, Nk, d, scale, mask_kind, window, dilation, wrap, grid_h, grid_w};
+  problem_t p = {Nq, Nk, d, scale, mask_kind, window_h, window_w, dilation,
+                 wrap_h, wrap_w, grid_h, grid_w};
   if (check_args(&p, B, H) != 0) return -1;
   const int64_t total = (int64_t)B * H * Nq;
   const int64_t n = rows ? nrows : total;
@@ -213,9 +221,10 @@ int oracle_max_threads(void) {
 }
 
 /* The allowed-set predicate itself, exposed so tests can inspect masks. */
-int oracle_allowed(int i, int j, int Nq, int Nk, int mask_kind, int window,
-                   int dilation, int wrap, int grid_h, int grid_w) {
-  problem_t p = {Nq, Nk, 1, 1.0, mask_kind, window, dilation, wrap, grid_h, grid_w};
+int oracle_allowed(int i, int j, int Nq, int Nk, int mask_kind, int window_h, int window_w,
+                   int dilation, int wrap_h, int wrap_w, int grid_h, int grid_w) {
+  problem_t p = {Nq, Nk, 1, 1.0, mask_kind, window_h, window_w, dilation,
+                 wrap_h, wrap_w, grid_h, grid_w};
   if (check_args(&p, 1, 1) != 0) return -1;
   if (i < 0 || i >= Nq || j < 0 || j >= Nk) return -1;
   return allowed(&p, i, j);

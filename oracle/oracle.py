@@ -48,6 +48,21 @@ def _dptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
+def _axes(mask_kind, window, wrap):
+    """(window_h, window_w, wrap_h, wrap_w) from a window given as k or (k_h, k_w) and
+    wrap given as a bool (both axes) or a pair (rows, columns); "wrap" as the mask
+    name wraps both axes unless the pair says otherwise."""
+    if isinstance(window, (tuple, list)):
+        kh, kw = int(window[0]), int(window[1])
+    else:
+        kh = kw = int(window)
+    if isinstance(wrap, (tuple, list)):
+        wh, ww = bool(wrap[0]), bool(wrap[1])
+    else:
+        wh = ww = bool(wrap) or mask_kind == "wrap"
+    return kh, kw, int(wh), int(ww)
+
+
 def _grid(mask_kind, Nq, grid):
     if mask_kind != MASK_NA2D:
         return 0, 0
@@ -70,12 +85,12 @@ class Oracle:
             dp, dp, dp, dp, dp,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int,
         ]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_allowed.restype = ctypes.c_int
-        lib.oracle_allowed.argtypes = [ctypes.c_int] * 10
+        lib.oracle_allowed.argtypes = [ctypes.c_int] * 12
         self._lib = lib
         self.path = path
 
@@ -87,9 +102,10 @@ class Oracle:
         rows: None for every row, else flat indices b*H*Nq + h*Nq + i.
         Returns (o, lse): o [B,H,Nq,d] / lse [B,H,Nq] for rows=None, else
         o [len(rows), d] / lse [len(rows)].
+        window: k, or (k_h, k_w) per grid axis; wrap: bool, or (rows, columns).
         """
+        kh, kw, wh, ww = _axes(mask_kind, window, wrap)
         if isinstance(mask_kind, str):
-            wrap = wrap or mask_kind == "wrap"
             mask_kind = MASK_CODES[mask_kind]
         q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
         k = np.ascontiguousarray(np.asarray(k, dtype=np.float64))
@@ -110,8 +126,8 @@ class Oracle:
             rp = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
         rc = self._lib.oracle_attn_rows(
             _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
-            B, H, Nq, Nk, d, float(scale), int(mask_kind), int(window), int(dilation),
-            int(bool(wrap)), gh, gw, rp, n, int(nthreads),
+            B, H, Nq, Nk, d, float(scale), int(mask_kind), kh, kw, int(dilation),
+            wh, ww, gh, gw, rp, n, int(nthreads),
         )
         if rc != 0:
             raise ValueError(f"oracle rejected the problem (code {rc})")
@@ -123,12 +139,12 @@ class Oracle:
 
     def allowed(self, i, j, *, Nq, Nk, mask_kind, window=0, dilation=1, wrap=False, grid=None):
         """The oracle's allowed-set predicate for one (query, key) pair."""
+        kh, kw, wh, ww = _axes(mask_kind, window, wrap)
         if isinstance(mask_kind, str):
-            wrap = wrap or mask_kind == "wrap"
             mask_kind = MASK_CODES[mask_kind]
         gh, gw = _grid(mask_kind, Nq, grid)
         r = self._lib.oracle_allowed(int(i), int(j), int(Nq), int(Nk), int(mask_kind),
-                                     int(window), int(dilation), int(bool(wrap)), gh, gw)
+                                     kh, kw, int(dilation), wh, ww, gh, gw)
         if r < 0:
             raise ValueError("bad arguments")
         return bool(r)

@@ -35,9 +35,13 @@ def _window_coords_wrap(c: int, G: int, k: int, dil: int) -> set:
     return {(c + dil * t) % G for t in range(-(k // 2), k // 2 + 1)}
 
 
-def mask_matrix(Nq: int, Nk: int, mask: str, window: int = 0, dilation: int = 1,
-                grid=None) -> np.ndarray:
-    """Boolean [Nq, Nk] allowed-set matrix. mask: none | causal | clamp | wrap."""
+def mask_matrix(Nq: int, Nk: int, mask: str, window=0, dilation: int = 1,
+                grid=None, wrap_axes=None) -> np.ndarray:
+    """Boolean [Nq, Nk] allowed-set matrix. mask: none | causal | clamp | wrap.
+
+    window: k, or (k_rows, k_cols); wrap_axes: None (both axes wrap for "wrap",
+    neither for "clamp") or (rows, cols) booleans.
+    """
     if mask == "none":
         return np.ones((Nq, Nk), dtype=bool)
     if mask == "causal":
@@ -47,12 +51,15 @@ def mask_matrix(Nq: int, Nk: int, mask: str, window: int = 0, dilation: int = 1,
         return m
     gh, gw = grid
     assert gh * gw == Nq == Nk
-    fn = _window_coords_clamp if mask == "clamp" else _window_coords_wrap
+    kh, kw = (window, window) if np.isscalar(window) else (window[0], window[1])
+    wh, ww = (mask == "wrap",) * 2 if wrap_axes is None else wrap_axes
+    fn_h = _window_coords_wrap if wh else _window_coords_clamp
+    fn_w = _window_coords_wrap if ww else _window_coords_clamp
     m = np.zeros((Nq, Nk), dtype=bool)
     for qy in range(gh):
-        rows = fn(qy, gh, window, dilation)
+        rows = fn_h(qy, gh, kh, dilation)
         for qx in range(gw):
-            cols = fn(qx, gw, window, dilation)
+            cols = fn_w(qx, gw, kw, dilation)
             i = qy * gw + qx
             for ky in rows:
                 for kx in cols:

@@ -16,6 +16,9 @@ What pins what:
   sdpa_fp64               torch scaled_dot_product_attention (math) in fp64, none/causal/mask
   invariants              key shift, linearity in V, key permutation, causal prefix
   wrap_equals_pad_clamp   circular pad + clamped NA + crop == wrap NA (issue #142's recipe)
+  one_axis_wrap_pad_clamp the same recipe along one axis == wrap along that axis only
+  axis_windows_by_hand    literal key sets for a rectangular window and one-axis wrap
+  one_d_closed_form       a 1 x N grid is 1-D neighbourhood attention: closed-form windows
 """
 from __future__ import annotations
 
@@ -95,12 +98,16 @@ CASES = [
     dict(mask_kind="wrap", Nq=48, Nk=48, window=3, grid=(6, 8)),
     dict(mask_kind="clamp", Nq=64, Nk=64, window=3, grid=(8, 8), dilation=2),
     dict(mask_kind="wrap", Nq=64, Nk=64, window=3, grid=(8, 8), dilation=2),
+    dict(mask_kind="clamp", Nq=54, Nk=54, window=(3, 5), grid=(6, 9)),
+    dict(mask_kind="clamp", Nq=54, Nk=54, window=(5, 3), grid=(6, 9), wrap=(True, False)),
+    dict(mask_kind="clamp", Nq=54, Nk=54, window=(3, 3), grid=(6, 9), wrap=(False, True), dilation=2),
+    dict(mask_kind="clamp", Nq=15, Nk=15, window=(1, 5), grid=(1, 15)),
 ]
 
 
 def _kw(case):
     kw = dict(mask_kind=case["mask_kind"])
-    for name in ("window", "grid", "dilation"):
+    for name in ("window", "grid", "dilation", "wrap"):
         if name in case:
             kw[name] = case[name]
     return kw
@@ -108,7 +115,7 @@ def _kw(case):
 
 def _twin_mask(case):
     return twin.mask_matrix(case["Nq"], case["Nk"], case["mask_kind"], case.get("window", 0),
-                            case.get("dilation", 1), case.get("grid"))
+                            case.get("dilation", 1), case.get("grid"), case.get("wrap"))
 
 
 def constant_v(orc):
@@ -142,7 +149,8 @@ def zero_qk_means(orc):
             exp_n = cnt
         else:
             kk = case["window"]
-            exp_n = np.full(Nq, kk * kk)        # every query sees a full k x k window
+            kh, kw = (kk, kk) if np.isscalar(kk) else kk
+            exp_n = np.full(Nq, kh * kw)        # every query sees a full k_h x k_w window
             allowed = _twin_mask(case)
             exp_o = np.stack([v[0, 0][allowed[i]].mean(axis=0) for i in range(Nq)])
         assert np.max(np.abs(o[0, 0] - exp_o)) < 1e-13, case
@@ -275,6 +283,76 @@ def wrap_equals_pad_clamp(orc):
         assert np.max(np.abs(lc - lw)) < 1e-12, (gh, gw, win, dil)
 
 
+def one_axis_wrap_pad_clamp(orc):
+    """Issue #142's recipe along one axis only: circularly pad that axis by
+    (k_axis // 2) * dilation, run clamped NA on the padded grid, crop. It must
+    equal NA that wraps that axis and clamps the other."""
+    rng = np.random.default_rng(17)
+    for (gh, gw, kh, kw, dil, axis) in ((7, 9, 3, 5, 1, 0), (7, 9, 5, 3, 1, 1), (9, 8, 3, 3, 2, 0),
+                                        (6, 11, 3, 5, 2, 1), (5, 12, 1, 7, 1, 1)):
+        d = 4
+        x = [rng.standard_normal((gh, gw, d)) for _ in range(3)]
+        ph = (kh // 2) * dil if axis == 0 else 0
+        pw = (kw // 2) * dil if axis == 1 else 0
+        padded = [np.pad(t, ((ph, ph), (pw, pw), (0, 0)), mode="wrap") for t in x]
+        PH, PW = gh + 2 * ph, gw + 2 * pw
+
+        def flat(t, h, w):
+            return t.reshape(1, 1, h * w, d)
+
+        ow, lw = orc.attention(*(flat(t, gh, gw) for t in x), scale=0.6, mask_kind="clamp",
+                               window=(kh, kw), dilation=dil, grid=(gh, gw),
+                               wrap=(axis == 0, axis == 1))
+        oc, lc = orc.attention(*(flat(t, PH, PW) for t in padded), scale=0.6, mask_kind="clamp",
+                               window=(kh, kw), dilation=dil, grid=(PH, PW))
+        oc = oc.reshape(PH, PW, d)[ph:ph + gh, pw:pw + gw].reshape(1, 1, gh * gw, d)
+        lc = lc.reshape(PH, PW)[ph:ph + gh, pw:pw + gw].reshape(1, 1, gh * gw)
+        assert np.max(np.abs(oc - ow)) < 1e-12, (gh, gw, kh, kw, dil, axis)
+        assert np.max(np.abs(lc - lw)) < 1e-12, (gh, gw, kh, kw, dil, axis)
+
+
+def axis_windows_by_hand(orc):
+    def keys(i, grid, window, wrap=False):
+        n = grid[0] * grid[1]
+        return {j for j in range(n)
+                if orc.allowed(i, j, Nq=n, Nk=n, mask_kind="clamp", window=window, wrap=wrap,
+                               grid=grid)}
+
+    def tok(y, x, w):
+        return y * w + x
+
+    g = (5, 7)
+    # window 3 rows x 5 columns, clamp: (0,0) -> rows {0,1,2} x cols {0..4};
+    # (4,6) -> rows {2,3,4} x cols {2..6}; (2,3) -> rows {1,2,3} x cols {1..5}
+    assert keys(tok(0, 0, 7), g, (3, 5)) == {tok(y, x, 7) for y in (0, 1, 2) for x in range(5)}
+    assert keys(tok(4, 6, 7), g, (3, 5)) == {tok(y, x, 7) for y in (2, 3, 4) for x in range(2, 7)}
+    assert keys(tok(2, 3, 7), g, (3, 5)) == {tok(y, x, 7) for y in (1, 2, 3) for x in range(1, 6)}
+    # window 5 rows x 1 column: a column of the grid, clamped
+    assert keys(tok(0, 2, 7), g, (5, 1)) == {tok(y, 2, 7) for y in range(5)}
+    # rows wrap, columns clamp, window 3 x 3: (0,0) -> rows {4,0,1} x cols {0,1,2}
+    assert keys(tok(0, 0, 7), g, (3, 3), (True, False)) == \
+        {tok(y, x, 7) for y in (4, 0, 1) for x in (0, 1, 2)}
+    # rows clamp, columns wrap, window 3 x 5: (0,6) -> rows {0,1,2} x cols {4,5,6,0,1}
+    assert keys(tok(0, 6, 7), g, (3, 5), (False, True)) == \
+        {tok(y, x, 7) for y in (0, 1, 2) for x in (4, 5, 6, 0, 1)}
+
+
+def one_d_closed_form(orc):
+    """A 1 x N grid with window (1, k): key j is allowed for query i iff it lies in
+    [s, s + k), s = min(max(i - k//2, 0), N - k) (clamp), or iff its circular
+    distance to i is at most k//2 (wrap)."""
+    for (N, k) in ((11, 3), (16, 5), (9, 9), (13, 1)):
+        for i in range(N):
+            s0 = min(max(i - k // 2, 0), N - k)
+            for j in range(N):
+                clamp = orc.allowed(i, j, Nq=N, Nk=N, mask_kind="clamp", window=(1, k), grid=(1, N))
+                wrap = orc.allowed(i, j, Nq=N, Nk=N, mask_kind="clamp", window=(1, k), grid=(1, N),
+                                   wrap=(False, True))
+                assert clamp == (s0 <= j < s0 + k), (N, k, i, j)
+                dist = min((j - i) % N, (i - j) % N)
+                assert wrap == (dist <= k // 2), (N, k, i, j)
+
+
 def row_subset_matches_full(orc):
     rng = np.random.default_rng(14)
     q = _rand(2, 2, 33, 8, rng=rng)
@@ -301,5 +379,8 @@ def all_checks(goldens):
         ("sdpa_fp64", sdpa_fp64),
         ("invariants", invariants),
         ("wrap_equals_pad_clamp", wrap_equals_pad_clamp),
+        ("one_axis_wrap_pad_clamp", one_axis_wrap_pad_clamp),
+        ("axis_windows_by_hand", axis_windows_by_hand),
+        ("one_d_closed_form", one_d_closed_form),
         ("row_subset_matches_full", row_subset_matches_full),
     ]

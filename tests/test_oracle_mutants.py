@@ -26,8 +26,11 @@ MUTANTS = {
     "wrap_negative_modulo": ("if (c < 0) c += G;", ""),
     "clamp_no_upper_shift": ("if (start > len - k) start = len - k;", ""),
     "clamp_window_off_centre": ("int start = a - k / 2;", "int start = a - k / 2 + 1;"),
-    "na_axis_swapped": ("axis_allowed_clamp(qx, kx, p->grid_w, p->window, p->dilation);",
-                        "axis_allowed_clamp(qx, kx, p->grid_h, p->window, p->dilation);"),
+    "na_axis_swapped": (": axis_allowed_clamp(qx, kx, p->grid_w, p->window_w, p->dilation);",
+                        ": axis_allowed_clamp(qx, kx, p->grid_h, p->window_w, p->dilation);"),
+    "na_window_axes_swapped": (": axis_allowed_clamp(qy, ky, p->grid_h, p->window_h, p->dilation);",
+                               ": axis_allowed_clamp(qy, ky, p->grid_h, p->window_w, p->dilation);"),
+    "na_wrap_axes_swapped": ("const int row_ok = p->wrap_h ?", "const int row_ok = p->wrap_w ?"),
     "dilation_residue_ignored": ("if (kc % dl != residue) return 0;", ""),
     "softmax_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
 }

@@ -24,12 +24,12 @@ def test_twin_masks_agree_with_oracle_predicate(orc):
     from oracle import reference_np as twin
     for case in pins.CASES:
         m = twin.mask_matrix(case["Nq"], case["Nk"], case["mask_kind"], case.get("window", 0),
-                             case.get("dilation", 1), case.get("grid"))
+                             case.get("dilation", 1), case.get("grid"), case.get("wrap"))
         for i in range(case["Nq"]):
             for j in range(case["Nk"]):
                 got = orc.allowed(i, j, Nq=case["Nq"], Nk=case["Nk"], mask_kind=case["mask_kind"],
                                   window=case.get("window", 0), dilation=case.get("dilation", 1),
-                                  grid=case.get("grid"))
+                                  grid=case.get("grid"), wrap=case.get("wrap", False))
                 assert got == bool(m[i, j]), (case, i, j)
 
 
