@@ -61,6 +61,7 @@ class AttnParamsEx(ctypes.Structure):
         ("schedule", ctypes.c_int),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_uint64),
+        ("window_w", ctypes.c_int),
     ]
 
 

@@ -7,7 +7,8 @@ the library's sm_103a kernel per call. Nothing here computes attention.
                                   are staged to the GPU and back)
     na2d(q, k, v, kernel_size, mode)
                                   NATTEN's heads-last [B, X, Y, heads, d] layout,
-                                  'clamp' or 'wrap' windows (NATTEN issue #142)
+                                  'clamp' or 'wrap' windows (NATTEN issue #142),
+                                  per axis if asked
 """
 from __future__ import annotations
 
@@ -35,6 +36,16 @@ def _strides(t: torch.Tensor, layout: str):
     return (sb, sh, sn)
 
 
+def _na_axes(mask, window, wrap_axes):
+    """(window along the rows, window along the columns, ABI wrap code)."""
+    kh, kw = (int(window), int(window)) if isinstance(window, int) else (int(window[0]),
+                                                                         int(window[1]))
+    if wrap_axes is None:
+        wrap_axes = (mask == "wrap", mask == "wrap")
+    code = {(False, False): 0, (True, True): 1, (True, False): 2, (False, True): 3}
+    return kh, kw, code[(bool(wrap_axes[0]), bool(wrap_axes[1]))]
+
+
 def _check_dev(*ts):
     for t in ts:
         if t.dtype != torch.bfloat16:
@@ -44,7 +55,8 @@ def _check_dev(*ts):
 
 
 def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, grid,
-            layout, num_ctas, timeout_ns, inject, events, stream, schedule=0, workspace=None):
+            layout, num_ctas, timeout_ns, inject, events, stream, schedule=0, workspace=None,
+            wrap_axes=None):
     p = _lib.params()
     p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
     p.lse = lse.data_ptr() if lse is not None else None
@@ -52,9 +64,9 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
     p.scale = float(scale)
     p.mask_kind = _MASKS[mask]
     if mask in ("clamp", "wrap"):
-        p.window = int(window)
+        kh, kw, p.wrap = _na_axes(mask, window, wrap_axes)
+        p.window, p.window_w = kh, (kw if kw != kh else 0)
         p.dilation = int(dilation)
-        p.wrap = 1 if mask == "wrap" else 0
         if grid is not None:
             p.grid_h, p.grid_w = int(grid[0]), int(grid[1])
     else:
@@ -82,16 +94,18 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
-             mask: str = "none", window: int = 0, dilation: int = 1, grid=None,
+             mask: str = "none", window=0, dilation: int = 1, grid=None,
              out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
              return_lse: bool = True, num_ctas: int = 0, timeout_ns: int = 0, inject: int = 0,
              events=None, stream=None, schedule: int = 0,
-             workspace: torch.Tensor | None = None):
+             workspace: torch.Tensor | None = None, wrap_axes=None):
     """Fused exact attention forward over [B, H, N, d] bf16 tensors.
 
     mask: 'none' | 'causal' | 'clamp' | 'wrap' (the last two: 2-D neighbourhood
-    attention with an odd `window` over a grid_h x grid_w token grid, square
-    by default). Returns (o, lse) or o. CPU inputs are copied to the current
+    attention over a grid_h x grid_w token grid, square by default, with an odd
+    `window`, or (rows, columns) windows; wrap_axes=(rows, columns) chooses
+    per axis whether the window wraps, overriding the mask name; a (1, N) grid
+    with window (1, k) is 1-D neighbourhood attention). Returns (o, lse) or o. CPU inputs are copied to the current
     CUDA device, and the results back to the CPU (the end-to-end path).
     schedule: 0 automatic, 1 whole tasks per CTA, 2 equal shares of K/V tiles
     with cut tasks merged (unmasked only). workspace: optional zero-filled
@@ -102,7 +116,8 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
         raise ValueError("expected [B, H, N, d] tensors")
     if not q.is_cuda:
         return _host_roundtrip(q, k, v, scale=scale, mask=mask, window=window,
-                               dilation=dilation, grid=grid, return_lse=return_lse)
+                               dilation=dilation, grid=grid, return_lse=return_lse,
+                               wrap_axes=wrap_axes)
     _check_dev(q, k, v)
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
@@ -117,7 +132,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
     _launch(q, k, v, out, lse, B=B, H=H, Nq=Nq, Nk=Nk, d=d, scale=scale, mask=mask,
             window=window, dilation=dilation, grid=grid, layout="bhnd", num_ctas=num_ctas,
             timeout_ns=timeout_ns, inject=inject, events=events, stream=stream,
-            schedule=schedule, workspace=workspace)
+            schedule=schedule, workspace=workspace, wrap_axes=wrap_axes)
     return (out, lse) if return_lse else out
 
 
@@ -150,17 +165,19 @@ def _host_roundtrip(q, k, v, *, return_lse, **kw):
     return (o_h, l_h) if return_lse else o_h
 
 
-def na2d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size: int, *,
-         mode: str = "clamp", dilation: int = 1, scale: float | None = None,
+def na2d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size, *,
+         mode="clamp", dilation: int = 1, scale: float | None = None,
          out: torch.Tensor | None = None, return_lse: bool = False, stream=None):
     """2-D neighbourhood attention in NATTEN's heads-last layout [B, X, Y, heads, d].
 
-    mode 'clamp': windows keep their full kernel_size^2 and shift inward at the
-    borders; mode 'wrap': windows wrap around the borders (circular). The
-    output has the same layout; no permute or copy of the inputs is made.
+    kernel_size: k, or (k_x, k_y). mode 'clamp': windows keep their full size
+    and shift inward at the borders; 'wrap': windows wrap around the borders
+    (circular); or a pair of those, one per axis (x, y). The output has the
+    same layout; no permute or copy of the inputs is made.
     """
-    if mode not in ("clamp", "wrap"):
-        raise ValueError("mode must be 'clamp' or 'wrap'")
+    modes = (mode, mode) if isinstance(mode, str) else tuple(mode)
+    if len(modes) != 2 or any(m not in ("clamp", "wrap") for m in modes):
+        raise ValueError("mode must be 'clamp' or 'wrap', or a pair of them")
     if q.dim() != 5:
         raise ValueError("expected [B, X, Y, heads, d] tensors")
     _check_dev(q, k, v)
@@ -170,9 +187,10 @@ def na2d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size: int, *,
     if out is None:
         out = torch.empty_like(q, memory_format=torch.contiguous_format)
     lse = torch.empty((B, H, X * Y), dtype=torch.float32, device=q.device) if return_lse else None
-    _launch(q, k, v, out, lse, B=B, H=H, Nq=X * Y, Nk=X * Y, d=d, scale=scale, mask=mode,
+    _launch(q, k, v, out, lse, B=B, H=H, Nq=X * Y, Nk=X * Y, d=d, scale=scale, mask="clamp",
             window=kernel_size, dilation=dilation, grid=(X, Y), layout="bxyhd", num_ctas=0,
-            timeout_ns=0, inject=0, events=None, stream=stream)
+            timeout_ns=0, inject=0, events=None, stream=stream,
+            wrap_axes=(modes[0] == "wrap", modes[1] == "wrap"))
     return (out, lse) if return_lse else out
 
 

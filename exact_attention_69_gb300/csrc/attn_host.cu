@@ -139,13 +139,19 @@ int validate(const attn_params_ex* p, Checked* c) {
   if (BH * n_qpairs >= (int64_t{1} << 31))
     return fail(ATTN_ERR_INVALID_ARG, "too many (batch, head, query-tile) tasks");
   if (p->mask_kind != ATTN_MASK_NA2D) {
-    if (p->window != 0 || p->dilation != 1 || p->wrap != 0 || p->grid_h != 0 || p->grid_w != 0)
+    if (p->window != 0 || p->window_w != 0 || p->dilation != 1 || p->wrap != 0 ||
+        p->grid_h != 0 || p->grid_w != 0)
       return fail(ATTN_ERR_INVALID_ARG,
                   "window/dilation/wrap/grid apply to NA2D only (need 0/1/0/0x0)");
   } else {
-    if (p->wrap != 0 && p->wrap != 1) return fail(ATTN_ERR_INVALID_ARG, "wrap must be 0 or 1");
+    if (p->wrap < 0 || p->wrap > 3)
+      return fail(ATTN_ERR_INVALID_ARG, "wrap must be 0 (none), 1 (both axes), 2 (rows) or 3 "
+                  "(columns)");
     if (p->window < 1 || p->window % 2 == 0)
       return fail(ATTN_ERR_INVALID_ARG, "window must be odd and >= 1 (got %d)", p->window);
+    if (p->window_w != 0 && (p->window_w < 1 || p->window_w % 2 == 0))
+      return fail(ATTN_ERR_INVALID_ARG, "window_w must be 0 or odd and >= 1 (got %d)",
+                  p->window_w);
     if (p->dilation < 1) return fail(ATTN_ERR_INVALID_ARG, "dilation must be >= 1");
     if (p->Nq != p->Nk) return fail(ATTN_ERR_INVALID_ARG, "NA2D needs Nq == Nk");
     if (p->grid_h == 0 && p->grid_w == 0) {
@@ -162,10 +168,15 @@ int validate(const attn_params_ex* p, Checked* c) {
       c->grid_h = p->grid_h;
       c->grid_w = p->grid_w;
     }
-    const int64_t span = static_cast<int64_t>(p->window) * p->dilation;
-    if (span > c->grid_h || span > c->grid_w)
-      return fail(ATTN_ERR_INVALID_ARG, "window*dilation=%lld exceeds the grid side",
-                  static_cast<long long>(span));
+    const int64_t span_h = static_cast<int64_t>(p->window) * p->dilation;
+    const int64_t span_w = static_cast<int64_t>(p->window_w ? p->window_w : p->window) * p->dilation;
+    // a window of 1 holds only the query, whatever the dilation
+    if ((p->window > 1 && span_h > c->grid_h) ||
+        ((p->window_w ? p->window_w : p->window) > 1 && span_w > c->grid_w))
+      return fail(ATTN_ERR_INVALID_ARG,
+                  "window*dilation (%lld rows, %lld columns) exceeds the %dx%d grid",
+                  static_cast<long long>(span_h), static_cast<long long>(span_w), c->grid_h,
+                  c->grid_w);
   }
   if (!p->q || !p->k || !p->v || !p->o)
     return fail(ATTN_ERR_INVALID_ARG, "q, k, v and o must be non-null");
@@ -327,7 +338,8 @@ int attn_fwd_ex(const attn_params_ex* p) {
   kp.c = p->scale * 1.4426950408889634f;
   kp.grid_h = c.grid_h;
   kp.grid_w = c.grid_w;
-  kp.window = p->window;
+  kp.window_h = p->window;
+  kp.window_w = p->window_w ? p->window_w : p->window;
   kp.dilation = p->mask_kind == ATTN_MASK_NA2D ? p->dilation : 1;
   Plan pl;
   if ((rc = make_plan(p, ds->sm_count, &pl)) != ATTN_OK) return rc;
@@ -349,10 +361,9 @@ int attn_fwd_ex(const attn_params_ex* p) {
 
   int mask = attn::kMaskNone;
   if (p->mask_kind == ATTN_MASK_CAUSAL) mask = attn::kMaskCausal;
-  if (p->mask_kind == ATTN_MASK_NA2D) {
-    if (p->dilation > 1) mask = p->wrap ? attn::kMaskNaWrapDil : attn::kMaskNaClampDil;
-    else mask = p->wrap ? attn::kMaskNaWrap : attn::kMaskNaClamp;
-  }
+  if (p->mask_kind == ATTN_MASK_NA2D)
+    mask = attn::na_mask(p->wrap == 1 || p->wrap == 2, p->wrap == 1 || p->wrap == 3,
+                         p->dilation > 1);
 
   const int grid = pl.grid;
 

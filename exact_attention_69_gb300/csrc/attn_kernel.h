@@ -21,19 +21,26 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSplitCtas = 256;  // largest grid of the split schedule (its range table lives in shared memory)  // keep a stale row maximum until the true one exceeds it by 2^8
 
 // Mask specialisations (the C-ABI's NA2D splits into clamp and wrap here).
-// Kernel variants. The neighbourhood masks come with and without dilation:
-// dilation 1 keeps its interval arithmetic, free of the strided case.
-enum MaskKind : int {
-  kMaskNone = 0,
-  kMaskCausal = 1,
-  kMaskNaClamp = 2,
-  kMaskNaWrap = 3,
-  kMaskNaClampDil = 4,
-  kMaskNaWrapDil = 5
-};
-__host__ __device__ constexpr bool mask_is_na(int m) { return m >= kMaskNaClamp; }
-__host__ __device__ constexpr bool mask_na_wrap(int m) { return m == kMaskNaWrap || m == kMaskNaWrapDil; }
-__host__ __device__ constexpr bool mask_na_dilated(int m) { return m == kMaskNaClampDil || m == kMaskNaWrapDil; }
+// Kernel variants. Neighbourhood masks are kMaskNa plus flags: which axes
+// wrap (rows, columns) and whether the windows are dilated, so that each
+// combination compiles to its own arithmetic (dilation 1 keeps intervals).
+enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskNa = 2 };
+constexpr int kNaWrapCols = 1, kNaWrapRows = 2, kNaDilated = 4;
+constexpr int kMaskKinds = kMaskNa + 8;
+__host__ __device__ constexpr int na_mask(bool wrap_rows, bool wrap_cols, bool dilated) {
+  return kMaskNa + (wrap_cols ? kNaWrapCols : 0) + (wrap_rows ? kNaWrapRows : 0) +
+         (dilated ? kNaDilated : 0);
+}
+__host__ __device__ constexpr bool mask_is_na(int m) { return m >= kMaskNa; }
+__host__ __device__ constexpr bool mask_na_wrap_rows(int m) {
+  return m >= kMaskNa && ((m - kMaskNa) & kNaWrapRows) != 0;
+}
+__host__ __device__ constexpr bool mask_na_wrap_cols(int m) {
+  return m >= kMaskNa && ((m - kMaskNa) & kNaWrapCols) != 0;
+}
+__host__ __device__ constexpr bool mask_na_dilated(int m) {
+  return m >= kMaskNa && ((m - kMaskNa) & kNaDilated) != 0;
+}
 
 // Roles recorded in the device status word when a bounded wait runs out.
 enum Role : uint32_t { kRoleLoader = 0, kRoleMma = 1, kRoleSoftmax = 2 };
@@ -47,7 +54,8 @@ struct KernelParams {
   int64_t o_sb, o_sh, o_sn;     // element strides of O for b, h, n
   int B, H, Nq, Nk;
   float c;                      // scale * log2(e): scores enter exp2 in log2 units
-  int grid_h, grid_w, window;   // neighbourhood masks only
+  int grid_h, grid_w;           // neighbourhood masks only: token grid
+  int window_h, window_w;       // window size along the rows and the columns
   int dilation;                 // neighbourhood masks: key stride along each axis (>= 1)
   int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head
   int n_kv;                     // ceil(Nk / 128)

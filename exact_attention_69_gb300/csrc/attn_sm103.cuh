@@ -449,20 +449,20 @@ __host__ __device__ __forceinline__ bool axis_meets_nd(int c0, int c1, int e0, i
 // Does any query in rows [q0, q1) attend any key in [k0, k1)? The Q and K
 // ranges are cut into their grid-row segments; exact for dilation 1, a
 // superset for dilation > 1 (see axis_meets_dilated).
-template <bool WRAP, bool DIL>
+template <bool WRAP_H, bool WRAP_W, bool DIL>
 __host__ __device__ __forceinline__ bool na_tile_meets(int q0, int q1, int k0, int k1, const KernelParams& p) {
   const int W = p.grid_w;
   const int kr0 = k0 / W, kr1 = (k1 - 1) / W;
   for (int qa = q0; qa < q1;) {
     const int qr = qa / W;
     const int qb = min(q1, (qr + 1) * W);
-    if (axis_meets_nd<WRAP, DIL>(qr, qr, kr0, kr1, p.grid_h, p.window, p.dilation)) {
+    if (axis_meets_nd<WRAP_H, DIL>(qr, qr, kr0, kr1, p.grid_h, p.window_h, p.dilation)) {
       for (int ka = k0; ka < k1;) {
         const int kr = ka / W;
         const int kb = min(k1, (kr + 1) * W);
-        if (axis_meets_nd<WRAP, DIL>(qr, qr, kr, kr, p.grid_h, p.window, p.dilation) &&
-            axis_meets_nd<WRAP, DIL>(qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W, W,
-                                p.window, p.dilation))
+        if (axis_meets_nd<WRAP_H, DIL>(qr, qr, kr, kr, p.grid_h, p.window_h, p.dilation) &&
+            axis_meets_nd<WRAP_W, DIL>(qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W,
+                                       W, p.window_w, p.dilation))
           return true;
         ka = kb;
       }
@@ -484,7 +484,8 @@ __host__ __device__ __forceinline__ int tile_class(int q0, int j, const KernelPa
     if (k0 > q1 - 1) return 0;
     return (!ragged && k0 + kBN - 1 <= q0) ? 1 : 2;
   }
-  return na_tile_meets<mask_na_wrap(MASK), mask_na_dilated(MASK)>(q0, q1, k0, min(k0 + kBN, p.Nk), p)
+  return na_tile_meets<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
+             q0, q1, k0, min(k0 + kBN, p.Nk), p)
              ? 2 : 0;
 }
 
@@ -584,13 +585,13 @@ __host__ __device__ __forceinline__ int na_window_first(int c, int G, int w, int
 
 // Grid coordinates of query token q and the first key coordinates of its
 // window along each axis.
-template <bool WRAP, bool DIL>
+template <bool WRAP_H, bool WRAP_W, bool DIL>
 __host__ __device__ __forceinline__ void na_query_coords(const KernelParams& p, int q, int& qy,
                                                          int& qx, int& wy, int& wx) {
   qy = q / p.grid_w;
   qx = q - qy * p.grid_w;
-  wy = na_window_first<WRAP, DIL>(qy, p.grid_h, p.window, p.dilation);
-  wx = na_window_first<WRAP, DIL>(qx, p.grid_w, p.window, p.dilation);
+  wy = na_window_first<WRAP_H, DIL>(qy, p.grid_h, p.window_h, p.dilation);
+  wx = na_window_first<WRAP_W, DIL>(qx, p.grid_w, p.window_w, p.dilation);
 }
 
 // Is key coordinate k in the window that starts at f (stride dl, w keys)?
@@ -616,27 +617,28 @@ __host__ __device__ __forceinline__ void set_bits(uint32_t (&bits)[4], int lo, i
 }
 
 // Allowed keys of query (qy, qx) in the K/V tile starting at key k0, as bits
-// of a 128-bit mask (bit i: key k0 + i). The window's rows are wy + dl * t and
-// its columns wx + dl * t, t in [0, w) (modulo the grid side for wrap). With
-// dilation 1 a row's allowed columns form one interval (two when a wrapped
-// window crosses the last column); with dilation > 1 they are set one by one.
-template <bool WRAP, bool DIL>
+// of a 128-bit mask (bit i: key k0 + i). The window's rows are wy + dl * t,
+// t in [0, w_h), and its columns wx + dl * t, t in [0, w_w) (modulo the grid
+// side along an axis that wraps). With dilation 1 a row's allowed columns
+// form one interval (two when a wrapped window crosses the last column); with
+// dilation > 1 they are set one by one.
+template <bool WRAP_H, bool WRAP_W, bool DIL>
 __host__ __device__ __forceinline__ void na_tile_bits(const KernelParams& p, int k0, int qy, int qx, int wy,
                                              int wx, uint32_t (&bits)[4]) {
-  const int G_h = p.grid_h, G_w = p.grid_w, w = p.window, dl = p.dilation;
+  const int G_h = p.grid_h, G_w = p.grid_w, w_h = p.window_h, w = p.window_w, dl = p.dilation;
   bits[0] = bits[1] = bits[2] = bits[3] = 0u;
   const int nvalid = min(kBN, p.Nk - k0);
   int ky = k0 / G_w;
   int kx0 = k0 - ky * G_w;
   for (int i = 0; i < nvalid; ++ky) {
     const int len = min(G_w - kx0, nvalid - i);  // this row's columns [kx0, kx0 + len)
-    if (na_in_window<WRAP, DIL>(ky, wy, G_h, w, dl)) {
+    if (na_in_window<WRAP_H, DIL>(ky, wy, G_h, w_h, dl)) {
       const int base = i - kx0;  // bit of column 0 of this row
       if (!DIL) {
         const int e1 = min(wx + w, G_w);
         int lo = max(wx, kx0), hi = min(e1, kx0 + len);
         if (lo < hi) set_bits(bits, base + lo, base + hi);
-        if (WRAP && wx + w > G_w) {  // the window wraps past the last column
+        if (WRAP_W && wx + w > G_w) {  // the window wraps past the last column
           lo = kx0;
           hi = min(wx + w - G_w, kx0 + len);
           if (lo < hi) set_bits(bits, base + lo, base + hi);
@@ -644,7 +646,7 @@ __host__ __device__ __forceinline__ void na_tile_bits(const KernelParams& p, int
       } else {
         for (int t = 0; t < w; ++t) {
           int cx = wx + dl * t;
-          if (WRAP && cx >= G_w) cx -= G_w;
+          if (WRAP_W && cx >= G_w) cx -= G_w;
           if (cx >= kx0 && cx < kx0 + len) {
             const int bit = base + cx;
             bits[bit >> 5] |= 1u << (bit & 31);
@@ -1037,7 +1039,8 @@ __device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams
     // keys as a 128-bit mask, one column interval per row segment,
     // then clear the rest with independent selects.
     uint32_t bits[4];
-    na_tile_bits<mask_na_wrap(MASK), mask_na_dilated(MASK)>(p, k0, qy, qx, wy, wx, bits);
+    na_tile_bits<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
+        p, k0, qy, qx, wy, wx, bits);
 #pragma unroll
     for (int i = 0; i < 128; ++i)
       if (((bits[i >> 5] >> (i & 31)) & 1u) == 0u) s[i] = neg_inf;
@@ -1095,7 +1098,8 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     // neighbourhood: this query's grid coordinates and clamped window starts
     int qy = 0, qx = 0, wy = 0, wx = 0;
     if (mask_is_na(MASK))
-      na_query_coords<mask_na_wrap(MASK), mask_na_dilated(MASK)>(p, q, qy, qx, wy, wx);
+      na_query_coords<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
+          p, q, qy, qx, wy, wx);
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
@@ -1292,10 +1296,14 @@ cudaError_t launch_dim(const KernelParams& p, int mask, int grid, cudaStream_t s
   switch (mask) {
     case kMaskNone: return launch_mask<D, kMaskNone>(p, grid, s);
     case kMaskCausal: return launch_mask<D, kMaskCausal>(p, grid, s);
-    case kMaskNaClamp: return launch_mask<D, kMaskNaClamp>(p, grid, s);
-    case kMaskNaWrap: return launch_mask<D, kMaskNaWrap>(p, grid, s);
-    case kMaskNaClampDil: return launch_mask<D, kMaskNaClampDil>(p, grid, s);
-    case kMaskNaWrapDil: return launch_mask<D, kMaskNaWrapDil>(p, grid, s);
+    case kMaskNa + 0: return launch_mask<D, kMaskNa + 0>(p, grid, s);
+    case kMaskNa + 1: return launch_mask<D, kMaskNa + 1>(p, grid, s);
+    case kMaskNa + 2: return launch_mask<D, kMaskNa + 2>(p, grid, s);
+    case kMaskNa + 3: return launch_mask<D, kMaskNa + 3>(p, grid, s);
+    case kMaskNa + 4: return launch_mask<D, kMaskNa + 4>(p, grid, s);
+    case kMaskNa + 5: return launch_mask<D, kMaskNa + 5>(p, grid, s);
+    case kMaskNa + 6: return launch_mask<D, kMaskNa + 6>(p, grid, s);
+    case kMaskNa + 7: return launch_mask<D, kMaskNa + 7>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

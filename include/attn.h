@@ -27,15 +27,19 @@
  *   ATTN_MASK_NONE   every key j < Nk.
  *   ATTN_MASK_CAUSAL j <= i (top-left alignment, also when Nq != Nk).
  *   ATTN_MASK_NA2D   tokens are row-major on a grid_h x grid_w grid (Nq = Nk =
- *                    grid_h * grid_w); per axis the window holds `window` (odd)
- *                    positions: clamp mode (wrap = 0) shifts a full window
- *                    inward at the borders, start = clamp(c - window/2, 0,
- *                    G - window); wrap mode (wrap = 1) takes the positions
- *                    (c + t) mod G, t in [-window/2, window/2]. With dilation
- *                    dl > 1 (NATTEN's convention): clamp keeps the keys of
- *                    c's residue class modulo dl and applies the rule above
- *                    to the index inside that class; wrap takes
- *                    (c + dl * t) mod G. window * dl <= each grid side.
+ *                    grid_h * grid_w); along each axis the window holds k
+ *                    positions (k odd: `window` along the rows, `window_w`
+ *                    along the columns, 0 = `window`). A clamped axis shifts a
+ *                    full window inward at the borders, start = clamp(c - k/2,
+ *                    0, G - k); a wrapped axis takes the positions (c + t)
+ *                    mod G, t in [-k/2, k/2]. `wrap`: 0 = neither axis wraps,
+ *                    1 = both, 2 = the rows only, 3 = the columns only. With
+ *                    dilation dl > 1 (NATTEN's convention): a clamped axis
+ *                    keeps the keys of c's residue class modulo dl and applies
+ *                    the rule above to the index inside that class; a wrapped
+ *                    axis takes (c + dl * t) mod G. k * dl <= the grid side of
+ *                    its axis, unless k = 1. A 1 x N grid with window 1 along
+ *                    the rows is 1-D neighbourhood attention.
  *
  * Data layout (device memory, owned and allocated by the caller):
  *   q, o : bf16 [B, H, Nq, d]   k, v : bf16 [B, H, Nk, d]   (contiguous by
@@ -72,7 +76,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 typedef enum {
   ATTN_MASK_NONE = 0,
@@ -105,9 +109,11 @@ typedef struct attn_params_ex {
   int B, H, Nq, Nk, d;
   float scale;     /* > 0 and finite, typically 1/sqrt(d) */
   int mask_kind;   /* attn_mask_kind */
-  int window;      /* NA2D: odd window size; others: must be 0 */
+  int window;      /* NA2D: odd window size along the rows (and the columns
+                      unless window_w is set); others: must be 0 */
   int dilation;    /* NA2D: key stride >= 1 along each axis; others: must be 1 */
-  int wrap;        /* NA2D: 0 = clamp, 1 = wrap; others: must be 0 */
+  int wrap;        /* NA2D: 0 = clamp, 1 = wrap both axes, 2 = wrap the rows,
+                      3 = wrap the columns; others: must be 0 */
   int grid_h, grid_w; /* NA2D token grid; 0,0 = square grid of side sqrt(Nq) */
   /* element strides of dims (b, h, n); all zero = contiguous [B,H,N,d] */
   int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
@@ -127,6 +133,8 @@ typedef struct attn_params_ex {
                       before its first use (later calls leave it reusable);
                       NULL = the library's own */
   uint64_t workspace_bytes; /* size of `workspace` */
+  int window_w;    /* NA2D: odd window size along the columns; 0 = `window`;
+                      others: must be 0 */
 } attn_params_ex;
 
 /* Fill *p with defaults (zero pointers and sizes, dilation 1, contiguous). */

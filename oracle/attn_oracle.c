@@ -118,7 +118,10 @@ static int check_args(const problem_t* p, int B, int H) {
     if (p->window_h < 1 || p->window_h % 2 == 0 || p->window_w < 1 || p->window_w % 2 == 0)
       return -1;
     if (p->dilation < 1) return -1;
-    if (p->window_h * p->dilation > p->grid_h || p->window_w * p->dilation > p->grid_w) return -1;
+    /* every residue class of an axis holds at least k members (clamp), and the
+     * k wrapped keys are distinct (wrap), iff k = 1 or k * dilation <= G */
+    if (p->window_h > 1 && p->window_h * p->dilation > p->grid_h) return -1;
+    if (p->window_w > 1 && p->window_w * p->dilation > p->grid_w) return -1;
   }
   return 0;
 }

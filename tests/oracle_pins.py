@@ -351,6 +351,17 @@ def one_d_closed_form(orc):
                 assert clamp == (s0 <= j < s0 + k), (N, k, i, j)
                 dist = min((j - i) % N, (i - j) % N)
                 assert wrap == (dist <= k // 2), (N, k, i, j)
+    # dilated, clamp: the keys of i's residue class mod dl, k of them, the
+    # window of positions inside that class shifted inward at its ends
+    for (N, k, dl) in ((20, 3, 3), (17, 5, 2), (9, 3, 3)):
+        for i in range(N):
+            members = list(range(i % dl, N, dl))
+            a0 = min(max(members.index(i) - k // 2, 0), len(members) - k)
+            want = set(members[a0:a0 + k])
+            got = {j for j in range(N)
+                   if orc.allowed(i, j, Nq=N, Nk=N, mask_kind="clamp", window=(1, k),
+                                  dilation=dl, grid=(1, N))}
+            assert got == want, (N, k, dl, i)
 
 
 def row_subset_matches_full(orc):

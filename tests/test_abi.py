@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.attn_params_size() == ctypes.sizeof(_lib.AttnParamsEx)
-    assert lib.attn_abi_version() == 2
+    assert lib.attn_abi_version() == 3
 
 
 def test_error_strings(lib):
@@ -67,6 +67,10 @@ BAD = [
     ("na_bad_grid", dict(mask_kind=2, window=3, grid_h=10, grid_w=20), _lib.ATTN_ERR_INVALID_ARG),
     ("na_dilation0", dict(mask_kind=2, window=3, dilation=0), _lib.ATTN_ERR_INVALID_ARG),
     ("na_dilated_window_too_big", dict(mask_kind=2, window=3, dilation=6), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_wrap4", dict(mask_kind=2, window=3, wrap=4), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_even_window_w", dict(mask_kind=2, window=3, window_w=2), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_window_w_too_big", dict(mask_kind=2, window=3, window_w=17), _lib.ATTN_ERR_INVALID_ARG),
+    ("window_w_without_na", dict(window_w=3), _lib.ATTN_ERR_INVALID_ARG),
     ("null_q", dict(q=None), _lib.ATTN_ERR_INVALID_ARG),
     ("misaligned_k", dict(k=(1 << 20) + 8), _lib.ATTN_ERR_MISALIGNED),
     ("misaligned_lse", dict(lse=(1 << 20) + 2), _lib.ATTN_ERR_MISALIGNED),

@@ -50,15 +50,16 @@ def check(o, lse, ref_o, ref_lse, rows=None):
 
 
 def run(E, B, H, Nq, Nk, d, mask="none", window=0, grid=None, sigma=1.0, seed=1, rows=None,
-        num_ctas=0, scale=None, dilation=1):
+        num_ctas=0, scale=None, dilation=1, wrap_axes=None):
     q, k, v = make_qkv(B, H, Nq, Nk, d, sigma, seed)
     scale = scale if scale is not None else 1.0 / math.sqrt(d)
     o, lse = E.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, mask=mask, window=window,
-                        dilation=dilation, grid=grid, num_ctas=num_ctas)
+                        dilation=dilation, grid=grid, num_ctas=num_ctas, wrap_axes=wrap_axes)
     _status_ok(E)
     ref_o, ref_lse = oracle.attention_rows(to_f64(q), to_f64(k), to_f64(v), rows, scale=scale,
                                            mask_kind=mask, window=window, dilation=dilation,
-                                           grid=grid)
+                                           grid=grid,
+                                           wrap=wrap_axes if wrap_axes is not None else False)
     return check(o, lse, ref_o, ref_lse, rows)
 
 
@@ -100,6 +101,37 @@ NA_DILATED = [(8, 8, 3, 2), (16, 16, 5, 3), (20, 12, 3, 4), (13, 29, 3, 4), (24,
 def test_neighbourhood_dilated(E, mode, gh, gw, win, dil, d):
     run(E, 1, 2, gh * gw, gh * gw, d, mode, window=win, dilation=dil, grid=(gh, gw),
         seed=gh * gw + 31 * win + dil)
+
+
+# per-axis windows and wrap: (grid, (k_rows, k_cols), (wrap_rows, wrap_cols), dilation)
+NA_AXES = [((16, 24), (3, 7), (True, False), 1), ((20, 20), (5, 3), (False, True), 1),
+           ((32, 64), (7, 5), (True, True), 1), ((48, 40), (5, 3), (True, False), 4),
+           ((13, 29), (1, 9), (False, True), 2), ((1, 1000), (1, 15), (False, False), 1),
+           ((1, 1000), (1, 15), (False, True), 1), ((1, 777), (1, 9), (False, False), 3),
+           ((1, 4096), (1, 63), (False, False), 1)]
+
+
+@pytest.mark.parametrize("grid,win,wrap_axes,dil", NA_AXES)
+@pytest.mark.parametrize("d", [32, 64])
+def test_neighbourhood_per_axis(E, grid, win, wrap_axes, dil, d):
+    N = grid[0] * grid[1]
+    run(E, 1, 2, N, N, d, "clamp", window=win, dilation=dil, grid=grid, wrap_axes=wrap_axes,
+        seed=N + 7 * win[0] + 13 * win[1] + dil)
+
+
+def test_na2d_heads_last_per_axis_modes(E):
+    B, X, Y, H, d = 1, 12, 20, 2, 32
+    q, k, v = (torch.randn(B, X, Y, H, d, generator=torch.Generator().manual_seed(s)).to(
+        torch.bfloat16) for s in (1, 2, 3))
+    o = E.na2d(q.cuda(), k.cuda(), v.cuda(), (5, 3), mode=("wrap", "clamp"))
+    _status_ok(E)
+    to_bhnd = lambda t: t.float().permute(0, 3, 1, 2, 4).reshape(B, H, X * Y, d)
+    ref_o, _ = oracle.attention_rows(to_bhnd(q).numpy(), to_bhnd(k).numpy(), to_bhnd(v).numpy(),
+                                     None, scale=1 / math.sqrt(d), mask_kind="clamp",
+                                     window=(5, 3), wrap=(True, False), grid=(X, Y))
+    got = to_bhnd(o.cpu()).numpy()
+    err = np.abs(got - ref_o)
+    assert (err <= ATOL + RTOL * np.abs(ref_o)).all(), float(err.max())
 
 
 def test_neighbourhood_dilated_d128_and_persistent(E):

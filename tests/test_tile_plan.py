@@ -18,7 +18,7 @@ import pytest
 from oracle import reference_np as twin
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-MASK_CODE = {"none": 0, "causal": 1, "clamp": 2, "wrap": 3}
+KIND = {"none": 0, "causal": 1, "clamp": 2, "wrap": 2}
 
 
 @pytest.fixture(scope="module")
@@ -32,10 +32,10 @@ def plan(tmp_path_factory):
                     "-I", os.path.join(ROOT, "exact_attention_69_gb300", "csrc"),
                     os.path.join(ROOT, "tests", "host", "tile_plan.cu"), "-o", out], check=True)
     lib = ctypes.CDLL(out)
-    lib.tile_class_host.argtypes = [ctypes.c_int] * 9
+    lib.tile_class_host.argtypes = [ctypes.c_int] * 12
     lib.tile_class_host.restype = ctypes.c_int
     lib.decode_task_host.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
-    lib.na_bits_host.argtypes = [ctypes.c_int] * 8 + [ctypes.POINTER(ctypes.c_uint)]
+    lib.na_bits_host.argtypes = [ctypes.c_int] * 10 + [ctypes.POINTER(ctypes.c_uint)]
     return lib
 
 
@@ -59,11 +59,30 @@ DILATED = [
     ("clamp", 64, 64, (8, 8), 3, 2), ("wrap", 64, 64, (8, 8), 3, 2),
 ]
 
+# per-axis windows and wrap: (grid, (k_rows, k_cols), (wrap_rows, wrap_cols), dilation)
+AXES = [
+    ((64, 64), (7, 3), (True, False), 1), ((64, 64), (3, 9), (False, True), 1),
+    ((20, 60), (5, 11), (False, False), 1), ((20, 60), (1, 9), (True, True), 1),
+    ((1, 4096), (1, 31), (False, False), 1), ((1, 4096), (1, 31), (False, True), 1),
+    ((1, 700), (1, 9), (False, False), 3), ((48, 40), (5, 3), (True, False), 4),
+    ((30, 160), (9, 5), (False, True), 2), ((13, 29), (3, 7), (True, False), 1),
+]
 
-@pytest.mark.parametrize("mask,Nq,Nk,grid,window,dilation",
-                         [c + (1,) for c in CASES] + DILATED)
-def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window, dilation):
-    allowed = twin.mask_matrix(Nq, Nk, mask, window, dilation, grid)
+
+def _na_args(mask, window, wrap_axes):
+    kh, kw = (window, window) if isinstance(window, int) else window
+    if wrap_axes is None:
+        wrap_axes = (mask == "wrap", mask == "wrap")
+    return kh, kw, int(wrap_axes[0]), int(wrap_axes[1])
+
+
+@pytest.mark.parametrize("mask,Nq,Nk,grid,window,dilation,wrap_axes",
+                         [c + (1, None) for c in CASES] + [c + (None,) for c in DILATED] +
+                         [("clamp", g[0] * g[1], g[0] * g[1], g, win, dil, wr)
+                          for (g, win, wr, dil) in AXES])
+def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window, dilation, wrap_axes):
+    allowed = twin.mask_matrix(Nq, Nk, mask, window, dilation, grid, wrap_axes)
+    kh, kw, wh, ww = _na_args(mask, window, wrap_axes)
     gh, gw = grid if grid else (0, 0)
     n_kv = -(-Nk // 128)
     visited = wasted = 0
@@ -71,7 +90,7 @@ def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window, dilati
         rows = allowed[q0:min(q0 + 128, Nq)]
         for j in range(n_kv):
             block = rows[:, j * 128:min(j * 128 + 128, Nk)]
-            c = plan.tile_class_host(MASK_CODE[mask], q0, j, Nq, Nk, gh, gw, window, dilation)
+            c = plan.tile_class_host(KIND[mask], q0, j, Nq, Nk, gh, gw, kh, kw, dilation, wh, ww)
             assert c in (0, 1, 2)
             if c == 0:
                 assert not block.any(), (q0, j)
@@ -92,7 +111,7 @@ def test_tasks_cover_every_q_tile_once(plan, mask):
     seen = set()
     out = (ctypes.c_int * 3)()
     for t in range(B * H * n_qpairs):
-        plan.decode_task_host(MASK_CODE[mask], t, B, H, Nq, out)
+        plan.decode_task_host(KIND[mask], t, B, H, Nq, out)
         key = (out[0], out[1], out[2])
         assert key not in seen
         seen.add(key)
@@ -108,19 +127,24 @@ def test_tasks_cover_every_q_tile_once(plan, mask):
     ("clamp", 30, 160, 9, 1), ("wrap", 39, 39, 39, 1), ("clamp", 12, 20, 1, 1),
     ("clamp", 8, 8, 3, 2), ("wrap", 8, 8, 3, 2), ("clamp", 20, 20, 5, 3), ("wrap", 20, 20, 5, 4),
     ("clamp", 13, 29, 3, 4), ("wrap", 13, 29, 3, 4), ("clamp", 64, 64, 7, 2), ("wrap", 64, 64, 7, 9),
-    ("wrap", 21, 21, 7, 3), ("clamp", 21, 35, 3, 7)])
+    ("wrap", 21, 21, 7, 3), ("clamp", 21, 35, 3, 7)] +
+    [("axes", g[0], g[1], (win, wr), dil) for (g, win, wr, dil) in AXES])
 def test_in_tile_mask_bits_match_oracle_mask(plan, mode, gh, gw, window, dilation):
     """The kernel's in-tile neighbourhood mask, bit for bit, against the oracle
     twin's allowed-set matrix, for every query and every K/V tile."""
     N = gh * gw
-    allowed = twin.mask_matrix(N, N, mode, window, dilation, (gh, gw))
+    if mode == "axes":
+        (window, wrap_axes), mode = window, "clamp"
+    else:
+        wrap_axes = None
+    allowed = twin.mask_matrix(N, N, mode, window, dilation, (gh, gw), wrap_axes)
+    kh, kw, wh, ww = _na_args(mode, window, wrap_axes)
     out = (ctypes.c_uint * 4)()
     rng = np.random.default_rng(0)
     queries = range(N) if N <= 1600 else rng.choice(N, 400, replace=False)
     for q in queries:
         for k0 in range(0, N, 128):
-            plan.na_bits_host(1 if mode == "wrap" else 0, int(q), k0, N, gh, gw, window, dilation,
-                              out)
+            plan.na_bits_host(int(q), k0, N, gh, gw, kh, kw, dilation, wh, ww, out)
             bits = np.array([(out[i >> 5] >> (i & 31)) & 1 for i in range(128)], dtype=bool)
             ref = np.zeros(128, dtype=bool)
             n = min(128, N - k0)
