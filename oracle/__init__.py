@@ -17,6 +17,9 @@ exp(s_ij). Sources: "Fused Self Attention" (NKI tutorial), section
 "Background"; "Profiling in PyTorch" part 3, section "Deconstructing Naive
 Attention" (scale, masked_fill with -inf, softmax, matmul); NATTEN issue #142
 for the neighbourhood windows and the float32 logsumexp output.
+
+The backward pass (``attention_bwd``) gives dq, dk, dv of a loss whose gradient at
+the output is dout, by the chain rule through the same definition.
 """
 from .oracle import (  # noqa: F401
     MASK_CAUSAL,
@@ -27,6 +30,7 @@ from .oracle import (  # noqa: F401
     Oracle,
     allowed,
     attention,
+    attention_bwd,
     attention_rows,
     build,
     compile_oracle,

@@ -214,6 +214,109 @@ int oracle_attn_rows(const double* q, const double* k, const double* v,
   return failed ? -2 : 0;
 }
 
+/*
+ * Backward pass (the gradients of a scalar loss L through the forward above),
+ * for one (batch, head), row by row in fp64. With P_ij = exp(s_ij - lse_i) the
+ * softmax weights of row i (0 outside A(i)) and dO the gradient of L at O:
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   D_i   = dO_i . o_i              (= sum_j P_ij dP_ij)
+ *   dS_ij = P_ij (dP_ij - D_i)       (the softmax Jacobian applied to dP)
+ *   dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i
+ * which is the chain rule through s = scale q.k, the row softmax and o = P v.
+ * Sources: the forward's sources above (S = Q K^T, the row softmax, R = S V);
+ * the backward itself is the textbook chain rule.
+ */
+static void one_head_bwd(const problem_t* p, const double* q, const double* k, const double* v,
+                         const double* dout, double* dq, double* dk, double* dv, double* s,
+                         unsigned char* ok, double* pw, double* dp) {
+  const int Nq = p->Nq, Nk = p->Nk, d = p->d;
+  for (int64_t x = 0; x < (int64_t)Nk * d; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+  for (int i = 0; i < Nq; ++i) {
+    const double* qi = q + (int64_t)i * d;
+    const double* gi = dout + (int64_t)i * d;
+    double M = -INFINITY;
+    int any = 0;
+    for (int j = 0; j < Nk; ++j) {
+      ok[j] = (unsigned char)allowed(p, i, j);
+      if (!ok[j]) continue;
+      double dot = 0.0;
+      for (int t = 0; t < d; ++t) dot += qi[t] * k[(int64_t)j * d + t];
+      s[j] = p->scale * dot;
+      if (!any || s[j] > M) M = s[j];
+      any = 1;
+    }
+    double* dqi = dq + (int64_t)i * d;
+    for (int t = 0; t < d; ++t) dqi[t] = 0.0;
+    if (!any) continue;
+    double l = 0.0;
+    for (int j = 0; j < Nk; ++j)
+      if (ok[j]) l += exp(s[j] - M);
+    /* o_i (for D_i), the weights P_ij and dP_ij */
+    double Di = 0.0;
+    for (int t = 0; t < d; ++t) {
+      double ot = 0.0;
+      for (int j = 0; j < Nk; ++j)
+        if (ok[j]) ot += exp(s[j] - M) / l * v[(int64_t)j * d + t];
+      Di += gi[t] * ot;
+    }
+    for (int j = 0; j < Nk; ++j) {
+      if (!ok[j]) continue;
+      pw[j] = exp(s[j] - M) / l;
+      double g = 0.0;
+      for (int t = 0; t < d; ++t) g += gi[t] * v[(int64_t)j * d + t];
+      dp[j] = g;
+    }
+    for (int j = 0; j < Nk; ++j) {
+      if (!ok[j]) continue;
+      const double dsij = pw[j] * (dp[j] - Di);
+      for (int t = 0; t < d; ++t) {
+        dqi[t] += p->scale * dsij * k[(int64_t)j * d + t];
+        dk[(int64_t)j * d + t] += p->scale * dsij * qi[t];
+        dv[(int64_t)j * d + t] += pw[j] * gi[t];
+      }
+    }
+  }
+}
+
+/*
+ * q, dout: [B,H,Nq,d]; k, v: [B,H,Nk,d]; outputs dq [B,H,Nq,d], dk and dv
+ * [B,H,Nk,d]; all fp64 contiguous. Mask arguments as oracle_attn_rows.
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
+                    double* dq, double* dk, double* dv, int B, int H, int Nq, int Nk, int d,
+                    double scale, int mask_kind, int window_h, int window_w, int dilation,
+                    int wrap_h, int wrap_w, int grid_h, int grid_w, int nthreads) {
+  problem_t p = {Nq, Nk, d, scale, mask_kind, window_h, window_w, dilation,
+                 wrap_h, wrap_w, grid_h, grid_w};
+  if (check_args(&p, B, H) != 0) return -1;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  int failed = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)Nk * 3);
+    unsigned char* ok = (unsigned char*)malloc((size_t)Nk);
+    if (!s || !ok) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        const int64_t qo = bh * (int64_t)Nq * d, ko = bh * (int64_t)Nk * d;
+        one_head_bwd(&p, q + qo, k + ko, v + ko, dout + qo, dq + qo, dk + ko, dv + ko, s, ok,
+                     s + Nk, s + 2 * (int64_t)Nk);
+      }
+    }
+    free(s);
+    free(ok);
+  }
+  return failed ? -2 : 0;
+}
+
 /* Number of threads the OpenMP runtime will use (for reporting). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -88,6 +88,9 @@ class Oracle:
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int,
         ]
+        lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [ctypes.c_double] + \
+            [ctypes.c_int] * 9
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_allowed.restype = ctypes.c_int
         lib.oracle_allowed.argtypes = [ctypes.c_int] * 12
@@ -133,6 +136,31 @@ class Oracle:
             raise ValueError(f"oracle rejected the problem (code {rc})")
         return o, lse
 
+    def attention_bwd(self, q, k, v, dout, *, scale, mask_kind=MASK_NONE, window=0, dilation=1,
+                      wrap=False, grid=None, nthreads=0):
+        """Gradients (dq, dk, dv) in fp64 of a loss whose gradient at the output O is
+        dout [B, H, Nq, d]; q [B, H, Nq, d], k and v [B, H, Nk, d]. Mask arguments as
+        attention_rows."""
+        kh, kw, wh, ww = _axes(mask_kind, window, wrap)
+        if isinstance(mask_kind, str):
+            mask_kind = MASK_CODES[mask_kind]
+        q, k, v, dout = (np.ascontiguousarray(np.asarray(t, dtype=np.float64))
+                         for t in (q, k, v, dout))
+        B, H, Nq, d = q.shape
+        Nk = k.shape[2]
+        assert k.shape == (B, H, Nk, d) and v.shape == (B, H, Nk, d) and dout.shape == q.shape
+        gh, gw = _grid(mask_kind, Nq, grid)
+        dq = np.empty_like(q)
+        dk = np.empty_like(k)
+        dv = np.empty_like(v)
+        rc = self._lib.oracle_attn_bwd(_dptr(q), _dptr(k), _dptr(v), _dptr(dout), _dptr(dq),
+                                       _dptr(dk), _dptr(dv), B, H, Nq, Nk, d, float(scale),
+                                       int(mask_kind), kh, kw, int(dilation), wh, ww, gh, gw,
+                                       int(nthreads))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the problem (code {rc})")
+        return dq, dk, dv
+
     def attention(self, q, k, v, **kw):
         """Every row; see attention_rows."""
         return self.attention_rows(q, k, v, None, **kw)
@@ -163,6 +191,10 @@ def default() -> Oracle:
 
 def attention_rows(*a, **kw):
     return default().attention_rows(*a, **kw)
+
+
+def attention_bwd(*a, **kw):
+    return default().attention_bwd(*a, **kw)
 
 
 def attention(*a, **kw):

@@ -19,6 +19,11 @@ What pins what:
   one_axis_wrap_pad_clamp the same recipe along one axis == wrap along that axis only
   axis_windows_by_hand    literal key sets for a rectangular window and one-axis wrap
   one_d_closed_form       a 1 x N grid is 1-D neighbourhood attention: closed-form windows
+  bwd_autograd_fp64       backward: torch autograd through an explicit fp64 forward
+  bwd_finite_differences  backward: central differences of sum(dO * O) along random directions
+  bwd_invariants          backward: a common shift of all keys leaves O unchanged (sum_j dK_j
+                          = 0); a common shift of V moves every o_i by it (sum_j dV_j =
+                          sum_i dO_i)
 """
 from __future__ import annotations
 
@@ -364,6 +369,68 @@ def one_d_closed_form(orc):
             assert got == want, (N, k, dl, i)
 
 
+BWD_CASES = [
+    dict(mask_kind="none", Nq=13, Nk=21),
+    dict(mask_kind="causal", Nq=17, Nk=17),
+    dict(mask_kind="causal", Nq=9, Nk=20),
+    dict(mask_kind="clamp", Nq=30, Nk=30, window=(3, 5), grid=(5, 6)),
+    dict(mask_kind="wrap", Nq=36, Nk=36, window=3, grid=(6, 6), dilation=2),
+]
+
+
+def _bwd_inputs(case, rng, d=6):
+    B, H = 1, 2
+    shapes = [(B, H, case["Nq"], d), (B, H, case["Nk"], d), (B, H, case["Nk"], d),
+              (B, H, case["Nq"], d)]
+    return [rng.standard_normal(sh) for sh in shapes]
+
+
+def bwd_autograd_fp64(orc):
+    import torch
+    rng = np.random.default_rng(21)
+    for case in BWD_CASES:
+        q, k, v, g = _bwd_inputs(case, rng)
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, scale=0.45, **_kw(case))
+        t = [torch.tensor(x, requires_grad=True) for x in (q, k, v)]
+        allowed = torch.from_numpy(_twin_mask(case))
+        sc = (0.45 * t[0] @ t[1].transpose(-1, -2)).masked_fill(~allowed, float("-inf"))
+        o = torch.softmax(sc, dim=-1) @ t[2]
+        (o * torch.from_numpy(g)).sum().backward()
+        for name, ref, got in (("dq", t[0].grad, dq), ("dk", t[1].grad, dk), ("dv", t[2].grad, dv)):
+            err = np.max(np.abs(ref.numpy() - got))
+            assert err < 1e-12, (case, name, err)
+
+
+def bwd_finite_differences(orc):
+    rng = np.random.default_rng(22)
+    h = 1e-5
+    for case in BWD_CASES:
+        q, k, v, g = _bwd_inputs(case, rng)
+        grads = orc.attention_bwd(q, k, v, g, scale=0.45, **_kw(case))
+        for which in range(3):
+            e = rng.standard_normal(grads[which].shape)
+
+            def loss(eps):
+                x = [q, k, v]
+                x[which] = x[which] + eps * e
+                o, _ = orc.attention(*x, scale=0.45, **_kw(case))
+                return float(np.sum(o * g))
+
+            fd = (loss(h) - loss(-h)) / (2 * h)
+            an = float(np.sum(grads[which] * e))
+            assert abs(fd - an) < 1e-7 * max(1.0, abs(an)), (case, which, fd, an)
+
+
+def bwd_invariants(orc):
+    rng = np.random.default_rng(23)
+    for case in BWD_CASES:
+        q, k, v, g = _bwd_inputs(case, rng)
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, scale=0.45, **_kw(case))
+        # every query row has a non-empty allowed set in these cases
+        assert np.max(np.abs(dk.sum(axis=2))) < 1e-12, case
+        assert np.max(np.abs(dv.sum(axis=2) - g.sum(axis=2))) < 1e-12, case
+
+
 def row_subset_matches_full(orc):
     rng = np.random.default_rng(14)
     q = _rand(2, 2, 33, 8, rng=rng)
@@ -393,5 +460,8 @@ def all_checks(goldens):
         ("one_axis_wrap_pad_clamp", one_axis_wrap_pad_clamp),
         ("axis_windows_by_hand", axis_windows_by_hand),
         ("one_d_closed_form", one_d_closed_form),
+        ("bwd_autograd_fp64", bwd_autograd_fp64),
+        ("bwd_finite_differences", bwd_finite_differences),
+        ("bwd_invariants", bwd_invariants),
         ("row_subset_matches_full", row_subset_matches_full),
     ]

@@ -33,6 +33,13 @@ MUTANTS = {
     "na_wrap_axes_swapped": ("const int row_ok = p->wrap_h ?", "const int row_ok = p->wrap_w ?"),
     "dilation_residue_ignored": ("if (kc % dl != residue) return 0;", ""),
     "softmax_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
+    "bwd_dropped_d_term": ("const double dsij = pw[j] * (dp[j] - Di);", "const double dsij = pw[j] * dp[j];"),
+    "bwd_dk_unscaled": ("dk[(int64_t)j * d + t] += p->scale * dsij * qi[t];",
+                        "dk[(int64_t)j * d + t] += dsij * qi[t];"),
+    "bwd_dv_wrong_weight": ("dv[(int64_t)j * d + t] += pw[j] * gi[t];",
+                            "dv[(int64_t)j * d + t] += dp[j] * gi[t];"),
+    "bwd_dp_wrong_operand": ("for (int t = 0; t < d; ++t) g += gi[t] * v[(int64_t)j * d + t];",
+                             "for (int t = 0; t < d; ++t) g += gi[t] * k[(int64_t)j * d + t];"),
 }
 
 
