@@ -65,6 +65,31 @@ class AttnParamsEx(ctypes.Structure):
     ]
 
 
+class AttnBwdParams(ctypes.Structure):
+    """Mirror of ``attn_bwd_params``."""
+
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p),
+        ("o", ctypes.c_void_p),
+        ("dout", ctypes.c_void_p),
+        ("lse", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p),
+        ("dk", ctypes.c_void_p),
+        ("dv", ctypes.c_void_p),
+        ("B", ctypes.c_int),
+        ("H", ctypes.c_int),
+        ("Nq", ctypes.c_int),
+        ("Nk", ctypes.c_int),
+        ("d", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("mask_kind", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+        ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
 class AttnError(RuntimeError):
     def __init__(self, code: int, message: str):
         super().__init__(message)
@@ -109,6 +134,10 @@ def load(path: str = LIB_PATH):
         lib.attn_abi_version.restype = i
         lib.attn_params_size.argtypes = []
         lib.attn_params_size.restype = i
+        lib.attn_bwd_params_init.argtypes = [ctypes.POINTER(AttnBwdParams)]
+        lib.attn_bwd_params_init.restype = None
+        lib.attn_bwd.argtypes = [ctypes.POINTER(AttnBwdParams)]
+        lib.attn_bwd.restype = i
         lib.attn_workspace_bytes.argtypes = [ctypes.POINTER(AttnParamsEx)]
         lib.attn_workspace_bytes.restype = ctypes.c_int64
         lib.attn_fwd_noalloc.argtypes = [ctypes.POINTER(AttnParamsEx)]
@@ -139,6 +168,16 @@ def params() -> AttnParamsEx:
 
 def fwd_ex(p: AttnParamsEx) -> int:
     return load().attn_fwd_ex(ctypes.byref(p))
+
+
+def bwd_params() -> AttnBwdParams:
+    p = AttnBwdParams()
+    load().attn_bwd_params_init(ctypes.byref(p))
+    return p
+
+
+def bwd(p: AttnBwdParams) -> int:
+    return load().attn_bwd(ctypes.byref(p))
 
 
 def device_status():

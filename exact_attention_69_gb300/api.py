@@ -136,6 +136,65 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
     return (out, lse) if return_lse else out
 
 
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, *, scale: float | None = None,
+             mask: str = "none", stream=None, timeout_ns: int = 0):
+    """Backward pass of attn_fwd: (dq, dk, dv) for the gradient dout at the output.
+
+    q, o, dout [B, H, Nq, d]; k, v [B, H, Nk, d] contiguous bf16 CUDA tensors;
+    lse the forward's float32 [B, H, Nq]. mask: 'none' | 'causal'.
+    """
+    if mask not in ("none", "causal"):
+        raise ValueError("the backward pass covers mask 'none' and 'causal'")
+    ts = (q, k, v, o, dout)
+    _check_dev(*ts)
+    if any(not t.is_contiguous() for t in ts) or not lse.is_contiguous():
+        raise ValueError("the backward pass takes contiguous tensors")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = _lib.bwd_params()
+    p.q, p.k, p.v, p.o, p.dout = (t.data_ptr() for t in ts)
+    p.lse = lse.data_ptr()
+    p.dq, p.dk, p.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
+    p.B, p.H, p.Nq, p.Nk, p.d = B, H, Nq, Nk, d
+    p.scale = float(scale)
+    p.mask_kind = _MASKS[mask]
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    p.stream = stream.cuda_stream
+    p.timeout_ns = int(timeout_ns)
+    with torch.cuda.device(q.device):
+        _lib.check(_lib.bwd(p), "attn_bwd")
+    return dq, dk, dv
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, scale, mask):
+        o, lse = attn_fwd(q, k, v, scale=scale, mask=mask)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale, ctx.mask = scale, mask
+        return o
+
+    @staticmethod
+    def backward(ctx, dout):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, dout.contiguous(), scale=ctx.scale, mask=ctx.mask)
+        return dq, dk, dv, None, None
+
+
+def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
+              mask: str = "none") -> torch.Tensor:
+    """attn_fwd as a differentiable torch op (no mask or causal; contiguous bf16 CUDA
+    tensors [B, H, N, d]): the backward pass runs attn_bwd."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _Attention.apply(q, k, v, float(scale), mask)
+
+
 def workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, *, mask: str = "none",
                     num_ctas: int = 0, schedule: int = 0) -> int:
     """Bytes of workspace an attn_fwd call of this shape needs on the current device."""

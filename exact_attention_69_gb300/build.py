@@ -22,7 +22,7 @@ LIB = os.path.join(HERE, "libattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["attn_host.cu", "attn_fwd_d32.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu"]
+SOURCES = ["attn_host.cu", "attn_fwd_d32.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu", "attn_bwd.cu"]
 
 
 def nvcc() -> str:

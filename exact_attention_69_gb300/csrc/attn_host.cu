@@ -32,6 +32,8 @@ struct DeviceState {
   void* ws = nullptr;          // workspace of split schedules (zero-filled when allocated)
   size_t ws_bytes = 0;
   uint32_t epoch = 0;          // tag of the last split call
+  float* dd = nullptr;         // backward scratch: rowsum(dO * O), grown when too small
+  size_t dd_bytes = 0;
 };
 
 std::mutex g_mu;
@@ -221,6 +223,10 @@ int device_state(DeviceState** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+  // make the device's primary context current on this thread: the tensor-map
+  // encoder is a driver call, and a thread may not have touched CUDA yet
+  // (e.g. an autograd worker thread)
+  if ((e = cudaSetDevice(dev)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState& s = g_dev[dev];
   if (s.status == nullptr) {
@@ -457,11 +463,14 @@ void attn_shutdown(void) {
       if (cudaSetDevice(i) == cudaSuccess) {
         cudaFree(g_dev[i].status);
         if (g_dev[i].ws) cudaFree(g_dev[i].ws);
+        if (g_dev[i].dd) cudaFree(g_dev[i].dd);
       }
       cudaSetDevice(prev);
       g_dev[i].status = nullptr;
       g_dev[i].ws = nullptr;
       g_dev[i].ws_bytes = 0;
+      g_dev[i].dd = nullptr;
+      g_dev[i].dd_bytes = 0;
     }
   }
 }
@@ -481,6 +490,89 @@ int64_t attn_workspace_bytes(const attn_params_ex* p) {
 }
 
 int attn_params_size(void) { return static_cast<int>(sizeof(attn_params_ex)); }
+
+void attn_bwd_params_init(attn_bwd_params* p) {
+  if (!p) return;
+  std::memset(p, 0, sizeof(*p));
+}
+
+int attn_bwd(const attn_bwd_params* p) {
+  t_err[0] = 0;
+  if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
+  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1)
+    return fail(ATTN_ERR_INVALID_ARG, "B, H, Nq, Nk must be >= 1");
+  if (p->d != 32 && p->d != 64 && p->d != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head dimension %d (need 32, 64 or 128)", p->d);
+  if (!(p->scale > 0.f) || !std::isfinite(p->scale))
+    return fail(ATTN_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (p->mask_kind == ATTN_MASK_NA2D)
+    return fail(ATTN_ERR_UNSUPPORTED, "the backward pass covers no mask and causal");
+  if (p->mask_kind != ATTN_MASK_NONE && p->mask_kind != ATTN_MASK_CAUSAL)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", p->mask_kind);
+  const int64_t BH = static_cast<int64_t>(p->B) * p->H;
+  if (BH * ((p->Nq + 127) / 128) >= (int64_t{1} << 31) || BH * ((p->Nk + 127) / 128) >= (int64_t{1} << 31))
+    return fail(ATTN_ERR_INVALID_ARG, "too many tiles");
+  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->dout, p->lse, p->dq, p->dk, p->dv};
+  for (const void* x : ptrs) {
+    if (!x) return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv must be non-null");
+    if (!aligned16(x)) return fail(ATTN_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
+  }
+  int rc;
+  if ((rc = get_encoder()) != ATTN_OK) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  const size_t need = static_cast<size_t>(BH) * p->Nq * sizeof(float);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (ds->dd_bytes < need) {
+      cudaError_t e;
+      if (ds->dd) {
+        if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+        cudaFree(ds->dd);
+        ds->dd = nullptr;
+        ds->dd_bytes = 0;
+      }
+      void* ptr = nullptr;
+      if ((e = cudaMalloc(&ptr, need)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(backward scratch)");
+      ds->dd = static_cast<float*>(ptr);
+      ds->dd_bytes = need;
+    }
+  }
+  attn::BwdParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  attn::KernelParams& kp = bp.f;
+  const int box_cols = p->d >= 64 ? 64 : 32;
+  const CUtensorMapSwizzle swz = p->d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const int64_t qs[3] = {static_cast<int64_t>(p->H) * p->Nq * p->d, static_cast<int64_t>(p->Nq) * p->d, p->d};
+  const int64_t ks[3] = {static_cast<int64_t>(p->H) * p->Nk * p->d, static_cast<int64_t>(p->Nk) * p->d, p->d};
+  if ((rc = encode_map(&kp.tm_q, p->q, p->d, p->Nq, p->H, p->B, qs, box_cols, swz, "q")) != ATTN_OK ||
+      (rc = encode_map(&kp.tm_k, p->k, p->d, p->Nk, p->H, p->B, ks, box_cols, swz, "k")) != ATTN_OK ||
+      (rc = encode_map(&kp.tm_v, p->v, p->d, p->Nk, p->H, p->B, ks, box_cols, swz, "v")) != ATTN_OK ||
+      (rc = encode_map(&bp.tm_do, p->dout, p->d, p->Nq, p->H, p->B, qs, box_cols, swz, "dout")) != ATTN_OK)
+    return rc;
+  kp.B = p->B;
+  kp.H = p->H;
+  kp.Nq = p->Nq;
+  kp.Nk = p->Nk;
+  kp.c = p->scale * 1.4426950408889634f;
+  kp.dilation = 1;
+  kp.n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
+  kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
+  kp.status = ds->status;
+  bp.o = p->o;
+  bp.dout = p->dout;
+  bp.lse = p->lse;
+  bp.dd = ds->dd;
+  bp.dq = p->dq;
+  bp.dk = p->dk;
+  bp.dv = p->dv;
+  bp.scale = p->scale;
+  const int mask = p->mask_kind == ATTN_MASK_CAUSAL ? attn::kMaskCausal : attn::kMaskNone;
+  cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
+  const cudaError_t e = attn::launch_bwd(bp, p->d, mask, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return ATTN_OK;
+}
 
 }  // extern "C"
 

@@ -75,9 +75,26 @@ struct KernelParams {
   uint32_t* status;             // device status word: code, role, tile, CTA
 };
 
+// Backward pass: the forward's parameters (maps of Q, K, V, shapes, masks,
+// status) plus dO and the gradients (all bf16 contiguous [B, H, N, d]).
+struct BwdParams {
+  KernelParams f;               // f.c = scale * log2(e)
+  CUtensorMap tm_do;            // dO, the same map shape as Q
+  const void* o;                // forward output
+  const void* dout;
+  const float* lse;             // forward log-sum-exp, natural log, [B, H, Nq]
+  float* dd;                    // scratch [B, H, Nq]: rowsum(dO * O)
+  void* dq;
+  void* dk;
+  void* dv;
+  float scale;
+};
+
 // Per-head-dimension launchers, defined in attn_fwd_d{32,64,128}.cu.
 cudaError_t launch_d32(const KernelParams& p, int mask, int grid, cudaStream_t s);
 cudaError_t launch_d64(const KernelParams& p, int mask, int grid, cudaStream_t s);
+// Backward launchers (D = rowsum(dO * O), dQ, then dK and dV), in attn_bwd.cu.
+cudaError_t launch_bwd(const BwdParams& p, int d, int mask, cudaStream_t s);
 cudaError_t launch_d128(const KernelParams& p, int mask, int grid, cudaStream_t s);
 
 }  // namespace attn

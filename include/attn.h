@@ -190,6 +190,44 @@ int attn_abi_version(void);
 int attn_params_size(void);
 
 /*
+ * Backward pass: the gradients of a scalar loss through attn_fwd, given the
+ * loss's gradient dout at the output O. With P the forward's softmax weights
+ * (recomputed from Q, K and the saved log-sum-exp) and D_i = dout_i . O_i:
+ *   dV = P^T dout,  dS = P * (dout V^T - D),  dQ = scale dS K,  dK = scale dS^T Q
+ * (the chain rule through S = Q K^T, the row softmax and R = S V of "Fused Self
+ * Attention", section "Background").
+ * Layout: q, o, dout, dq: bf16 [B, H, Nq, d]; k, v, dk, dv: bf16 [B, H, Nk, d];
+ * lse: fp32 [B, H, Nq] as written by attn_fwd; all contiguous, device memory
+ * owned by the caller, 16-byte aligned. mask_kind: ATTN_MASK_NONE or
+ * ATTN_MASK_CAUSAL (ATTN_MASK_NA2D: ATTN_ERR_UNSUPPORTED). dq, dk and dv are
+ * overwritten. Three kernels are enqueued on the stream (rowsum(dout * O),
+ * dQ, dK and dV); the library keeps a lazily grown per-device scratch of
+ * B*H*Nq floats for D, so calls on one device must not overlap in time.
+ */
+typedef struct attn_bwd_params {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, Nq, Nk, d;
+  float scale;          /* the forward's scale */
+  int mask_kind;        /* ATTN_MASK_NONE or ATTN_MASK_CAUSAL */
+  void* stream;         /* cudaStream_t; NULL = the calling thread's stream */
+  uint64_t timeout_ns;  /* bound on every device-side wait; 0 = 2 seconds */
+} attn_bwd_params;
+
+/* Zero every field of *p. */
+void attn_bwd_params_init(attn_bwd_params* p);
+
+/* The backward pass; returns an attn_status code. Asynchronous. */
+int attn_bwd(const attn_bwd_params* p);
+
+/*
  * attn_fwd_noalloc: attn_fwd_ex for callers that cannot allocate device
  * memory -- code that runs where cudaMalloc is forbidden or unavailable (an
  * allocator's or memory pool's own internals, an embedded runtime that owns
