@@ -87,6 +87,12 @@ class AttnBwdParams(ctypes.Structure):
         ("mask_kind", ctypes.c_int),
         ("stream", ctypes.c_void_p),
         ("timeout_ns", ctypes.c_uint64),
+        ("window", ctypes.c_int),
+        ("window_w", ctypes.c_int),
+        ("dilation", ctypes.c_int),
+        ("wrap", ctypes.c_int),
+        ("grid_h", ctypes.c_int),
+        ("grid_w", ctypes.c_int),
     ]
 
 

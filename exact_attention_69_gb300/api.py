@@ -138,14 +138,14 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
 
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
              lse: torch.Tensor, dout: torch.Tensor, *, scale: float | None = None,
-             mask: str = "none", stream=None, timeout_ns: int = 0):
+             mask: str = "none", window=0, dilation: int = 1, grid=None, wrap_axes=None,
+             stream=None, timeout_ns: int = 0):
     """Backward pass of attn_fwd: (dq, dk, dv) for the gradient dout at the output.
 
     q, o, dout [B, H, Nq, d]; k, v [B, H, Nk, d] contiguous bf16 CUDA tensors;
-    lse the forward's float32 [B, H, Nq]. mask: 'none' | 'causal'.
+    lse the forward's float32 [B, H, Nq]. mask and the neighbourhood options as
+    for attn_fwd.
     """
-    if mask not in ("none", "causal"):
-        raise ValueError("the backward pass covers mask 'none' and 'causal'")
     ts = (q, k, v, o, dout)
     _check_dev(*ts)
     if any(not t.is_contiguous() for t in ts) or not lse.is_contiguous():
@@ -162,6 +162,12 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     p.B, p.H, p.Nq, p.Nk, p.d = B, H, Nq, Nk, d
     p.scale = float(scale)
     p.mask_kind = _MASKS[mask]
+    if mask in ("clamp", "wrap"):
+        kh, kw, p.wrap = _na_axes(mask, window, wrap_axes)
+        p.window, p.window_w = kh, (kw if kw != kh else 0)
+        p.dilation = int(dilation)
+        if grid is not None:
+            p.grid_h, p.grid_w = int(grid[0]), int(grid[1])
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     p.stream = stream.cuda_stream
@@ -173,26 +179,29 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
 
 class _Attention(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, scale, mask):
-        o, lse = attn_fwd(q, k, v, scale=scale, mask=mask)
+    def forward(ctx, q, k, v, scale, mask, opts):
+        o, lse = attn_fwd(q, k, v, scale=scale, mask=mask, **opts)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.scale, ctx.mask = scale, mask
+        ctx.scale, ctx.mask, ctx.opts = scale, mask, opts
         return o
 
     @staticmethod
     def backward(ctx, dout):
         q, k, v, o, lse = ctx.saved_tensors
-        dq, dk, dv = attn_bwd(q, k, v, o, lse, dout.contiguous(), scale=ctx.scale, mask=ctx.mask)
-        return dq, dk, dv, None, None
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, dout.contiguous(), scale=ctx.scale, mask=ctx.mask,
+                              **ctx.opts)
+        return dq, dk, dv, None, None, None
 
 
 def attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
-              mask: str = "none") -> torch.Tensor:
-    """attn_fwd as a differentiable torch op (no mask or causal; contiguous bf16 CUDA
-    tensors [B, H, N, d]): the backward pass runs attn_bwd."""
+              mask: str = "none", window=0, dilation: int = 1, grid=None,
+              wrap_axes=None) -> torch.Tensor:
+    """attn_fwd as a differentiable torch op over contiguous bf16 CUDA tensors
+    [B, H, N, d] (every mask): the backward pass runs attn_bwd."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
-    return _Attention.apply(q, k, v, float(scale), mask)
+    opts = dict(window=window, dilation=dilation, grid=grid, wrap_axes=wrap_axes)
+    return _Attention.apply(q, k, v, float(scale), mask, opts)
 
 
 def workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, *, mask: str = "none",

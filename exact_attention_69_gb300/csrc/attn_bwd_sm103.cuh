@@ -331,10 +331,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 
 // ------------------------------------------------------------------ dK, dV
 
-// One CTA per (batch, head, 128-key K/V tile). No mask or causal.
+// Neighbourhood masks seen from a key: bit e set iff query q0 + e (< Nq) has
+// key (ky, kx) in its window. Clamped windows are not symmetric at the grid's
+// borders, so each query's window is placed and tested.
+template <int MASK>
+__device__ __forceinline__ void na_key_bits(const KernelParams& p, int q0, int ky, int kx,
+                                            uint32_t (&bits)[4]) {
+  constexpr bool WH = mask_na_wrap_rows(MASK), WW = mask_na_wrap_cols(MASK);
+  constexpr bool DIL = mask_na_dilated(MASK);
+  bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+  int qy = q0 / p.grid_w;
+  int qx = q0 - qy * p.grid_w;
+  const int n = min(kBM, p.Nq - q0);
+  for (int e = 0; e < n; ++e) {
+    const int fy = na_window_first<WH, DIL>(qy, p.grid_h, p.window_h, p.dilation);
+    const int fx = na_window_first<WW, DIL>(qx, p.grid_w, p.window_w, p.dilation);
+    if (na_in_window<WH, DIL>(ky, fy, p.grid_h, p.window_h, p.dilation) &&
+        na_in_window<WW, DIL>(kx, fx, p.grid_w, p.window_w, p.dilation))
+      bits[e >> 5] |= 1u << (e & 31);
+    if (++qx == p.grid_w) {
+      qx = 0;
+      ++qy;
+    }
+  }
+}
+
+// One CTA per (batch, head, 128-key K/V tile).
 template <int D, int MASK>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __grid_constant__ BwdParams bp) {
-  static_assert(MASK == kMaskNone || MASK == kMaskCausal, "dK/dV: no mask or causal");
   using C = Cfg<D>;
   using BC = BwdCfg<D>;
   const KernelParams& p = bp.f;
@@ -470,6 +494,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
       const int q0 = i * kBM;
       // causal: query q sees key kk iff q >= kk; first allowed column of this tile
       const int first = MASK == kMaskCausal ? kk - q0 : 0;
+      uint32_t nab[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (mask_is_na(MASK)) {
+        const int ky = kk / p.grid_w;
+        na_key_bits<MASK>(p, q0, ky, kk - ky * p.grid_w, nab);
+      }
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[64], pv[64];
@@ -484,7 +513,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = 2 * i2 + u, col = 64 * half + e;
-            const bool ok = col >= first;
+            const bool ok = col >= first && ((nab[col >> 5] >> (col & 31)) & 1u);
             const float pe = ok ? ex2(__uint_as_float(sv[e]) * p.c - vec[col]) : 0.f;
             pe2[u] = pe;
             ds2[u] = pe * (__uint_as_float(pv[e]) - vec[kBM + col]);
@@ -567,6 +596,14 @@ cudaError_t launch_bwd_dim(const BwdParams& bp, int mask, cudaStream_t s) {
   switch (mask) {
     case kMaskNone: return launch_bwd_mask<D, kMaskNone>(bp, s);
     case kMaskCausal: return launch_bwd_mask<D, kMaskCausal>(bp, s);
+    case kMaskNa + 0: return launch_bwd_mask<D, kMaskNa + 0>(bp, s);
+    case kMaskNa + 1: return launch_bwd_mask<D, kMaskNa + 1>(bp, s);
+    case kMaskNa + 2: return launch_bwd_mask<D, kMaskNa + 2>(bp, s);
+    case kMaskNa + 3: return launch_bwd_mask<D, kMaskNa + 3>(bp, s);
+    case kMaskNa + 4: return launch_bwd_mask<D, kMaskNa + 4>(bp, s);
+    case kMaskNa + 5: return launch_bwd_mask<D, kMaskNa + 5>(bp, s);
+    case kMaskNa + 6: return launch_bwd_mask<D, kMaskNa + 6>(bp, s);
+    case kMaskNa + 7: return launch_bwd_mask<D, kMaskNa + 7>(bp, s);
     default: return cudaErrorInvalidValue;
   }
 }

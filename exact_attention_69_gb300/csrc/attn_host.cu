@@ -494,30 +494,44 @@ int attn_params_size(void) { return static_cast<int>(sizeof(attn_params_ex)); }
 void attn_bwd_params_init(attn_bwd_params* p) {
   if (!p) return;
   std::memset(p, 0, sizeof(*p));
+  p->dilation = 1;
 }
 
 int attn_bwd(const attn_bwd_params* p) {
   t_err[0] = 0;
   if (!p) return fail(ATTN_ERR_INVALID_ARG, "params is NULL");
-  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1)
-    return fail(ATTN_ERR_INVALID_ARG, "B, H, Nq, Nk must be >= 1");
-  if (p->d != 32 && p->d != 64 && p->d != 128)
-    return fail(ATTN_ERR_UNSUPPORTED, "head dimension %d (need 32, 64 or 128)", p->d);
-  if (!(p->scale > 0.f) || !std::isfinite(p->scale))
-    return fail(ATTN_ERR_INVALID_ARG, "scale must be positive and finite");
-  if (p->mask_kind == ATTN_MASK_NA2D)
-    return fail(ATTN_ERR_UNSUPPORTED, "the backward pass covers no mask and causal");
-  if (p->mask_kind != ATTN_MASK_NONE && p->mask_kind != ATTN_MASK_CAUSAL)
-    return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", p->mask_kind);
+  // the forward's checks, on the forward's view of the problem
+  attn_params_ex fp;
+  attn_params_init(&fp);
+  fp.q = p->q;
+  fp.k = p->k;
+  fp.v = p->v;
+  fp.o = const_cast<void*>(p->o);
+  fp.lse = const_cast<float*>(p->lse);
+  fp.B = p->B;
+  fp.H = p->H;
+  fp.Nq = p->Nq;
+  fp.Nk = p->Nk;
+  fp.d = p->d;
+  fp.scale = p->scale;
+  fp.mask_kind = p->mask_kind;
+  fp.window = p->window;
+  fp.window_w = p->window_w;
+  fp.dilation = p->dilation;
+  fp.wrap = p->wrap;
+  fp.grid_h = p->grid_h;
+  fp.grid_w = p->grid_w;
+  Checked c;
+  int rc = validate(&fp, &c);
+  if (rc != ATTN_OK) return rc;
   const int64_t BH = static_cast<int64_t>(p->B) * p->H;
   if (BH * ((p->Nq + 127) / 128) >= (int64_t{1} << 31) || BH * ((p->Nk + 127) / 128) >= (int64_t{1} << 31))
     return fail(ATTN_ERR_INVALID_ARG, "too many tiles");
-  const void* ptrs[] = {p->q, p->k, p->v, p->o, p->dout, p->lse, p->dq, p->dk, p->dv};
+  const void* ptrs[] = {p->dout, p->lse, p->dq, p->dk, p->dv};
   for (const void* x : ptrs) {
-    if (!x) return fail(ATTN_ERR_INVALID_ARG, "q, k, v, o, dout, lse, dq, dk, dv must be non-null");
+    if (!x) return fail(ATTN_ERR_INVALID_ARG, "dout, lse, dq, dk, dv must be non-null");
     if (!aligned16(x)) return fail(ATTN_ERR_MISALIGNED, "every pointer must be 16-byte aligned");
   }
-  int rc;
   if ((rc = get_encoder()) != ATTN_OK) return rc;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
@@ -555,7 +569,11 @@ int attn_bwd(const attn_bwd_params* p) {
   kp.Nq = p->Nq;
   kp.Nk = p->Nk;
   kp.c = p->scale * 1.4426950408889634f;
-  kp.dilation = 1;
+  kp.grid_h = c.grid_h;
+  kp.grid_w = c.grid_w;
+  kp.window_h = p->window;
+  kp.window_w = p->window_w ? p->window_w : p->window;
+  kp.dilation = p->mask_kind == ATTN_MASK_NA2D ? p->dilation : 1;
   kp.n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
   kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
   kp.status = ds->status;
@@ -567,7 +585,10 @@ int attn_bwd(const attn_bwd_params* p) {
   bp.dk = p->dk;
   bp.dv = p->dv;
   bp.scale = p->scale;
-  const int mask = p->mask_kind == ATTN_MASK_CAUSAL ? attn::kMaskCausal : attn::kMaskNone;
+  int mask = p->mask_kind == ATTN_MASK_CAUSAL ? attn::kMaskCausal : attn::kMaskNone;
+  if (p->mask_kind == ATTN_MASK_NA2D)
+    mask = attn::na_mask(p->wrap == 1 || p->wrap == 2, p->wrap == 1 || p->wrap == 3,
+                         p->dilation > 1);
   cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
   const cudaError_t e = attn::launch_bwd(bp, p->d, mask, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");

@@ -198,8 +198,8 @@ int attn_params_size(void);
  * Attention", section "Background").
  * Layout: q, o, dout, dq: bf16 [B, H, Nq, d]; k, v, dk, dv: bf16 [B, H, Nk, d];
  * lse: fp32 [B, H, Nq] as written by attn_fwd; all contiguous, device memory
- * owned by the caller, 16-byte aligned. mask_kind: ATTN_MASK_NONE or
- * ATTN_MASK_CAUSAL (ATTN_MASK_NA2D: ATTN_ERR_UNSUPPORTED). dq, dk and dv are
+ * owned by the caller, 16-byte aligned. mask_kind and the neighbourhood
+ * fields as for attn_fwd (the same checks apply). dq, dk and dv are
  * overwritten. Three kernels are enqueued on the stream (rowsum(dout * O),
  * dQ, dK and dV); the library keeps a lazily grown per-device scratch of
  * B*H*Nq floats for D, so calls on one device must not overlap in time.
@@ -216,12 +216,13 @@ typedef struct attn_bwd_params {
   void* dv;
   int B, H, Nq, Nk, d;
   float scale;          /* the forward's scale */
-  int mask_kind;        /* ATTN_MASK_NONE or ATTN_MASK_CAUSAL */
+  int mask_kind;        /* attn_mask_kind */
   void* stream;         /* cudaStream_t; NULL = the calling thread's stream */
   uint64_t timeout_ns;  /* bound on every device-side wait; 0 = 2 seconds */
+  int window, window_w, dilation, wrap, grid_h, grid_w;  /* NA2D, as attn_params_ex */
 } attn_bwd_params;
 
-/* Zero every field of *p. */
+/* Zero every field of *p, dilation 1. */
 void attn_bwd_params_init(attn_bwd_params* p);
 
 /* The backward pass; returns an attn_status code. Asynchronous. */

@@ -101,3 +101,40 @@ def test_plain_entry_point_validates(lib):
     # attn_fwd with an unsupported head dimension, never reaching CUDA
     assert lib.attn_fwd(16, 16, 16, 16, None, 1, 1, 8, 8, 40, ctypes.c_float(0.1), 0, 0, 1, 0) == \
         _lib.ATTN_ERR_UNSUPPORTED
+
+
+def _bwd_base():
+    p = _lib.bwd_params()
+    p.q = p.k = p.v = p.o = p.dout = p.lse = p.dq = p.dk = p.dv = 1 << 20
+    p.B, p.H, p.Nq, p.Nk, p.d, p.scale = 1, 2, 256, 256, 64, 0.125
+    return p
+
+
+BWD_BAD = [
+    ("B0", dict(B=0), _lib.ATTN_ERR_INVALID_ARG),
+    ("d48", dict(d=48), _lib.ATTN_ERR_UNSUPPORTED),
+    ("mask9", dict(mask_kind=9), _lib.ATTN_ERR_INVALID_ARG),
+    ("null_dout", dict(dout=None), _lib.ATTN_ERR_INVALID_ARG),
+    ("null_dk", dict(dk=None), _lib.ATTN_ERR_INVALID_ARG),
+    ("misaligned_dv", dict(dv=(1 << 20) + 8), _lib.ATTN_ERR_MISALIGNED),
+    ("window_without_na", dict(window=3), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_even_window", dict(mask_kind=2, window=4), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_q_ne_k", dict(mask_kind=2, window=3, Nk=289), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_bad_grid", dict(mask_kind=2, window=3, grid_h=10, grid_w=20), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_dilated_window_too_big", dict(mask_kind=2, window=3, dilation=6), _lib.ATTN_ERR_INVALID_ARG),
+    ("na_wrap4", dict(mask_kind=2, window=3, wrap=4), _lib.ATTN_ERR_INVALID_ARG),
+]
+
+
+@pytest.mark.parametrize("name,changes,code", BWD_BAD, ids=[b[0] for b in BWD_BAD])
+def test_backward_rejects_bad_arguments_on_host(lib, name, changes, code):
+    p = _bwd_base()
+    for k, v in changes.items():
+        setattr(p, k, v)
+    assert _lib.bwd(p) == code
+    assert lib.attn_last_error()
+
+
+def test_backward_params_init_defaults(lib):
+    p = _lib.bwd_params()
+    assert p.dilation == 1 and p.window == 0 and p.wrap == 0 and p.mask_kind == 0

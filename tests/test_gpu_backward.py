@@ -39,19 +39,21 @@ def _grad_check(name, got, ref, scale_all):
                            f"max err {err.max():.3e}, max |ref| {np.abs(ref).max():.3e}")
 
 
-def run_bwd(E, B, H, Nq, Nk, d, mask, seed):
+def run_bwd(E, B, H, Nq, Nk, d, mask, seed, window=0, dilation=1, grid=None, wrap_axes=None):
     q, k, v = make_qkv(B, H, Nq, Nk, d, 1.0, seed)
     g = torch.Generator().manual_seed(seed + 1)
     dout = torch.randn(B, H, Nq, d, generator=g).to(torch.bfloat16)
     scale = 1.0 / math.sqrt(d)
     qc, kc, vc, gc = (t.cuda() for t in (q, k, v, dout))
-    o, lse = E.attn_fwd(qc, kc, vc, scale=scale, mask=mask)
-    dq, dk, dv = E.attn_bwd(qc, kc, vc, o, lse, gc, scale=scale, mask=mask)
+    na = dict(window=window, dilation=dilation, grid=grid, wrap_axes=wrap_axes)
+    o, lse = E.attn_fwd(qc, kc, vc, scale=scale, mask=mask, **na)
+    dq, dk, dv = E.attn_bwd(qc, kc, vc, o, lse, gc, scale=scale, mask=mask, **na)
     torch.cuda.synchronize()
     code, detail = E.device_status()
     assert code == 0, detail
     rq, rk, rv = oracle.attention_bwd(to_f64(q), to_f64(k), to_f64(v), to_f64(dout), scale=scale,
-                                      mask_kind=mask)
+                                      mask_kind=mask, window=window, dilation=dilation, grid=grid,
+                                      wrap=wrap_axes if wrap_axes is not None else False)
     scale_all = max(np.abs(r).max() for r in (rq, rk, rv))
     _grad_check("dq", dq, rq, scale_all)
     _grad_check("dk", dk, rk, scale_all)
@@ -89,8 +91,63 @@ def test_autograd_wrapper_matches_attn_bwd(E):
         assert torch.equal(a, b)
 
 
-def test_backward_rejects_neighbourhood_masks(E):
-    q, k, v = (t.cuda() for t in make_qkv(1, 1, 64, 64, 32, 1.0, 1))
-    o, lse = E.attn_fwd(q, k, v, mask="clamp", window=3, grid=(8, 8))
-    with pytest.raises(ValueError):
-        E.attn_bwd(q, k, v, o, lse, torch.ones_like(q), mask="clamp")
+# Neighbourhood attention: the dQ kernel masks each query row as the forward does;
+# the dK/dV kernel needs the transposed relation (which queries hold a key in their
+# window), which for wrap-around windows differs from a window centred on the key.
+NA_BWD = [(8, 8, 3), (16, 16, 5), (20, 12, 5), (13, 29, 7), (40, 40, 13)]
+
+
+@pytest.mark.parametrize("mode", ["clamp", "wrap"])
+@pytest.mark.parametrize("gh,gw,win", NA_BWD)
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_backward_neighbourhood(E, mode, gh, gw, win, d):
+    run_bwd(E, 1, 2, gh * gw, gh * gw, d, mode, seed=gh * gw + win + d, window=win, grid=(gh, gw))
+
+
+NA_BWD_DILATED = [(16, 16, 3, 2), (20, 12, 3, 4), (24, 50, 5, 4), (21, 21, 7, 3)]
+
+
+@pytest.mark.parametrize("mode", ["clamp", "wrap"])
+@pytest.mark.parametrize("gh,gw,win,dil", NA_BWD_DILATED)
+def test_backward_neighbourhood_dilated(E, mode, gh, gw, win, dil):
+    run_bwd(E, 1, 2, gh * gw, gh * gw, 64, mode, seed=gh + gw + win * dil, window=win,
+            dilation=dil, grid=(gh, gw))
+
+
+NA_BWD_AXES = [((16, 24), (3, 7), (True, False), 1), ((20, 20), (5, 3), (False, True), 1),
+               ((48, 40), (5, 3), (True, False), 4), ((13, 29), (1, 9), (False, True), 2),
+               ((1, 1000), (1, 15), (False, True), 1), ((1, 777), (1, 9), (False, False), 3)]
+
+
+@pytest.mark.parametrize("grid,win,wrap_axes,dil", NA_BWD_AXES)
+def test_backward_neighbourhood_per_axis(E, grid, win, wrap_axes, dil):
+    n = grid[0] * grid[1]
+    run_bwd(E, 1, 2, n, n, 64, "clamp", seed=n + dil, window=win, dilation=dil, grid=grid,
+            wrap_axes=wrap_axes)
+
+
+def test_backward_neighbourhood_full_window_is_unmasked(E):
+    """A window that covers the whole grid (clamp) allows every key: the gradients
+    equal those of the unmasked problem computed by the same kernels."""
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 15 * 15, 15 * 15, 64, 1.0, 21))
+    g = torch.randn(1, 2, 225, 64, generator=torch.Generator().manual_seed(22)).to(torch.bfloat16).cuda()
+    o, lse = E.attn_fwd(q, k, v)
+    ref = E.attn_bwd(q, k, v, o, lse, g)
+    o2, lse2 = E.attn_fwd(q, k, v, mask="clamp", window=15, grid=(15, 15))
+    got = E.attn_bwd(q, k, v, o2, lse2, g, mask="clamp", window=15, grid=(15, 15))
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+
+
+def test_autograd_wrapper_neighbourhood(E):
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 256, 256, 64, 1.0, 8))
+    g = torch.randn(1, 2, 256, 64, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+    na = dict(mask="wrap", window=(5, 3), grid=(16, 16), dilation=2)
+    qr, kr, vr = (t.clone().requires_grad_(True) for t in (q, k, v))
+    out = E.attention(qr, kr, vr, **na)
+    out.backward(g)
+    o, lse = E.attn_fwd(q, k, v, **na)
+    dq, dk, dv = E.attn_bwd(q, k, v, o, lse, g, **na)
+    assert torch.equal(out, o)
+    for a, b in ((qr.grad, dq), (kr.grad, dk), (vr.grad, dv)):
+        assert torch.equal(a, b)
