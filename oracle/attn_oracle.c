@@ -40,6 +40,13 @@
  *              modulo delta, and the dilation-1 rule is applied to the index
  *              inside that residue class.
  *     wrap : the keys are (q + delta*t) mod G for t in [-k/2, k/2].
+ *   3 NA3D   : tokens are laid out row-major on a grid_d x grid_h x grid_w
+ *              volume (depth slowest); query (qt, qy, qx), key (kt, ky, kx);
+ *              the key is allowed iff all three axes are allowed by the same
+ *              one-axis rule, each axis with its own window and its own clamp
+ *              or wrap choice; one dilation for all three. The NATTEN issue's
+ *              requester works with 3-D volumes (about 15-20 patches a side,
+ *              window 5) and wraps some of the axes.
  *   A row whose allowed set is empty gets o = 0 and lse = -inf (the
  *   NaN-guarding convention of a "safe" softmax).
  */
@@ -54,11 +61,13 @@
 #define ORACLE_MASK_NONE 0
 #define ORACLE_MASK_CAUSAL 1
 #define ORACLE_MASK_NA2D 2
+#define ORACLE_MASK_NA3D 3
 
 typedef struct {
   int Nq, Nk, d;
   double scale;
   int mask_kind, window_h, window_w, dilation, wrap_h, wrap_w, grid_h, grid_w;
+  int window_d, wrap_d, grid_d; /* NA3D's depth axis */
 } problem_t;
 
 /* One axis of the clamped neighbourhood: is key coordinate kc in the window of
@@ -88,6 +97,10 @@ static int axis_allowed_wrap(int qc, int kc, int G, int k, int dl) {
   return 0;
 }
 
+static int axis_allowed(int wrap, int qc, int kc, int G, int k, int dl) {
+  return wrap ? axis_allowed_wrap(qc, kc, G, k, dl) : axis_allowed_clamp(qc, kc, G, k, dl);
+}
+
 static int allowed(const problem_t* p, int i, int j) {
   switch (p->mask_kind) {
     case ORACLE_MASK_NONE:
@@ -103,6 +116,14 @@ static int allowed(const problem_t* p, int i, int j) {
                                    : axis_allowed_clamp(qx, kx, p->grid_w, p->window_w, p->dilation);
       return row_ok && col_ok;
     }
+    case ORACLE_MASK_NA3D: {
+      const int plane = p->grid_h * p->grid_w;
+      int qt = i / plane, qy = (i % plane) / p->grid_w, qx = i % p->grid_w;
+      int kt = j / plane, ky = (j % plane) / p->grid_w, kx = j % p->grid_w;
+      return axis_allowed(p->wrap_d, qt, kt, p->grid_d, p->window_d, p->dilation) &&
+             axis_allowed(p->wrap_h, qy, ky, p->grid_h, p->window_h, p->dilation) &&
+             axis_allowed(p->wrap_w, qx, kx, p->grid_w, p->window_w, p->dilation);
+    }
     default:
       return 0;
   }
@@ -111,10 +132,15 @@ static int allowed(const problem_t* p, int i, int j) {
 /* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
 static int check_args(const problem_t* p, int B, int H) {
   if (B < 1 || H < 1 || p->Nq < 1 || p->Nk < 1 || p->d < 1) return -1;
-  if (p->mask_kind < 0 || p->mask_kind > 2) return -1;
-  if (p->mask_kind == ORACLE_MASK_NA2D) {
+  if (p->mask_kind < 0 || p->mask_kind > 3) return -1;
+  if (p->mask_kind == ORACLE_MASK_NA3D) {
+    if (p->grid_d < 1 || p->window_d < 1 || p->window_d % 2 == 0) return -1;
+    if (p->window_d > 1 && (int64_t)p->window_d * p->dilation > p->grid_d) return -1;
+  }
+  if (p->mask_kind == ORACLE_MASK_NA2D || p->mask_kind == ORACLE_MASK_NA3D) {
+    const int64_t depth = p->mask_kind == ORACLE_MASK_NA3D ? p->grid_d : 1;
     if (p->grid_h < 1 || p->grid_w < 1) return -1;
-    if (p->grid_h * p->grid_w != p->Nq || p->Nq != p->Nk) return -1;
+    if (depth * p->grid_h * p->grid_w != p->Nq || p->Nq != p->Nk) return -1;
     if (p->window_h < 1 || p->window_h % 2 == 0 || p->window_w < 1 || p->window_w % 2 == 0)
       return -1;
     if (p->dilation < 1) return -1;
@@ -171,16 +197,17 @@ static void one_row(const problem_t* p, const double* q, const double* k,
  * rows == NULL: every row; o is [B,H,Nq,d], lse is [B,H,Nq].
  * rows != NULL: nrows flat row indices in [0, B*H*Nq); o is [nrows,d], lse [nrows].
  * window_h / window_w and wrap_h / wrap_w: the row (grid_h) and column (grid_w)
- * axes of NA2D; ignored for the other masks.
+ * axes of NA2D and NA3D; window_d / wrap_d / grid_d: NA3D's depth axis; all
+ * ignored for the other masks.
  * nthreads <= 0 leaves the OpenMP default.
  */
 int oracle_attn_rows(const double* q, const double* k, const double* v,
                      double* o, double* lse, int B, int H, int Nq, int Nk, int d,
                      double scale, int mask_kind, int window_h, int window_w, int dilation,
-                     int wrap_h, int wrap_w, int grid_h, int grid_w, const int64_t* rows,
-                     int64_t nrows, int nthreads) {
+                     int wrap_h, int wrap_w, int grid_h, int grid_w, int window_d, int wrap_d,
+                     int grid_d, const int64_t* rows, int64_t nrows, int nthreads) {
   problem_t p = {Nq, Nk, d, scale, mask_kind, window_h, window_w, dilation,
-                 wrap_h, wrap_w, grid_h, grid_w};
+                 wrap_h, wrap_w, grid_h, grid_w, window_d, wrap_d, grid_d};
   if (check_args(&p, B, H) != 0) return -1;
   const int64_t total = (int64_t)B * H * Nq;
   const int64_t n = rows ? nrows : total;
@@ -286,9 +313,10 @@ static void one_head_bwd(const problem_t* p, const double* q, const double* k, c
 int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout,
                     double* dq, double* dk, double* dv, int B, int H, int Nq, int Nk, int d,
                     double scale, int mask_kind, int window_h, int window_w, int dilation,
-                    int wrap_h, int wrap_w, int grid_h, int grid_w, int nthreads) {
+                    int wrap_h, int wrap_w, int grid_h, int grid_w, int window_d, int wrap_d,
+                    int grid_d, int nthreads) {
   problem_t p = {Nq, Nk, d, scale, mask_kind, window_h, window_w, dilation,
-                 wrap_h, wrap_w, grid_h, grid_w};
+                 wrap_h, wrap_w, grid_h, grid_w, window_d, wrap_d, grid_d};
   if (check_args(&p, B, H) != 0) return -1;
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -328,9 +356,10 @@ int oracle_max_threads(void) {
 
 /* The allowed-set predicate itself, exposed so tests can inspect masks. */
 int oracle_allowed(int i, int j, int Nq, int Nk, int mask_kind, int window_h, int window_w,
-                   int dilation, int wrap_h, int wrap_w, int grid_h, int grid_w) {
+                   int dilation, int wrap_h, int wrap_w, int grid_h, int grid_w, int window_d,
+                   int wrap_d, int grid_d) {
   problem_t p = {Nq, Nk, 1, 1.0, mask_kind, window_h, window_w, dilation,
-                 wrap_h, wrap_w, grid_h, grid_w};
+                 wrap_h, wrap_w, grid_h, grid_w, window_d, wrap_d, grid_d};
   if (check_args(&p, 1, 1) != 0) return -1;
   if (i < 0 || i >= Nq || j < 0 || j >= Nk) return -1;
   return allowed(&p, i, j);

@@ -16,6 +16,7 @@ import numpy as np
 MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_NA2D = 2
+MASK_NA3D = 3
 MASK_CODES = {"none": MASK_NONE, "causal": MASK_CAUSAL, "clamp": MASK_NA2D, "wrap": MASK_NA2D}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -48,30 +49,41 @@ def _dptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def _axes(mask_kind, window, wrap):
-    """(window_h, window_w, wrap_h, wrap_w) from a window given as k or (k_h, k_w) and
-    wrap given as a bool (both axes) or a pair (rows, columns); "wrap" as the mask
-    name wraps both axes unless the pair says otherwise."""
-    if isinstance(window, (tuple, list)):
-        kh, kw = int(window[0]), int(window[1])
-    else:
-        kh = kw = int(window)
-    if isinstance(wrap, (tuple, list)):
-        wh, ww = bool(wrap[0]), bool(wrap[1])
-    else:
-        wh = ww = bool(wrap) or mask_kind == "wrap"
-    return kh, kw, int(wh), int(ww)
+def _mask_args(mask_kind, window, wrap, grid, Nq):
+    """The C oracle's mask arguments (mask code, window_h, window_w, wrap_h, wrap_w,
+    grid_h, grid_w, window_d, wrap_d, grid_d).
 
-
-def _grid(mask_kind, Nq, grid):
-    if mask_kind != MASK_NA2D:
-        return 0, 0
+    mask_kind: a code, or "none" | "causal" | "clamp" | "wrap"; a neighbourhood mask
+    on a 3-entry grid (depth, rows, columns) is NA3D, else NA2D. window: k for every
+    axis, or one odd size per grid axis. wrap: a bool for every axis, or one per grid
+    axis; the mask name "wrap" wraps every axis unless wrap says otherwise. NA2D
+    without a grid needs a square token count."""
+    code = MASK_CODES[mask_kind] if isinstance(mask_kind, str) else int(mask_kind)
+    if code == MASK_NA2D and grid is not None and len(grid) == 3:
+        code = MASK_NA3D
+    if code not in (MASK_NA2D, MASK_NA3D):
+        return code, 0, 0, 0, 0, 0, 0, 0, 0, 0
+    nax = 3 if code == MASK_NA3D else 2
     if grid is None:
+        if nax == 3:
+            raise ValueError("NA3D needs an explicit (depth, rows, columns) grid")
         g = int(round(Nq ** 0.5))
         if g * g != Nq:
             raise ValueError("NA2D without explicit grid needs a square token count")
-        return g, g
-    return int(grid[0]), int(grid[1])
+        grid = (g, g)
+    if len(grid) != nax:
+        raise ValueError(f"grid {grid} does not match the mask's {nax} axes")
+    win = [int(x) for x in window] if isinstance(window, (tuple, list)) else [int(window)] * nax
+    if isinstance(wrap, (tuple, list)):
+        wr = [int(bool(x)) for x in wrap]
+    else:
+        wr = [int(bool(wrap) or mask_kind == "wrap")] * nax
+    if len(win) != nax or len(wr) != nax:
+        raise ValueError("window and wrap need one entry per grid axis")
+    g = [int(x) for x in grid]
+    if nax == 2:
+        return code, win[0], win[1], wr[0], wr[1], g[0], g[1], 0, 0, 0
+    return code, win[1], win[2], wr[1], wr[2], g[1], g[2], win[0], wr[0], g[0]
 
 
 class Oracle:
@@ -86,14 +98,15 @@ class Oracle:
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, ctypes.c_int,
         ]
         lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_attn_bwd.argtypes = [dp] * 7 + [ctypes.c_int] * 5 + [ctypes.c_double] + \
-            [ctypes.c_int] * 9
+            [ctypes.c_int] * 12
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_allowed.restype = ctypes.c_int
-        lib.oracle_allowed.argtypes = [ctypes.c_int] * 12
+        lib.oracle_allowed.argtypes = [ctypes.c_int] * 15
         self._lib = lib
         self.path = path
 
@@ -105,18 +118,16 @@ class Oracle:
         rows: None for every row, else flat indices b*H*Nq + h*Nq + i.
         Returns (o, lse): o [B,H,Nq,d] / lse [B,H,Nq] for rows=None, else
         o [len(rows), d] / lse [len(rows)].
-        window: k, or (k_h, k_w) per grid axis; wrap: bool, or (rows, columns).
+        grid: (rows, columns) for NA2D, (depth, rows, columns) for NA3D; window and
+        wrap: one value for every axis or one per grid axis (see _mask_args).
         """
-        kh, kw, wh, ww = _axes(mask_kind, window, wrap)
-        if isinstance(mask_kind, str):
-            mask_kind = MASK_CODES[mask_kind]
         q = np.ascontiguousarray(np.asarray(q, dtype=np.float64))
         k = np.ascontiguousarray(np.asarray(k, dtype=np.float64))
         v = np.ascontiguousarray(np.asarray(v, dtype=np.float64))
         B, H, Nq, d = q.shape
         Nk = k.shape[2]
         assert k.shape == (B, H, Nk, d) and v.shape == (B, H, Nk, d)
-        gh, gw = _grid(mask_kind, Nq, grid)
+        m = _mask_args(mask_kind, window, wrap, grid, Nq)
         if rows is None:
             o = np.empty((B, H, Nq, d), dtype=np.float64)
             lse = np.empty((B, H, Nq), dtype=np.float64)
@@ -129,8 +140,8 @@ class Oracle:
             rp = rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
         rc = self._lib.oracle_attn_rows(
             _dptr(q), _dptr(k), _dptr(v), _dptr(o), _dptr(lse),
-            B, H, Nq, Nk, d, float(scale), int(mask_kind), kh, kw, int(dilation),
-            wh, ww, gh, gw, rp, n, int(nthreads),
+            B, H, Nq, Nk, d, float(scale), m[0], m[1], m[2], int(dilation),
+            *m[3:], rp, n, int(nthreads),
         )
         if rc != 0:
             raise ValueError(f"oracle rejected the problem (code {rc})")
@@ -141,21 +152,18 @@ class Oracle:
         """Gradients (dq, dk, dv) in fp64 of a loss whose gradient at the output O is
         dout [B, H, Nq, d]; q [B, H, Nq, d], k and v [B, H, Nk, d]. Mask arguments as
         attention_rows."""
-        kh, kw, wh, ww = _axes(mask_kind, window, wrap)
-        if isinstance(mask_kind, str):
-            mask_kind = MASK_CODES[mask_kind]
         q, k, v, dout = (np.ascontiguousarray(np.asarray(t, dtype=np.float64))
                          for t in (q, k, v, dout))
         B, H, Nq, d = q.shape
         Nk = k.shape[2]
         assert k.shape == (B, H, Nk, d) and v.shape == (B, H, Nk, d) and dout.shape == q.shape
-        gh, gw = _grid(mask_kind, Nq, grid)
+        m = _mask_args(mask_kind, window, wrap, grid, Nq)
         dq = np.empty_like(q)
         dk = np.empty_like(k)
         dv = np.empty_like(v)
         rc = self._lib.oracle_attn_bwd(_dptr(q), _dptr(k), _dptr(v), _dptr(dout), _dptr(dq),
                                        _dptr(dk), _dptr(dv), B, H, Nq, Nk, d, float(scale),
-                                       int(mask_kind), kh, kw, int(dilation), wh, ww, gh, gw,
+                                       m[0], m[1], m[2], int(dilation), *m[3:],
                                        int(nthreads))
         if rc != 0:
             raise ValueError(f"oracle rejected the problem (code {rc})")
@@ -167,12 +175,9 @@ class Oracle:
 
     def allowed(self, i, j, *, Nq, Nk, mask_kind, window=0, dilation=1, wrap=False, grid=None):
         """The oracle's allowed-set predicate for one (query, key) pair."""
-        kh, kw, wh, ww = _axes(mask_kind, window, wrap)
-        if isinstance(mask_kind, str):
-            mask_kind = MASK_CODES[mask_kind]
-        gh, gw = _grid(mask_kind, Nq, grid)
-        r = self._lib.oracle_allowed(int(i), int(j), int(Nq), int(Nk), int(mask_kind),
-                                     kh, kw, int(dilation), wh, ww, gh, gw)
+        m = _mask_args(mask_kind, window, wrap, grid, Nq)
+        r = self._lib.oracle_allowed(int(i), int(j), int(Nq), int(Nk), m[0], m[1], m[2],
+                                     int(dilation), *m[3:])
         if r < 0:
             raise ValueError("bad arguments")
         return bool(r)

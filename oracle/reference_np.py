@@ -39,8 +39,10 @@ def mask_matrix(Nq: int, Nk: int, mask: str, window=0, dilation: int = 1,
                 grid=None, wrap_axes=None) -> np.ndarray:
     """Boolean [Nq, Nk] allowed-set matrix. mask: none | causal | clamp | wrap.
 
-    window: k, or (k_rows, k_cols); wrap_axes: None (both axes wrap for "wrap",
-    neither for "clamp") or (rows, cols) booleans.
+    grid: (rows, cols), or (depth, rows, cols) for a volume, tokens row-major with
+    the first axis slowest; window: k for every axis, or one size per axis;
+    wrap_axes: None (every axis wraps for "wrap", none for "clamp") or one boolean
+    per axis.
     """
     if mask == "none":
         return np.ones((Nq, Nk), dtype=bool)
@@ -49,21 +51,19 @@ def mask_matrix(Nq: int, Nk: int, mask: str, window=0, dilation: int = 1,
         for i in range(Nq):
             m[i, : min(i + 1, Nk)] = True
         return m
-    gh, gw = grid
-    assert gh * gw == Nq == Nk
-    kh, kw = (window, window) if np.isscalar(window) else (window[0], window[1])
-    wh, ww = (mask == "wrap",) * 2 if wrap_axes is None else wrap_axes
-    fn_h = _window_coords_wrap if wh else _window_coords_clamp
-    fn_w = _window_coords_wrap if ww else _window_coords_clamp
+    grid = tuple(int(g) for g in grid)
+    nax = len(grid)
+    assert int(np.prod(grid)) == Nq == Nk
+    ks = (window,) * nax if np.isscalar(window) else tuple(window)
+    wraps = (mask == "wrap",) * nax if wrap_axes is None else tuple(wrap_axes)
+    assert len(ks) == nax and len(wraps) == nax
     m = np.zeros((Nq, Nk), dtype=bool)
-    for qy in range(gh):
-        rows = fn_h(qy, gh, kh, dilation)
-        for qx in range(gw):
-            cols = fn_w(qx, gw, kw, dilation)
-            i = qy * gw + qx
-            for ky in rows:
-                for kx in cols:
-                    m[i, ky * gw + kx] = True
+    for i, qc in enumerate(np.ndindex(*grid)):
+        sets = [sorted((_window_coords_wrap if wraps[a] else _window_coords_clamp)(
+            qc[a], grid[a], ks[a], dilation)) for a in range(nax)]
+        for kc in np.ndindex(*(len(x) for x in sets)):
+            coord = tuple(sets[a][kc[a]] for a in range(nax))
+            m[i, np.ravel_multi_index(coord, grid)] = True
     return m
 
 

@@ -19,6 +19,12 @@ What pins what:
   one_axis_wrap_pad_clamp the same recipe along one axis == wrap along that axis only
   axis_windows_by_hand    literal key sets for a rectangular window and one-axis wrap
   one_d_closed_form       a 1 x N grid is 1-D neighbourhood attention: closed-form windows
+  na3d_windows_by_hand    literal key sets on a volume (clamp, wrap on some axes, dilation 2)
+  na3d_closed_form        NA3D allowed set == the product of per-axis closed-form windows
+                          (interval / circular distance / residue class), depth slowest
+  na3d_flat_is_na2d       a volume one slice deep with window 1 along depth == NA2D
+  na3d_wrap_pad_clamp     issue #142's recipe in 3-D: circular pad of the wrapped axes,
+                          clamped NA3D, crop == NA3D wrapping those axes
   bwd_autograd_fp64       backward: torch autograd through an explicit fp64 forward
   bwd_finite_differences  backward: central differences of sum(dO * O) along random directions
   bwd_invariants          backward: a common shift of all keys leaves O unchanged (sum_j dK_j
@@ -107,6 +113,11 @@ CASES = [
     dict(mask_kind="clamp", Nq=54, Nk=54, window=(5, 3), grid=(6, 9), wrap=(True, False)),
     dict(mask_kind="clamp", Nq=54, Nk=54, window=(3, 3), grid=(6, 9), wrap=(False, True), dilation=2),
     dict(mask_kind="clamp", Nq=15, Nk=15, window=(1, 5), grid=(1, 15)),
+    dict(mask_kind="clamp", Nq=60, Nk=60, window=3, grid=(3, 4, 5)),
+    dict(mask_kind="wrap", Nq=64, Nk=64, window=3, grid=(4, 4, 4)),
+    dict(mask_kind="clamp", Nq=90, Nk=90, window=(3, 5, 3), grid=(3, 6, 5), wrap=(True, False, True)),
+    dict(mask_kind="clamp", Nq=180, Nk=180, window=(1, 3, 3), grid=(5, 6, 6), wrap=(False, True, False),
+         dilation=2),
 ]
 
 
@@ -154,8 +165,9 @@ def zero_qk_means(orc):
             exp_n = cnt
         else:
             kk = case["window"]
-            kh, kw = (kk, kk) if np.isscalar(kk) else kk
-            exp_n = np.full(Nq, kh * kw)        # every query sees a full k_h x k_w window
+            nax = len(case["grid"])
+            ks = (kk,) * nax if np.isscalar(kk) else kk
+            exp_n = np.full(Nq, int(np.prod(ks)))  # every query sees a full window on each axis
             allowed = _twin_mask(case)
             exp_o = np.stack([v[0, 0][allowed[i]].mean(axis=0) for i in range(Nq)])
         assert np.max(np.abs(o[0, 0] - exp_o)) < 1e-13, case
@@ -369,12 +381,114 @@ def one_d_closed_form(orc):
             assert got == want, (N, k, dl, i)
 
 
+
+def _vol_keys(orc, i, grid, window, wrap=False, dilation=1):
+    n = grid[0] * grid[1] * grid[2]
+    return {j for j in range(n)
+            if orc.allowed(i, j, Nq=n, Nk=n, mask_kind="clamp", window=window, wrap=wrap,
+                           dilation=dilation, grid=grid)}
+
+
+def na3d_windows_by_hand(orc):
+    def tok(t, y, x, g):
+        return (t * g[1] + y) * g[2] + x
+
+    g = (4, 5, 6)
+    # clamp, window 3 on every axis: corner (0,0,0) -> {0,1,2} x {0,1,2} x {0,1,2};
+    # (3,4,5) -> {1,2,3} x {2,3,4} x {3,4,5}
+    assert _vol_keys(orc, tok(0, 0, 0, g), g, 3) == \
+        {tok(t, y, x, g) for t in (0, 1, 2) for y in (0, 1, 2) for x in (0, 1, 2)}
+    assert _vol_keys(orc, tok(3, 4, 5, g), g, 3) == \
+        {tok(t, y, x, g) for t in (1, 2, 3) for y in (2, 3, 4) for x in (3, 4, 5)}
+    # depth wraps, rows and columns clamp, window (3, 1, 5): (0,2,0) -> depth {3,0,1},
+    # row {2}, columns {0..4}
+    assert _vol_keys(orc, tok(0, 2, 0, g), g, (3, 1, 5), (True, False, False)) == \
+        {tok(t, 2, x, g) for t in (3, 0, 1) for x in range(5)}
+    # depth clamps, rows and columns wrap, window 3: (2,0,5) -> depth {1,2,3},
+    # rows {4,0,1}, columns {4,5,0}
+    assert _vol_keys(orc, tok(2, 0, 5, g), g, 3, (False, True, True)) == \
+        {tok(t, y, x, g) for t in (1, 2, 3) for y in (4, 0, 1) for x in (4, 5, 0)}
+    # dilation 2 on a 4 x 6 x 6 volume, window (1, 3, 3), clamp: (1,5,0) -> depth {1},
+    # rows of residue 1 {1,3,5}, columns of residue 0 {0,2,4}
+    g2 = (4, 6, 6)
+    assert _vol_keys(orc, tok(1, 5, 0, g2), g2, (1, 3, 3), False, 2) == \
+        {tok(1, y, x, g2) for y in (1, 3, 5) for x in (0, 2, 4)}
+
+
+def _axis_closed_form(qc, kc, G, k, wrap, dl):
+    """One axis, from closed forms: wrap -> circular distance a multiple of dl and at
+    most dl*(k//2); clamp -> same residue mod dl and the class index inside the
+    interval [s, s + k), s = min(max(a - k//2, 0), L - k), L the class size."""
+    if wrap:
+        for t in range(-(k // 2), k // 2 + 1):
+            if (qc + dl * t - kc) % G == 0:
+                return True
+        return False
+    if qc % dl != kc % dl:
+        return False
+    L = len(range(qc % dl, G, dl))
+    s = min(max(qc // dl - k // 2, 0), L - k)
+    return s <= kc // dl < s + k
+
+
+def na3d_closed_form(orc):
+    for (g, win, wrap, dl) in (((3, 4, 5), (3, 3, 3), (False, False, False), 1),
+                               ((4, 3, 5), (3, 1, 5), (True, False, True), 1),
+                               ((5, 4, 3), (5, 3, 1), (False, True, False), 1),
+                               ((6, 4, 6), (3, 1, 3), (True, False, False), 2)):
+        n = g[0] * g[1] * g[2]
+        for i in range(n):
+            qc = (i // (g[1] * g[2]), (i // g[2]) % g[1], i % g[2])
+            want = set()
+            for j in range(n):
+                kc = (j // (g[1] * g[2]), (j // g[2]) % g[1], j % g[2])
+                if all(_axis_closed_form(qc[a], kc[a], g[a], win[a], wrap[a], dl)
+                       for a in range(3)):
+                    want.add(j)
+            assert _vol_keys(orc, i, g, win, wrap, dl) == want, (g, win, wrap, dl, i)
+
+
+def na3d_flat_is_na2d(orc):
+    rng = np.random.default_rng(19)
+    for (gh, gw, kh, kw, wrap, dl) in ((6, 7, 3, 5, (False, True), 1), (8, 8, 3, 3, (True, True), 2),
+                                       (5, 9, 5, 1, (False, False), 1)):
+        n, d = gh * gw, 5
+        q, k, v = (_rand(1, 2, n, d, rng=rng) for _ in range(3))
+        o2, l2 = orc.attention(q, k, v, scale=0.7, mask_kind="clamp", window=(kh, kw), wrap=wrap,
+                               dilation=dl, grid=(gh, gw))
+        o3, l3 = orc.attention(q, k, v, scale=0.7, mask_kind="clamp", window=(1, kh, kw),
+                               wrap=(False,) + wrap, dilation=dl, grid=(1, gh, gw))
+        assert np.array_equal(o2, o3) and np.array_equal(l2, l3)
+
+
+def na3d_wrap_pad_clamp(orc):
+    rng = np.random.default_rng(23)
+    for (g, win, wrap, dl) in (((5, 6, 7), (3, 3, 3), (True, True, False), 1),
+                               ((6, 5, 5), (3, 5, 3), (True, False, True), 1),
+                               ((8, 6, 7), (3, 1, 3), (True, False, True), 2)):
+        d = 3
+        x = [rng.standard_normal(g + (d,)) for _ in range(3)]
+        pads = [((win[a] // 2) * dl if wrap[a] else 0) for a in range(3)]
+        padded = [np.pad(t, [(p_, p_) for p_ in pads] + [(0, 0)], mode="wrap") for t in x]
+        G = tuple(g[a] + 2 * pads[a] for a in range(3))
+        ow, lw = orc.attention(*(t.reshape(1, 1, -1, d) for t in x), scale=0.5, mask_kind="clamp",
+                               window=win, wrap=wrap, dilation=dl, grid=g)
+        oc, lc = orc.attention(*(t.reshape(1, 1, -1, d) for t in padded), scale=0.5,
+                               mask_kind="clamp", window=win, dilation=dl, grid=G)
+        crop = tuple(slice(pads[a], pads[a] + g[a]) for a in range(3))
+        oc = oc.reshape(G + (d,))[crop].reshape(1, 1, -1, d)
+        lc = lc.reshape(G)[crop].reshape(1, 1, -1)
+        assert np.max(np.abs(oc - ow)) < 1e-12, (g, win, wrap, dl)
+        assert np.max(np.abs(lc - lw)) < 1e-12, (g, win, wrap, dl)
+
+
 BWD_CASES = [
     dict(mask_kind="none", Nq=13, Nk=21),
     dict(mask_kind="causal", Nq=17, Nk=17),
     dict(mask_kind="causal", Nq=9, Nk=20),
     dict(mask_kind="clamp", Nq=30, Nk=30, window=(3, 5), grid=(5, 6)),
     dict(mask_kind="wrap", Nq=36, Nk=36, window=3, grid=(6, 6), dilation=2),
+    dict(mask_kind="clamp", Nq=48, Nk=48, window=(3, 3, 1), grid=(3, 4, 4), wrap=(True, False, True)),
 ]
 
 
@@ -460,6 +574,10 @@ def all_checks(goldens):
         ("one_axis_wrap_pad_clamp", one_axis_wrap_pad_clamp),
         ("axis_windows_by_hand", axis_windows_by_hand),
         ("one_d_closed_form", one_d_closed_form),
+        ("na3d_windows_by_hand", na3d_windows_by_hand),
+        ("na3d_closed_form", na3d_closed_form),
+        ("na3d_flat_is_na2d", na3d_flat_is_na2d),
+        ("na3d_wrap_pad_clamp", na3d_wrap_pad_clamp),
         ("bwd_autograd_fp64", bwd_autograd_fp64),
         ("bwd_finite_differences", bwd_finite_differences),
         ("bwd_invariants", bwd_invariants),

@@ -33,6 +33,15 @@ MUTANTS = {
     "na_wrap_axes_swapped": ("const int row_ok = p->wrap_h ?", "const int row_ok = p->wrap_w ?"),
     "dilation_residue_ignored": ("if (kc % dl != residue) return 0;", ""),
     "softmax_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
+    "na3_depth_dropped": ("return axis_allowed(p->wrap_d, qt, kt, p->grid_d, p->window_d, p->dilation) &&",
+                          "return 1 &&"),
+    "na3_plane_stride": ("const int plane = p->grid_h * p->grid_w;",
+                         "const int plane = p->grid_w * p->grid_w;"),
+    "na3_depth_wrap_from_rows": ("axis_allowed(p->wrap_d, qt, kt,", "axis_allowed(p->wrap_h, qt, kt,"),
+    "na3_depth_window_from_rows": ("p->grid_d, p->window_d, p->dilation)",
+                                   "p->grid_d, p->window_h, p->dilation)"),
+    "na3_axes_transposed": ("int kt = j / plane, ky = (j % plane) / p->grid_w, kx = j % p->grid_w;",
+                            "int kx = j / plane, ky = (j % plane) / p->grid_w, kt = j % p->grid_w;"),
     "bwd_dropped_d_term": ("const double dsij = pw[j] * (dp[j] - Di);", "const double dsij = pw[j] * dp[j];"),
     "bwd_dk_unscaled": ("dk[(int64_t)j * d + t] += p->scale * dsij * qi[t];",
                         "dk[(int64_t)j * d + t] += dsij * qi[t];"),
