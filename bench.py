@@ -76,9 +76,11 @@ def allowed_pairs_matrix(w) -> np.ndarray | None:
         return None
     if w.mask == "causal":
         return np.tril(np.ones((w.Nq, w.Nk), dtype=bool))
-    gh, gw = w.grid
-    return np.kron(_axis_allowed(gh, w.window, w.mask == "wrap"),
-                   _axis_allowed(gw, w.window, w.mask == "wrap")).astype(bool)
+    wraps = w.wrap_axes if w.wrap_axes is not None else (w.mask == "wrap",) * len(w.grid)
+    m = np.ones((1, 1), dtype=bool)
+    for G, wrap in zip(w.grid, wraps):  # row-major tokens: the first axis is the slowest
+        m = np.kron(m, _axis_allowed(G, w.window, wrap))
+    return m.astype(bool)
 
 
 def count_flops(w):
@@ -234,7 +236,8 @@ def oracle_sample(w, target_s: float, seed_rows: int = 7):
     qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
     total = w.B * w.H * w.Nq
     rng = np.random.default_rng(seed_rows)
-    kw = dict(scale=w.scale, mask_kind=w.mask, window=w.window, grid=w.grid)
+    kw = dict(scale=w.scale, mask_kind=w.mask, window=w.window, grid=w.grid,
+              wrap=w.wrap_axes if w.wrap_axes is not None else False)
     n = min(total, 64)
     rows = np.sort(rng.choice(total, size=n, replace=False))
     t = time.perf_counter()
@@ -289,6 +292,8 @@ def config_of(w, rotating_sets):
            "flop_rule": "4*128*128*d per 128x128 reference tile holding an allowed pair"}
     if w.mask in ("clamp", "wrap"):
         cfg.update({"window": w.window, "grid": list(w.grid), "dilation": w.dilation})
+        if w.wrap_axes is not None:
+            cfg["wrap_axes"] = list(w.wrap_axes)
     if rotating_sets is not None:
         cfg["l2"] = (f"inputs larger than L2: {rotating_sets} rotating input sets "
                      f"(> {L2_BYTES // 2**20} MiB in total), no explicit flush")
@@ -325,7 +330,7 @@ def ours_arm(args, w):
                      torch.empty(w.B, w.H, w.Nq, w.d, dtype=torch.bfloat16, device=dev),
                      torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device=dev)))
     stream = torch.cuda.current_stream(dev)
-    kw = dict(scale=w.scale, mask=w.mask, window=w.window, grid=w.grid)
+    kw = dict(scale=w.scale, mask=w.mask, window=w.window, grid=w.grid, wrap_axes=w.wrap_axes)
 
     def step(i, events=None):
         qq, kk, vv, oo, ll = sets[i % n_sets]

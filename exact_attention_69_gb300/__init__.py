@@ -7,8 +7,8 @@ attention with clamped or circular ("wrap") windows (tiles no window touches
 skipped). Outputs: O in bf16 and the fp32 log-sum-exp.
 """
 from .api import (  # noqa: F401
-    attention, attn_bwd, attn_fwd, device_status, na2d, sm_count, workspace_bytes)
+    attention, attn_bwd, attn_fwd, device_status, na2d, na3d, sm_count, workspace_bytes)
 from ._lib import AttnError  # noqa: F401
 
-__all__ = ["attn_fwd", "attn_bwd", "attention", "na2d", "device_status", "sm_count",
+__all__ = ["attn_fwd", "attn_bwd", "attention", "na2d", "na3d", "device_status", "sm_count",
            "workspace_bytes", "AttnError"]

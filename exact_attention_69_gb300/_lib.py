@@ -25,6 +25,7 @@ ATTN_ERR_TIMEOUT = 5
 ATTN_MASK_NONE = 0
 ATTN_MASK_CAUSAL = 1
 ATTN_MASK_NA2D = 2
+ATTN_MASK_NA3D = 3
 
 
 class AttnParamsEx(ctypes.Structure):
@@ -62,6 +63,9 @@ class AttnParamsEx(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_uint64),
         ("window_w", ctypes.c_int),
+        ("grid_d", ctypes.c_int),
+        ("window_d", ctypes.c_int),
+        ("wrap_d", ctypes.c_int),
     ]
 
 
@@ -93,6 +97,9 @@ class AttnBwdParams(ctypes.Structure):
         ("wrap", ctypes.c_int),
         ("grid_h", ctypes.c_int),
         ("grid_w", ctypes.c_int),
+        ("grid_d", ctypes.c_int),
+        ("window_d", ctypes.c_int),
+        ("wrap_d", ctypes.c_int),
     ]
 
 

@@ -9,6 +9,10 @@ the library's sm_103a kernel per call. Nothing here computes attention.
                                   NATTEN's heads-last [B, X, Y, heads, d] layout,
                                   'clamp' or 'wrap' windows (NATTEN issue #142),
                                   per axis if asked
+    na3d(q, k, v, kernel_size, mode)
+                                  the same on volumes [B, X, Y, Z, heads, d]
+    attn_bwd(q, k, v, o, lse, dout, ...), attention(q, k, v, ...)
+                                  gradients; a differentiable op
 """
 from __future__ import annotations
 
@@ -28,6 +32,11 @@ def _strides(t: torch.Tensor, layout: str):
         raise ValueError("the last (head) dimension must be contiguous")
     if layout == "bhnd":
         sb, sh, sn, _ = t.stride()
+    elif layout == "bxyzhd":  # heads-last volume [B, X, Y, Z, H, d]: n = (x * Y + y) * Z + z
+        sb, sx, sy, sz, sh, _ = t.stride()
+        if sy != sz * t.shape[3] or sx != sy * t.shape[2]:
+            raise ValueError("X, Y and Z must be jointly contiguous in a heads-last layout")
+        sn = sz
     else:  # heads-last [B, X, Y, H, d]: token n = x * Y + y
         sb, sx, sy, sh, _ = t.stride()
         if sx != sy * t.shape[2]:
@@ -36,14 +45,33 @@ def _strides(t: torch.Tensor, layout: str):
     return (sb, sh, sn)
 
 
-def _na_axes(mask, window, wrap_axes):
-    """(window along the rows, window along the columns, ABI wrap code)."""
-    kh, kw = (int(window), int(window)) if isinstance(window, int) else (int(window[0]),
-                                                                         int(window[1]))
-    if wrap_axes is None:
-        wrap_axes = (mask == "wrap", mask == "wrap")
-    code = {(False, False): 0, (True, True): 1, (True, False): 2, (False, True): 3}
-    return kh, kw, code[(bool(wrap_axes[0]), bool(wrap_axes[1]))]
+def _set_mask(p, mask, window, dilation, grid, wrap_axes):
+    """mask_kind and the neighbourhood fields of a parameter block. A 'clamp' or
+    'wrap' mask on a 3-entry grid (depth, rows, columns) is NA3D, else NA2D;
+    window: k for every axis or one per grid axis; wrap_axes: None (every axis
+    as the mask name says) or one boolean per grid axis."""
+    if mask not in _MASKS:
+        raise ValueError(f"unknown mask {mask!r}")
+    p.mask_kind = _MASKS[mask]
+    if mask not in ("clamp", "wrap"):
+        p.window, p.dilation, p.wrap = int(window), int(dilation), 0
+        return
+    nax = 3 if grid is not None and len(grid) == 3 else 2
+    win = tuple(int(x) for x in window) if isinstance(window, (tuple, list)) else (int(window),) * nax
+    wr = (mask == "wrap",) * nax if wrap_axes is None else tuple(bool(x) for x in wrap_axes)
+    if len(win) != nax or len(wr) != nax:
+        raise ValueError("window and wrap_axes need one entry per grid axis")
+    kh, kw = win[-2], win[-1]
+    p.window, p.window_w = kh, (kw if kw != kh else 0)
+    p.wrap = {(False, False): 0, (True, True): 1, (True, False): 2, (False, True): 3}[wr[-2:]]
+    p.dilation = int(dilation)
+    if nax == 3:
+        p.mask_kind = _lib.ATTN_MASK_NA3D
+        p.grid_d, p.grid_h, p.grid_w = (int(x) for x in grid)
+        p.window_d = win[0] if win[0] != kh else 0
+        p.wrap_d = int(wr[0])
+    elif grid is not None:
+        p.grid_h, p.grid_w = int(grid[0]), int(grid[1])
 
 
 def _check_dev(*ts):
@@ -62,15 +90,7 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
     p.lse = lse.data_ptr() if lse is not None else None
     p.B, p.H, p.Nq, p.Nk, p.d = B, H, Nq, Nk, d
     p.scale = float(scale)
-    p.mask_kind = _MASKS[mask]
-    if mask in ("clamp", "wrap"):
-        kh, kw, p.wrap = _na_axes(mask, window, wrap_axes)
-        p.window, p.window_w = kh, (kw if kw != kh else 0)
-        p.dilation = int(dilation)
-        if grid is not None:
-            p.grid_h, p.grid_w = int(grid[0]), int(grid[1])
-    else:
-        p.window, p.dilation, p.wrap = int(window), int(dilation), 0
+    _set_mask(p, mask, window, dilation, grid, wrap_axes)
     for name, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", o)):
         getattr(p, name)[:] = _strides(t, layout)
     if stream is None:
@@ -101,11 +121,12 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
              workspace: torch.Tensor | None = None, wrap_axes=None):
     """Fused exact attention forward over [B, H, N, d] bf16 tensors.
 
-    mask: 'none' | 'causal' | 'clamp' | 'wrap' (the last two: 2-D neighbourhood
-    attention over a grid_h x grid_w token grid, square by default, with an odd
-    `window`, or (rows, columns) windows; wrap_axes=(rows, columns) chooses
-    per axis whether the window wraps, overriding the mask name; a (1, N) grid
-    with window (1, k) is 1-D neighbourhood attention). Returns (o, lse) or o. CPU inputs are copied to the current
+    mask: 'none' | 'causal' | 'clamp' | 'wrap' (the last two: neighbourhood
+    attention over grid=(rows, columns), square by default, or a volume
+    grid=(depth, rows, columns), with an odd `window` or one per axis;
+    wrap_axes (one boolean per axis) chooses per axis whether the window
+    wraps, overriding the mask name; a (1, N) grid with window (1, k) is 1-D
+    neighbourhood attention). Returns (o, lse) or o. CPU inputs are copied to the current
     CUDA device, and the results back to the CPU (the end-to-end path).
     schedule: 0 automatic, 1 whole tasks per CTA, 2 equal shares of K/V tiles
     with cut tasks merged (unmasked only). workspace: optional zero-filled
@@ -161,13 +182,7 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
     p.dq, p.dk, p.dv = dq.data_ptr(), dk.data_ptr(), dv.data_ptr()
     p.B, p.H, p.Nq, p.Nk, p.d = B, H, Nq, Nk, d
     p.scale = float(scale)
-    p.mask_kind = _MASKS[mask]
-    if mask in ("clamp", "wrap"):
-        kh, kw, p.wrap = _na_axes(mask, window, wrap_axes)
-        p.window, p.window_w = kh, (kw if kw != kh else 0)
-        p.dilation = int(dilation)
-        if grid is not None:
-            p.grid_h, p.grid_w = int(grid[0]), int(grid[1])
+    _set_mask(p, mask, window, dilation, grid, wrap_axes)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     p.stream = stream.cuda_stream
@@ -259,6 +274,34 @@ def na2d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size, *,
             window=kernel_size, dilation=dilation, grid=(X, Y), layout="bxyhd", num_ctas=0,
             timeout_ns=0, inject=0, events=None, stream=stream,
             wrap_axes=(modes[0] == "wrap", modes[1] == "wrap"))
+    return (out, lse) if return_lse else out
+
+
+def na3d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size, *,
+         mode="clamp", dilation: int = 1, scale: float | None = None,
+         out: torch.Tensor | None = None, return_lse: bool = False, stream=None):
+    """3-D neighbourhood attention in NATTEN's heads-last layout [B, X, Y, Z, heads, d].
+
+    kernel_size: k, or (k_x, k_y, k_z). mode: 'clamp' | 'wrap', or one per axis
+    (x, y, z). The output has the same layout; no permute or copy is made.
+    """
+    modes = (mode,) * 3 if isinstance(mode, str) else tuple(mode)
+    if len(modes) != 3 or any(m not in ("clamp", "wrap") for m in modes):
+        raise ValueError("mode must be 'clamp' or 'wrap', or three of them")
+    if q.dim() != 6:
+        raise ValueError("expected [B, X, Y, Z, heads, d] tensors")
+    _check_dev(q, k, v)
+    B, X, Y, Z, H, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    n = X * Y * Z
+    lse = torch.empty((B, H, n), dtype=torch.float32, device=q.device) if return_lse else None
+    _launch(q, k, v, out, lse, B=B, H=H, Nq=n, Nk=n, d=d, scale=scale, mask="clamp",
+            window=kernel_size, dilation=dilation, grid=(X, Y, Z), layout="bxyzhd", num_ctas=0,
+            timeout_ns=0, inject=0, events=None, stream=stream,
+            wrap_axes=tuple(m == "wrap" for m in modes))
     return (out, lse) if return_lse else out
 
 

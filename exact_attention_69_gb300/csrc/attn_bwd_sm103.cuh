@@ -123,6 +123,21 @@ __device__ __forceinline__ void store_packed32(uint32_t taddr, const uint32_t (&
   tmem_st32(taddr, pk);
 }
 
+// Tiles of the other side a 128-token tile starting at t0 (of n tokens) may
+// meet: the neighbourhood band, else all `tiles`.
+template <int MASK>
+__host__ __device__ __forceinline__ Band bwd_band(int t0, int n, int tiles, const KernelParams& p) {
+  if constexpr (mask_is_na(MASK)) {
+    return na_band<MASK>(t0, min(t0 + kBM, n) - 1, p);
+  } else {
+    Band b;
+    b.lo0 = 0;
+    b.hi0 = tiles;
+    b.lo1 = b.hi1 = 0;
+    return b;
+  }
+}
+
 // ------------------------------------------------------------------ dQ
 
 // One CTA per (batch, head, 128-row Q tile).
@@ -143,6 +158,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
   const int bh = blockIdx.x / n_qt;
   const int q0 = (blockIdx.x - bh * n_qt) * kBM;
   const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
+  const Band band = bwd_band<MASK>(q0, p.Nq, p.n_kv, p);  // K/V tiles this Q tile may meet
 
   if (threadIdx.x == 0) {
     mbar_init(bars.a_full(), 1);
@@ -175,7 +191,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     load_tile<D>(sbase + BC::kOffA, &p.tm_q, bars.a_full(), q0, h, b);
     load_tile<D>(sbase + BC::kOffB, &bp.tm_do, bars.a_full(), q0, h, b);
     armed_a = 0;
-    for (int j = 0; j < p.n_kv; ++j) {
+    for (int j = band_next(band, -1); j < p.n_kv; j = band_next(band, j)) {
       if (tile_class<MASK>(q0, j, p) == 0) continue;
       const int s = static_cast<int>(it % BC::kStages);
       if (!warp_wait(bars.ring_empty(s), ((it / BC::kStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
@@ -198,7 +214,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     bool acc = false;
     if (!warp_wait(bars.a_full(), 0, ctl, -1, kRoleMma)) goto mdrain;
     tc_fence_after();
-    for (int j = 0; j < p.n_kv; ++j) {
+    for (int j = band_next(band, -1); j < p.n_kv; j = band_next(band, j)) {
       if (tile_class<MASK>(q0, j, p) == 0) continue;
       const int s = static_cast<int>(it % BC::kStages);
       if (!warp_wait(bars.ring_full(s), (it / BC::kStages) & 1u, ctl, j, kRoleMma)) goto mdrain;
@@ -238,13 +254,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     const int64_t ri = static_cast<int64_t>(bh) * p.Nq + q;
     const float lse2 = row_ok ? bp.lse[ri] * 1.44269504088896340736f : 0.f;
     const float drow = row_ok ? bp.dd[ri] : 0.f;
-    int qy = 0, qx = 0, wy = 0, wx = 0;
-    if (mask_is_na(MASK))
-      na_query_coords<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
-          p, q, qy, qx, wy, wx);
+    const NaQuery nq = na_query<MASK>(p, q);
     uint32_t s_par = 0;
     bool any = false;
-    for (int j = 0; j < p.n_kv; ++j) {
+    for (int j = band_next(band, -1); j < p.n_kv; j = band_next(band, j)) {
       const int cls = tile_class<MASK>(q0, j, p);
       if (cls == 0) continue;
       if (!warp_wait(bars.s_full(), s_par, ctl, j)) goto cdone;
@@ -255,7 +268,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
         uint32_t allk[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) allk[i] = 0u;
-        mask_tile<MASK>(allk, p, j, q, qy, qx, wy, wx);
+        mask_tile<MASK>(allk, p, j, q, nq);
         // mask_tile writes -inf bit patterns where a key is not allowed
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -335,23 +348,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 // key (ky, kx) in its window. Clamped windows are not symmetric at the grid's
 // borders, so each query's window is placed and tested.
 template <int MASK>
-__device__ __forceinline__ void na_key_bits(const KernelParams& p, int q0, int ky, int kx,
+__host__ __device__ __forceinline__ void na_key_bits(const KernelParams& p, int q0, int kk,
                                             uint32_t (&bits)[4]) {
-  constexpr bool WH = mask_na_wrap_rows(MASK), WW = mask_na_wrap_cols(MASK);
-  constexpr bool DIL = mask_na_dilated(MASK);
   bits[0] = bits[1] = bits[2] = bits[3] = 0u;
-  int qy = q0 / p.grid_w;
-  int qx = q0 - qy * p.grid_w;
   const int n = min(kBM, p.Nq - q0);
-  for (int e = 0; e < n; ++e) {
-    const int fy = na_window_first<WH, DIL>(qy, p.grid_h, p.window_h, p.dilation);
-    const int fx = na_window_first<WW, DIL>(qx, p.grid_w, p.window_w, p.dilation);
-    if (na_in_window<WH, DIL>(ky, fy, p.grid_h, p.window_h, p.dilation) &&
-        na_in_window<WW, DIL>(kx, fx, p.grid_w, p.window_w, p.dilation))
-      bits[e >> 5] |= 1u << (e & 31);
-    if (++qx == p.grid_w) {
-      qx = 0;
-      ++qy;
+  if constexpr (MASK == kMaskNa3) {
+    const bool wd = (p.na_wrap & kNa3WrapDepth) != 0, wh = (p.na_wrap & kNa3WrapRows) != 0,
+               ww = (p.na_wrap & kNa3WrapCols) != 0;
+    const int plane = p.grid_h * p.grid_w, dl = p.dilation;
+    const int kt = kk / plane, ky = (kk - kt * plane) / p.grid_w, kx = kk - kt * plane - ky * p.grid_w;
+    int qt = q0 / plane;
+    int qy = (q0 - qt * plane) / p.grid_w;
+    int qx = q0 - qt * plane - qy * p.grid_w;
+    for (int e = 0; e < n; ++e) {
+      if (na_in_rt(kt, na_first_rt(qt, p.grid_d, p.window_d, dl, wd), p.grid_d, p.window_d, dl, wd) &&
+          na_in_rt(ky, na_first_rt(qy, p.grid_h, p.window_h, dl, wh), p.grid_h, p.window_h, dl, wh) &&
+          na_in_rt(kx, na_first_rt(qx, p.grid_w, p.window_w, dl, ww), p.grid_w, p.window_w, dl, ww))
+        bits[e >> 5] |= 1u << (e & 31);
+      if (++qx == p.grid_w) {
+        qx = 0;
+        if (++qy == p.grid_h) {
+          qy = 0;
+          ++qt;
+        }
+      }
+    }
+  } else {
+    constexpr bool WH = mask_na_wrap_rows(MASK), WW = mask_na_wrap_cols(MASK);
+    constexpr bool DIL = mask_na_dilated(MASK);
+    const int ky = kk / p.grid_w, kx = kk - ky * p.grid_w;
+    int qy = q0 / p.grid_w;
+    int qx = q0 - qy * p.grid_w;
+    for (int e = 0; e < n; ++e) {
+      const int fy = na_window_first<WH, DIL>(qy, p.grid_h, p.window_h, p.dilation);
+      const int fx = na_window_first<WW, DIL>(qx, p.grid_w, p.window_w, p.dilation);
+      if (na_in_window<WH, DIL>(ky, fy, p.grid_h, p.window_h, p.dilation) &&
+          na_in_window<WW, DIL>(kx, fx, p.grid_w, p.window_w, p.dilation))
+        bits[e >> 5] |= 1u << (e & 31);
+      if (++qx == p.grid_w) {
+        qx = 0;
+        ++qy;
+      }
     }
   }
 }
@@ -375,6 +412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
   const int k0 = j * kBN;
   const int b = bh / p.H, h = bh - (bh / p.H) * p.H;
   const int n_qt = (p.Nq + kBM - 1) / kBM;
+  const Band band = bwd_band<MASK>(k0, p.Nk, n_qt, p);  // Q tiles that may meet this K/V tile
 
   if (threadIdx.x == 0) {
     mbar_init(bars.a_full(), 1);
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
     load_tile<D>(sbase + BC::kOffA, &p.tm_k, bars.a_full(), k0, h, b);
     load_tile<D>(sbase + BC::kOffB, &p.tm_v, bars.a_full(), k0, h, b);
     armed_a = 0;
-    for (int i = 0; i < n_qt; ++i) {
+    for (int i = band_next(band, -1); i < n_qt; i = band_next(band, i)) {
       if (tile_class<MASK>(i * kBM, j, p) == 0) continue;
       const int s = static_cast<int>(it % BC::kStages);
       if (!warp_wait(bars.ring_empty(s), ((it / BC::kStages) & 1u) ^ 1u, ctl, i, kRoleLoader))
@@ -439,7 +477,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
     bool acc = false;
     if (!warp_wait(bars.a_full(), 0, ctl, -1, kRoleMma)) goto mdrain;
     tc_fence_after();
-    for (int i = 0; i < n_qt; ++i) {
+    for (int i = band_next(band, -1); i < n_qt; i = band_next(band, i)) {
       if (tile_class<MASK>(i * kBM, j, p) == 0) continue;
       const int s = static_cast<int>(it % BC::kStages);
       if (!warp_wait(bars.ring_full(s), (it / BC::kStages) & 1u, ctl, i, kRoleMma)) goto mdrain;
@@ -481,7 +519,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint32_t s_par = 0, it = 0;
     bool any = false;
-    for (int i = 0; i < n_qt; ++i) {
+    for (int i = band_next(band, -1); i < n_qt; i = band_next(band, i)) {
       if (tile_class<MASK>(i * kBM, j, p) == 0) continue;
       const int s = static_cast<int>(it % BC::kStages);
       // the loader's vector stores are ordered by ring_full (already complete once S^T is)
@@ -495,10 +533,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
       // causal: query q sees key kk iff q >= kk; first allowed column of this tile
       const int first = MASK == kMaskCausal ? kk - q0 : 0;
       uint32_t nab[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-      if (mask_is_na(MASK)) {
-        const int ky = kk / p.grid_w;
-        na_key_bits<MASK>(p, q0, ky, kk - ky * p.grid_w, nab);
-      }
+      if (mask_is_na(MASK)) na_key_bits<MASK>(p, q0, kk, nab);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t sv[64], pv[64];
@@ -604,6 +639,7 @@ cudaError_t launch_bwd_dim(const BwdParams& bp, int mask, cudaStream_t s) {
     case kMaskNa + 5: return launch_bwd_mask<D, kMaskNa + 5>(bp, s);
     case kMaskNa + 6: return launch_bwd_mask<D, kMaskNa + 6>(bp, s);
     case kMaskNa + 7: return launch_bwd_mask<D, kMaskNa + 7>(bp, s);
+    case kMaskNa3: return launch_bwd_mask<D, kMaskNa3>(bp, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -101,7 +101,7 @@ int64_t isqrt64(int64_t n) {
 
 // Host-only argument checks; fills the derived grid and strides.
 struct Checked {
-  int grid_h = 0, grid_w = 0;
+  int grid_h = 0, grid_w = 0, grid_d = 0;
   int64_t qs[3], ks[3], vs[3], os[3];
 };
 
@@ -134,17 +134,20 @@ int validate(const attn_params_ex* p, Checked* c) {
     return fail(ATTN_ERR_UNSUPPORTED, "head dimension %d is not one of 32, 64, 128", p->d);
   if (!std::isfinite(p->scale) || !(p->scale > 0.f))
     return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
-  if (p->mask_kind < ATTN_MASK_NONE || p->mask_kind > ATTN_MASK_NA2D)
+  if (p->mask_kind < ATTN_MASK_NONE || p->mask_kind > ATTN_MASK_NA3D)
     return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", p->mask_kind);
   const int64_t BH = static_cast<int64_t>(p->B) * p->H;
   const int64_t n_qpairs = (static_cast<int64_t>(p->Nq) + 2 * attn::kBM - 1) / (2 * attn::kBM);
   if (BH * n_qpairs >= (int64_t{1} << 31))
     return fail(ATTN_ERR_INVALID_ARG, "too many (batch, head, query-tile) tasks");
-  if (p->mask_kind != ATTN_MASK_NA2D) {
+  const bool na3 = p->mask_kind == ATTN_MASK_NA3D;
+  if (!na3 && (p->grid_d != 0 || p->window_d != 0 || p->wrap_d != 0))
+    return fail(ATTN_ERR_INVALID_ARG, "grid_d/window_d/wrap_d apply to NA3D only (need 0)");
+  if (p->mask_kind != ATTN_MASK_NA2D && !na3) {
     if (p->window != 0 || p->window_w != 0 || p->dilation != 1 || p->wrap != 0 ||
         p->grid_h != 0 || p->grid_w != 0)
       return fail(ATTN_ERR_INVALID_ARG,
-                  "window/dilation/wrap/grid apply to NA2D only (need 0/1/0/0x0)");
+                  "window/dilation/wrap/grid apply to NA2D and NA3D only (need 0/1/0/0x0)");
   } else {
     if (p->wrap < 0 || p->wrap > 3)
       return fail(ATTN_ERR_INVALID_ARG, "wrap must be 0 (none), 1 (both axes), 2 (rows) or 3 "
@@ -155,8 +158,24 @@ int validate(const attn_params_ex* p, Checked* c) {
       return fail(ATTN_ERR_INVALID_ARG, "window_w must be 0 or odd and >= 1 (got %d)",
                   p->window_w);
     if (p->dilation < 1) return fail(ATTN_ERR_INVALID_ARG, "dilation must be >= 1");
-    if (p->Nq != p->Nk) return fail(ATTN_ERR_INVALID_ARG, "NA2D needs Nq == Nk");
-    if (p->grid_h == 0 && p->grid_w == 0) {
+    if (p->Nq != p->Nk) return fail(ATTN_ERR_INVALID_ARG, "neighbourhood masks need Nq == Nk");
+    if (na3) {
+      if (p->wrap_d != 0 && p->wrap_d != 1) return fail(ATTN_ERR_INVALID_ARG, "wrap_d must be 0 or 1");
+      if (p->window_d != 0 && (p->window_d < 1 || p->window_d % 2 == 0))
+        return fail(ATTN_ERR_INVALID_ARG, "window_d must be 0 or odd and >= 1 (got %d)",
+                    p->window_d);
+      if (p->grid_d < 1 || p->grid_h < 1 || p->grid_w < 1 ||
+          static_cast<int64_t>(p->grid_d) * p->grid_h * p->grid_w != p->Nq)
+        return fail(ATTN_ERR_INVALID_ARG, "NA3D volume %dx%dx%d does not hold Nq=%d tokens",
+                    p->grid_d, p->grid_h, p->grid_w, p->Nq);
+      const int kd = p->window_d ? p->window_d : p->window;
+      if (kd > 1 && static_cast<int64_t>(kd) * p->dilation > p->grid_d)
+        return fail(ATTN_ERR_INVALID_ARG, "window_d*dilation (%lld) exceeds the depth %d",
+                    static_cast<long long>(kd) * p->dilation, p->grid_d);
+      c->grid_d = p->grid_d;
+      c->grid_h = p->grid_h;
+      c->grid_w = p->grid_w;
+    } else if (p->grid_h == 0 && p->grid_w == 0) {
       const int64_t g = isqrt64(p->Nq);
       if (g * g != p->Nq)
         return fail(ATTN_ERR_INVALID_ARG, "NA2D with Nq=%d needs a square grid or grid_h/grid_w",
@@ -201,6 +220,27 @@ int validate(const attn_params_ex* p, Checked* c) {
   if ((rc = check_strides(p->v_stride, c->vs, p->Nk, p->H, p->d, "v")) != ATTN_OK) return rc;
   if ((rc = check_strides(p->o_stride, c->os, p->Nq, p->H, p->d, "o")) != ATTN_OK) return rc;
   return ATTN_OK;
+}
+
+// Kernel mask variant of a validated problem; fills the neighbourhood fields of kp.
+int kernel_mask(const attn_params_ex* p, const Checked& c, attn::KernelParams* kp) {
+  const bool na = p->mask_kind == ATTN_MASK_NA2D || p->mask_kind == ATTN_MASK_NA3D;
+  const bool wrap_rows = p->wrap == 1 || p->wrap == 2, wrap_cols = p->wrap == 1 || p->wrap == 3;
+  kp->grid_h = c.grid_h;
+  kp->grid_w = c.grid_w;
+  kp->grid_d = c.grid_d;
+  kp->window_h = p->window;
+  kp->window_w = p->window_w ? p->window_w : p->window;
+  kp->window_d = p->window_d ? p->window_d : p->window;
+  kp->dilation = na ? p->dilation : 1;
+  kp->na_wrap = (wrap_cols ? attn::kNa3WrapCols : 0) | (wrap_rows ? attn::kNa3WrapRows : 0) |
+                (p->wrap_d ? attn::kNa3WrapDepth : 0);
+  switch (p->mask_kind) {
+    case ATTN_MASK_CAUSAL: return attn::kMaskCausal;
+    case ATTN_MASK_NA2D: return attn::na_mask(wrap_rows, wrap_cols, p->dilation > 1);
+    case ATTN_MASK_NA3D: return attn::kMaskNa3;
+    default: return attn::kMaskNone;
+  }
 }
 
 int get_encoder() {
@@ -342,11 +382,7 @@ int attn_fwd_ex(const attn_params_ex* p) {
   kp.Nq = p->Nq;
   kp.Nk = p->Nk;
   kp.c = p->scale * 1.4426950408889634f;
-  kp.grid_h = c.grid_h;
-  kp.grid_w = c.grid_w;
-  kp.window_h = p->window;
-  kp.window_w = p->window_w ? p->window_w : p->window;
-  kp.dilation = p->mask_kind == ATTN_MASK_NA2D ? p->dilation : 1;
+  const int mask = kernel_mask(p, c, &kp);
   Plan pl;
   if ((rc = make_plan(p, ds->sm_count, &pl)) != ATTN_OK) return rc;
   kp.n_qpairs = pl.n_qpairs;
@@ -364,12 +400,6 @@ int attn_fwd_ex(const attn_params_ex* p) {
   kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
   kp.inject = p->inject;
   kp.status = ds->status;
-
-  int mask = attn::kMaskNone;
-  if (p->mask_kind == ATTN_MASK_CAUSAL) mask = attn::kMaskCausal;
-  if (p->mask_kind == ATTN_MASK_NA2D)
-    mask = attn::na_mask(p->wrap == 1 || p->wrap == 2, p->wrap == 1 || p->wrap == 3,
-                         p->dilation > 1);
 
   const int grid = pl.grid;
 
@@ -521,6 +551,9 @@ int attn_bwd(const attn_bwd_params* p) {
   fp.wrap = p->wrap;
   fp.grid_h = p->grid_h;
   fp.grid_w = p->grid_w;
+  fp.grid_d = p->grid_d;
+  fp.window_d = p->window_d;
+  fp.wrap_d = p->wrap_d;
   Checked c;
   int rc = validate(&fp, &c);
   if (rc != ATTN_OK) return rc;
@@ -569,11 +602,7 @@ int attn_bwd(const attn_bwd_params* p) {
   kp.Nq = p->Nq;
   kp.Nk = p->Nk;
   kp.c = p->scale * 1.4426950408889634f;
-  kp.grid_h = c.grid_h;
-  kp.grid_w = c.grid_w;
-  kp.window_h = p->window;
-  kp.window_w = p->window_w ? p->window_w : p->window;
-  kp.dilation = p->mask_kind == ATTN_MASK_NA2D ? p->dilation : 1;
+  const int mask = kernel_mask(&fp, c, &kp);
   kp.n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
   kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
   kp.status = ds->status;
@@ -585,10 +614,6 @@ int attn_bwd(const attn_bwd_params* p) {
   bp.dk = p->dk;
   bp.dv = p->dv;
   bp.scale = p->scale;
-  int mask = p->mask_kind == ATTN_MASK_CAUSAL ? attn::kMaskCausal : attn::kMaskNone;
-  if (p->mask_kind == ATTN_MASK_NA2D)
-    mask = attn::na_mask(p->wrap == 1 || p->wrap == 2, p->wrap == 1 || p->wrap == 3,
-                         p->dilation > 1);
   cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
   const cudaError_t e = attn::launch_bwd(bp, p->d, mask, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");

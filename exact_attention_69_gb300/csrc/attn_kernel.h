@@ -17,29 +17,34 @@ constexpr int kRegsSoftmax = 216;  // registers per thread of warpgroups 1-2 aft
 // 128 * kRegsControl + 256 * kRegsSoftmax must not exceed 384 * 168 (the launch's registers)
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * 168, "register split");
 constexpr int kThreads = kWarps * 32;
-constexpr float kRescaleLog2 = 8.0f;
-constexpr int kMaxSplitCtas = 256;  // largest grid of the split schedule (its range table lives in shared memory)  // keep a stale row maximum until the true one exceeds it by 2^8
+constexpr float kRescaleLog2 = 8.0f;  // keep a stale row maximum until the true one exceeds it by 2^8
+constexpr int kMaxSplitCtas = 256;  // largest grid of the split schedule (its range table lives in shared memory)
 
 // Mask specialisations (the C-ABI's NA2D splits into clamp and wrap here).
 // Kernel variants. Neighbourhood masks are kMaskNa plus flags: which axes
 // wrap (rows, columns) and whether the windows are dilated, so that each
 // combination compiles to its own arithmetic (dilation 1 keeps intervals).
+// Volumes (3-D windows) are one further variant, kMaskNa3, that reads the
+// wrap choice of each axis and the dilation at run time.
 enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskNa = 2 };
 constexpr int kNaWrapCols = 1, kNaWrapRows = 2, kNaDilated = 4;
-constexpr int kMaskKinds = kMaskNa + 8;
+constexpr int kMaskNa3 = kMaskNa + 8;
+constexpr int kMaskKinds = kMaskNa3 + 1;
+constexpr int kNa3WrapCols = 1, kNa3WrapRows = 2, kNa3WrapDepth = 4;  // KernelParams::na_wrap
 __host__ __device__ constexpr int na_mask(bool wrap_rows, bool wrap_cols, bool dilated) {
   return kMaskNa + (wrap_cols ? kNaWrapCols : 0) + (wrap_rows ? kNaWrapRows : 0) +
          (dilated ? kNaDilated : 0);
 }
 __host__ __device__ constexpr bool mask_is_na(int m) { return m >= kMaskNa; }
+__host__ __device__ constexpr bool mask_is_na2(int m) { return m >= kMaskNa && m < kMaskNa3; }
 __host__ __device__ constexpr bool mask_na_wrap_rows(int m) {
-  return m >= kMaskNa && ((m - kMaskNa) & kNaWrapRows) != 0;
+  return mask_is_na2(m) && ((m - kMaskNa) & kNaWrapRows) != 0;
 }
 __host__ __device__ constexpr bool mask_na_wrap_cols(int m) {
-  return m >= kMaskNa && ((m - kMaskNa) & kNaWrapCols) != 0;
+  return mask_is_na2(m) && ((m - kMaskNa) & kNaWrapCols) != 0;
 }
 __host__ __device__ constexpr bool mask_na_dilated(int m) {
-  return m >= kMaskNa && ((m - kMaskNa) & kNaDilated) != 0;
+  return mask_is_na2(m) && ((m - kMaskNa) & kNaDilated) != 0;
 }
 
 // Roles recorded in the device status word when a bounded wait runs out.
@@ -57,6 +62,8 @@ struct KernelParams {
   int grid_h, grid_w;           // neighbourhood masks only: token grid
   int window_h, window_w;       // window size along the rows and the columns
   int dilation;                 // neighbourhood masks: key stride along each axis (>= 1)
+  int grid_d, window_d;         // kMaskNa3: depth of the volume and window along it
+  int na_wrap;                  // kMaskNa3: kNa3Wrap* bits of the axes that wrap
   int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head
   int n_kv;                     // ceil(Nk / 128)
   int n_tasks;                  // B * H * n_qpairs

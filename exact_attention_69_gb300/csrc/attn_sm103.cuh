@@ -453,12 +453,11 @@ template <bool WRAP_H, bool WRAP_W, bool DIL>
 __host__ __device__ __forceinline__ bool na_tile_meets(int q0, int q1, int k0, int k1, const KernelParams& p) {
   const int W = p.grid_w;
   const int kr0 = k0 / W, kr1 = (k1 - 1) / W;
-  for (int qa = q0; qa < q1;) {
-    const int qr = qa / W;
+  // rows advance one by one: no division inside the loops
+  for (int qa = q0, qr = q0 / W; qa < q1; ++qr) {
     const int qb = min(q1, (qr + 1) * W);
     if (axis_meets_nd<WRAP_H, DIL>(qr, qr, kr0, kr1, p.grid_h, p.window_h, p.dilation)) {
-      for (int ka = k0; ka < k1;) {
-        const int kr = ka / W;
+      for (int ka = k0, kr = kr0; ka < k1; ++kr) {
         const int kb = min(k1, (kr + 1) * W);
         if (axis_meets_nd<WRAP_H, DIL>(qr, qr, kr, kr, p.grid_h, p.window_h, p.dilation) &&
             axis_meets_nd<WRAP_W, DIL>(qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W,
@@ -470,6 +469,150 @@ __host__ __device__ __forceinline__ bool na_tile_meets(int q0, int q1, int k0, i
     qa = qb;
   }
   return false;
+}
+
+// axis_meets_nd with the wrap choice and the dilation read at run time.
+__host__ __device__ __forceinline__ bool axis_meets_rt(bool wrap, int c0, int c1, int e0, int e1,
+                                                       int G, int w, int dl) {
+  if (dl > 1)
+    return wrap ? axis_meets_dilated<true>(c0, c1, e0, e1, G, w, dl)
+                : axis_meets_dilated<false>(c0, c1, e0, e1, G, w, dl);
+  return wrap ? axis_meets<true>(c0, c1, e0, e1, G, w) : axis_meets<false>(c0, c1, e0, e1, G, w);
+}
+
+// na_tile_meets for a volume (depth, rows, columns; depth slowest). A line of
+// the volume (fixed depth and row) holds grid_w consecutive tokens; the Q and
+// K ranges are cut into line segments and each pair of segments is tested
+// axis by axis (depth first, for the cheap rejection of far slices).
+__host__ __device__ __forceinline__ bool na3_tile_meets(int q0, int q1, int k0, int k1,
+                                                        const KernelParams& p) {
+  const int W = p.grid_w, Gh = p.grid_h, dl = p.dilation;
+  const bool wd = (p.na_wrap & kNa3WrapDepth) != 0, wh = (p.na_wrap & kNa3WrapRows) != 0,
+             ww = (p.na_wrap & kNa3WrapCols) != 0;
+  const int kr0 = k0 / W, kt0 = kr0 / Gh, ky0 = kr0 - kt0 * Gh, kt1 = ((k1 - 1) / W) / Gh;
+  int qr = q0 / W;
+  int qt = qr / Gh, qy = qr - qt * Gh;
+  // lines advance one by one (row, then depth): no division inside the loops
+  for (int qa = q0; qa < q1;) {
+    const int qb = min(q1, (qr + 1) * W);
+    if (axis_meets_rt(wd, qt, qt, kt0, kt1, p.grid_d, p.window_d, dl)) {
+      int kt = kt0, ky = ky0;
+      for (int ka = k0, kr = kr0; ka < k1; ++kr) {
+        const int kb = min(k1, (kr + 1) * W);
+        if (axis_meets_rt(wd, qt, qt, kt, kt, p.grid_d, p.window_d, dl) &&
+            axis_meets_rt(wh, qy, qy, ky, ky, Gh, p.window_h, dl) &&
+            axis_meets_rt(ww, qa - qr * W, qb - 1 - qr * W, ka - kr * W, kb - 1 - kr * W, W,
+                          p.window_w, dl))
+          return true;
+        ka = kb;
+        if (++ky == Gh) {
+          ky = 0;
+          ++kt;
+        }
+      }
+    }
+    qa = qb;
+    ++qr;
+    if (++qy == Gh) {
+      qy = 0;
+      ++qt;
+    }
+  }
+  return false;
+}
+
+// Tiles (128 tokens, for K/V and for Q alike) that can hold a partner of some
+// token in [a, b] (inclusive): at most two half-open intervals [lo0, hi0) and
+// [lo1, hi1), in increasing order. A superset, from the slowest grid axis that
+// is longer than one: a clamped window keeps every key within dl * (w - 1) of
+// its query on each axis and a wrapped one within dl * (w / 2) circularly;
+// both bounds hold in either direction (the keys of a query, the queries of a
+// key), so the forward and the backward passes share the band.
+struct Band {
+  int lo0, hi0, lo1, hi1;
+};
+
+template <int MASK>
+__host__ __device__ __forceinline__ Band na_band(int a, int b, const KernelParams& p) {
+  int unit, G, w;
+  bool wrap;
+  if (MASK == kMaskNa3 && p.grid_d > 1) {
+    unit = p.grid_h * p.grid_w;
+    G = p.grid_d;
+    w = p.window_d;
+    wrap = (p.na_wrap & kNa3WrapDepth) != 0;
+  } else if (p.grid_h > 1) {
+    unit = p.grid_w;
+    G = p.grid_h;
+    w = p.window_h;
+    wrap = MASK == kMaskNa3 ? (p.na_wrap & kNa3WrapRows) != 0 : mask_na_wrap_rows(MASK);
+  } else {
+    unit = 1;
+    G = p.grid_w;
+    w = p.window_w;
+    wrap = MASK == kMaskNa3 ? (p.na_wrap & kNa3WrapCols) != 0 : mask_na_wrap_cols(MASK);
+  }
+  const int dl = (MASK == kMaskNa3 || mask_na_dilated(MASK)) ? p.dilation : 1;
+  const int c0 = a / unit, c1 = b / unit;
+  int x0, x1, y0 = 0, y1 = -1;  // coordinate intervals [x0, x1] then [y0, y1]
+  if (wrap) {
+    const int reach = dl * (w >> 1);
+    const int lo = c0 - reach, hi = c1 + reach;
+    if (c1 - c0 + 1 + 2 * reach >= G) {
+      x0 = 0;
+      x1 = G - 1;
+    } else if (lo < 0) {
+      x0 = 0;
+      x1 = hi;
+      y0 = lo + G;
+      y1 = G - 1;
+    } else if (hi >= G) {
+      x0 = 0;
+      x1 = hi - G;
+      y0 = lo;
+      y1 = G - 1;
+    } else {
+      x0 = lo;
+      x1 = hi;
+    }
+  } else {
+    const int reach = dl * (w - 1);
+    x0 = max(c0 - reach, 0);
+    x1 = min(c1 + reach, G - 1);
+  }
+  Band r;
+  r.lo0 = x0 * unit / kBN;
+  r.hi0 = ((x1 + 1) * unit - 1) / kBN + 1;
+  r.lo1 = r.hi1 = 0;
+  if (y1 >= y0) {
+    r.lo1 = y0 * unit / kBN;
+    r.hi1 = ((y1 + 1) * unit - 1) / kBN + 1;
+  }
+  return r;
+}
+
+// The first tile of the band after tile j (a large number if none).
+__host__ __device__ __forceinline__ int band_next(const Band& b, int j) {
+  ++j;
+  if (j < b.lo0) return b.lo0;
+  if (j < b.hi0) return j;
+  if (j < b.lo1) j = b.lo1;
+  return j < b.hi1 ? j : 0x7fffffff;
+}
+
+// K/V tiles a task may visit: the band of its queries (every tile without a
+// neighbourhood mask).
+template <int MASK>
+__host__ __device__ __forceinline__ Band task_band(const Task& tk, const KernelParams& p) {
+  if constexpr (mask_is_na(MASK)) {
+    return na_band<MASK>(tk.q0[0], min(tk.q0[1] + kBM, p.Nq) - 1, p);
+  } else {
+    Band b;
+    b.lo0 = 0;
+    b.hi0 = p.n_kv;
+    b.lo1 = b.hi1 = 0;
+    return b;
+  }
 }
 
 // 0: no query of the tile attends any key of KV tile j (skip it);
@@ -484,6 +627,7 @@ __host__ __device__ __forceinline__ int tile_class(int q0, int j, const KernelPa
     if (k0 > q1 - 1) return 0;
     return (!ragged && k0 + kBN - 1 <= q0) ? 1 : 2;
   }
+  if (MASK == kMaskNa3) return na3_tile_meets(q0, q1, k0, min(k0 + kBN, p.Nk), p) ? 2 : 0;
   return na_tile_meets<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
              q0, q1, k0, min(k0 + kBN, p.Nk), p)
              ? 2 : 0;
@@ -494,14 +638,18 @@ __host__ __device__ __forceinline__ bool tile_active(const Task& tk, int h, int 
   return tk.live[h] && tile_class<MASK>(tk.q0[h], j, p) != 0;
 }
 
-// Next KV tile after j that some live Q tile of the task needs (n_kv if none).
 // Next KV tile after j and before `end` that some live Q tile of the task
-// needs (`end` if none).
+// needs (`end` if none); neighbourhood masks look only inside the task's band.
 template <int MASK>
-__host__ __device__ __forceinline__ int next_tile(const Task& tk, int j, int end,
+__host__ __device__ __forceinline__ int next_tile(const Task& tk, const Band& band, int j, int end,
                                                   const KernelParams& p) {
-  for (++j; j < end; ++j)
-    if (tile_active<MASK>(tk, 0, j, p) || tile_active<MASK>(tk, 1, j, p)) return j;
+  if constexpr (mask_is_na(MASK)) {
+    for (j = band_next(band, j); j < end; j = band_next(band, j))
+      if (tile_active<MASK>(tk, 0, j, p) || tile_active<MASK>(tk, 1, j, p)) return j;
+  } else {
+    for (++j; j < end; ++j)
+      if (tile_active<MASK>(tk, 0, j, p) || tile_active<MASK>(tk, 1, j, p)) return j;
+  }
   return end;
 }
 
@@ -616,6 +764,34 @@ __host__ __device__ __forceinline__ void set_bits(uint32_t (&bits)[4], int lo, i
   }
 }
 
+// Columns of one key line that the window's columns cover: the line's
+// columns [kx0, kx0 + len) sit at bits base + kx0 ... (base = bit of column 0).
+// With dilation 1 they form one interval (two when a wrapped window crosses
+// the last column); with dilation > 1 they are set one by one.
+template <bool WRAP_W, bool DIL>
+__host__ __device__ __forceinline__ void na_line_cols(uint32_t (&bits)[4], int base, int kx0, int len,
+                                                      int wx, int G_w, int w, int dl) {
+  if (!DIL) {
+    const int e1 = min(wx + w, G_w);
+    int lo = max(wx, kx0), hi = min(e1, kx0 + len);
+    if (lo < hi) set_bits(bits, base + lo, base + hi);
+    if (WRAP_W && wx + w > G_w) {  // the window wraps past the last column
+      lo = kx0;
+      hi = min(wx + w - G_w, kx0 + len);
+      if (lo < hi) set_bits(bits, base + lo, base + hi);
+    }
+  } else {
+    for (int t = 0; t < w; ++t) {
+      int cx = wx + dl * t;
+      if (WRAP_W && cx >= G_w) cx -= G_w;
+      if (cx >= kx0 && cx < kx0 + len) {
+        const int bit = base + cx;
+        bits[bit >> 5] |= 1u << (bit & 31);
+      }
+    }
+  }
+}
+
 // Allowed keys of query (qy, qx) in the K/V tile starting at key k0, as bits
 // of a 128-bit mask (bit i: key k0 + i). The window's rows are wy + dl * t,
 // t in [0, w_h), and its columns wx + dl * t, t in [0, w_w) (modulo the grid
@@ -632,30 +808,81 @@ __host__ __device__ __forceinline__ void na_tile_bits(const KernelParams& p, int
   int kx0 = k0 - ky * G_w;
   for (int i = 0; i < nvalid; ++ky) {
     const int len = min(G_w - kx0, nvalid - i);  // this row's columns [kx0, kx0 + len)
-    if (na_in_window<WRAP_H, DIL>(ky, wy, G_h, w_h, dl)) {
-      const int base = i - kx0;  // bit of column 0 of this row
-      if (!DIL) {
-        const int e1 = min(wx + w, G_w);
-        int lo = max(wx, kx0), hi = min(e1, kx0 + len);
-        if (lo < hi) set_bits(bits, base + lo, base + hi);
-        if (WRAP_W && wx + w > G_w) {  // the window wraps past the last column
-          lo = kx0;
-          hi = min(wx + w - G_w, kx0 + len);
-          if (lo < hi) set_bits(bits, base + lo, base + hi);
-        }
+    if (na_in_window<WRAP_H, DIL>(ky, wy, G_h, w_h, dl))
+      na_line_cols<WRAP_W, DIL>(bits, i - kx0, kx0, len, wx, G_w, w, dl);
+    i += len;
+    kx0 = 0;
+  }
+}
+
+// ---- volumes (kMaskNa3): the same rules with the wrap choice and dilation
+// read at run time, and a depth axis slower than the rows ----
+
+__host__ __device__ __forceinline__ int na_first_rt(int c, int G, int w, int dl, bool wrap) {
+  return wrap ? na_window_first<true, true>(c, G, w, dl) : na_window_first<false, true>(c, G, w, dl);
+}
+
+__host__ __device__ __forceinline__ bool na_in_rt(int k, int f, int G, int w, int dl, bool wrap) {
+  if (dl == 1) return wrap ? na_in_window<true, false>(k, f, G, w, 1) : na_in_window<false, false>(k, f, G, w, 1);
+  return wrap ? na_in_window<true, true>(k, f, G, w, dl) : na_in_window<false, true>(k, f, G, w, dl);
+}
+
+// A query's grid coordinates and the first key coordinate of its window on
+// each axis (depth only for volumes).
+struct NaQuery {
+  int qy = 0, qx = 0, wy = 0, wx = 0, qt = 0, wt = 0;
+};
+
+template <int MASK>
+__host__ __device__ __forceinline__ NaQuery na_query(const KernelParams& p, int q) {
+  NaQuery n;
+  if constexpr (MASK == kMaskNa3) {
+    const int plane = p.grid_h * p.grid_w;
+    n.qt = q / plane;
+    const int r = q - n.qt * plane;
+    n.qy = r / p.grid_w;
+    n.qx = r - n.qy * p.grid_w;
+    n.wt = na_first_rt(n.qt, p.grid_d, p.window_d, p.dilation, (p.na_wrap & kNa3WrapDepth) != 0);
+    n.wy = na_first_rt(n.qy, p.grid_h, p.window_h, p.dilation, (p.na_wrap & kNa3WrapRows) != 0);
+    n.wx = na_first_rt(n.qx, p.grid_w, p.window_w, p.dilation, (p.na_wrap & kNa3WrapCols) != 0);
+  } else if constexpr (mask_is_na2(MASK)) {
+    na_query_coords<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
+        p, q, n.qy, n.qx, n.wy, n.wx);
+  }
+  return n;
+}
+
+// na_tile_bits for a volume: a key line (fixed depth and row) is kept when
+// both its depth and its row are in the query's window, then its columns are
+// set as in two dimensions.
+__host__ __device__ __forceinline__ void na3_tile_bits(const KernelParams& p, int k0, const NaQuery& n,
+                                                       uint32_t (&bits)[4]) {
+  const int G_h = p.grid_h, G_w = p.grid_w, dl = p.dilation;
+  const bool wd = (p.na_wrap & kNa3WrapDepth) != 0, wh = (p.na_wrap & kNa3WrapRows) != 0,
+             ww = (p.na_wrap & kNa3WrapCols) != 0;
+  bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+  const int nvalid = min(kBN, p.Nk - k0);
+  const int r0 = k0 / G_w;
+  int kt = r0 / G_h, ky = r0 - kt * G_h;
+  int kx0 = k0 - r0 * G_w;
+  for (int i = 0; i < nvalid;) {
+    const int len = min(G_w - kx0, nvalid - i);
+    if (na_in_rt(kt, n.wt, p.grid_d, p.window_d, dl, wd) && na_in_rt(ky, n.wy, G_h, p.window_h, dl, wh)) {
+      const int base = i - kx0;
+      if (dl == 1) {
+        if (ww) na_line_cols<true, false>(bits, base, kx0, len, n.wx, G_w, p.window_w, 1);
+        else na_line_cols<false, false>(bits, base, kx0, len, n.wx, G_w, p.window_w, 1);
       } else {
-        for (int t = 0; t < w; ++t) {
-          int cx = wx + dl * t;
-          if (WRAP_W && cx >= G_w) cx -= G_w;
-          if (cx >= kx0 && cx < kx0 + len) {
-            const int bit = base + cx;
-            bits[bit >> 5] |= 1u << (bit & 31);
-          }
-        }
+        if (ww) na_line_cols<true, true>(bits, base, kx0, len, n.wx, G_w, p.window_w, dl);
+        else na_line_cols<false, true>(bits, base, kx0, len, n.wx, G_w, p.window_w, dl);
       }
     }
     i += len;
     kx0 = 0;
+    if (++ky == G_h) {
+      ky = 0;
+      ++kt;
+    }
   }
 }
 
@@ -674,6 +901,7 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
+    const Band band = task_band<MASK>(tk, p);
     if (!warp_wait(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, -1, kRoleLoader)) goto drain;
     mbar_expect_tx(bars.q_full(), 2 * C::kTileBytes);
     for (int h = 0; h < 2; ++h)
@@ -683,8 +911,8 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
     q_armed = static_cast<int>(q_it & 1u);
     ++q_it;
     int nth = 0;
-    for (int j = next_tile<MASK>(tk, sg.kv0 - 1, sg.kv1, p); j < sg.kv1;
-         j = next_tile<MASK>(tk, j, sg.kv1, p), ++nth) {
+    for (int j = next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p); j < sg.kv1;
+         j = next_tile<MASK>(tk, band, j, sg.kv1, p), ++nth) {
       const int ks = static_cast<int>(k_it % C::kKStages);
       if (!warp_wait(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
         goto drain;
@@ -773,11 +1001,12 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
+    const Band band = task_band<MASK>(tk, p);
     if (!warp_wait(bars.q_full(), q_it & 1u, ctl, -1, kRoleMma)) goto drain;
     ++q_it;
     tc_fence_after();
     bool o_ready[2] = {false, false};
-    int j = next_tile<MASK>(tk, sg.kv0 - 1, sg.kv1, p);
+    int j = next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
     if (j < sg.kv1) {
       const int ks = static_cast<int>(k_it % C::kKStages);
       if (!warp_wait(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, j, kRoleMma)) goto drain;
@@ -792,7 +1021,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       ++k_it;
     }
     while (j < sg.kv1) {
-      const int jn = next_tile<MASK>(tk, j, sg.kv1, p);
+      const int jn = next_tile<MASK>(tk, band, j, sg.kv1, p);
       const bool has_next = jn < sg.kv1;
       if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
       const int vs = static_cast<int>(v_it % C::kVStages);
@@ -1024,7 +1253,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
 // Keys of a partial tile (class 2) that the query may not see become -inf.
 template <int MASK>
 __device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams& p, int j, int q,
-                                          int qy, int qx, int wy, int wx) {
+                                          const NaQuery& nq) {
   const uint32_t neg_inf = __float_as_uint(-CUDART_INF_F);
   const int k0 = j * kBN;
   if (MASK == kMaskNone || MASK == kMaskCausal) {
@@ -1039,8 +1268,11 @@ __device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams
     // keys as a 128-bit mask, one column interval per row segment,
     // then clear the rest with independent selects.
     uint32_t bits[4];
-    na_tile_bits<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
-        p, k0, qy, qx, wy, wx, bits);
+    if constexpr (MASK == kMaskNa3)
+      na3_tile_bits(p, k0, nq, bits);
+    else
+      na_tile_bits<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
+          p, k0, nq.qy, nq.qx, nq.wy, nq.wx, bits);
 #pragma unroll
     for (int i = 0; i < 128; ++i)
       if (((bits[i >> 5] >> (i & 31)) & 1u) == 0u) s[i] = neg_inf;
@@ -1095,17 +1327,16 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     if (!tk.live[hh]) continue;
     const int q0 = tk.q0[hh];
     const int q = q0 + row;
-    // neighbourhood: this query's grid coordinates and clamped window starts
-    int qy = 0, qx = 0, wy = 0, wx = 0;
-    if (mask_is_na(MASK))
-      na_query_coords<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
-          p, q, qy, qx, wy, wx);
+    // neighbourhood: this query's grid coordinates and window starts
+    const NaQuery nq = na_query<MASK>(p, q);
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
     // P overwrites the first half of S, and each half of P is announced on
     // its own so that P V starts on the first.
-    for (int j = sg.kv0; j < sg.kv1; ++j) {
+    const Band band = task_band<MASK>(tk, p);
+    for (int j = mask_is_na(MASK) ? band_next(band, sg.kv0 - 1) : sg.kv0; j < sg.kv1;
+         j = mask_is_na(MASK) ? band_next(band, j) : j + 1) {
       const int cls = tile_class<MASK>(q0, j, p);
       if (cls == 0) continue;
       if (!warp_wait(bars.s_full(hh), s_par, ctl, j)) return;
@@ -1113,7 +1344,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld128(t_s, sr);
-      if (cls == 2) mask_tile<MASK>(sr, p, j, q, qy, qx, wy, wx);
+      if (cls == 2) mask_tile<MASK>(sr, p, j, q, nq);
       const float mx = row_max128(sr);
       float s[128];
 #pragma unroll
@@ -1304,6 +1535,7 @@ cudaError_t launch_dim(const KernelParams& p, int mask, int grid, cudaStream_t s
     case kMaskNa + 5: return launch_mask<D, kMaskNa + 5>(p, grid, s);
     case kMaskNa + 6: return launch_mask<D, kMaskNa + 6>(p, grid, s);
     case kMaskNa + 7: return launch_mask<D, kMaskNa + 7>(p, grid, s);
+    case kMaskNa3: return launch_mask<D, kMaskNa3>(p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -40,6 +40,15 @@
  *                    axis takes (c + dl * t) mod G. k * dl <= the grid side of
  *                    its axis, unless k = 1. A 1 x N grid with window 1 along
  *                    the rows is 1-D neighbourhood attention.
+ *   ATTN_MASK_NA3D   tokens are row-major on a grid_d x grid_h x grid_w
+ *                    volume (depth slowest; Nq = Nk = the product, the grid
+ *                    given explicitly); the key is allowed iff each of the
+ *                    three axes allows it by the rule above. `window_d` is the
+ *                    window along the depth (0 = `window`), `wrap_d` 1 wraps
+ *                    the depth; `window`, `window_w`, `wrap` and `dilation`
+ *                    as for NA2D (one dilation for all three axes). The
+ *                    NATTEN issue's requester works on such volumes and wraps
+ *                    some of their axes.
  *
  * Data layout (device memory, owned and allocated by the caller):
  *   q, o : bf16 [B, H, Nq, d]   k, v : bf16 [B, H, Nk, d]   (contiguous by
@@ -76,12 +85,13 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 typedef enum {
   ATTN_MASK_NONE = 0,
   ATTN_MASK_CAUSAL = 1,
-  ATTN_MASK_NA2D = 2
+  ATTN_MASK_NA2D = 2,
+  ATTN_MASK_NA3D = 3
 } attn_mask_kind;
 
 typedef enum {
@@ -109,12 +119,14 @@ typedef struct attn_params_ex {
   int B, H, Nq, Nk, d;
   float scale;     /* > 0 and finite, typically 1/sqrt(d) */
   int mask_kind;   /* attn_mask_kind */
-  int window;      /* NA2D: odd window size along the rows (and the columns
-                      unless window_w is set); others: must be 0 */
-  int dilation;    /* NA2D: key stride >= 1 along each axis; others: must be 1 */
-  int wrap;        /* NA2D: 0 = clamp, 1 = wrap both axes, 2 = wrap the rows,
-                      3 = wrap the columns; others: must be 0 */
-  int grid_h, grid_w; /* NA2D token grid; 0,0 = square grid of side sqrt(Nq) */
+  int window;      /* NA2D, NA3D: odd window size along the rows (and the
+                      columns / depth unless window_w / window_d is set);
+                      others: must be 0 */
+  int dilation;    /* NA2D, NA3D: key stride >= 1 along each axis; others: 1 */
+  int wrap;        /* NA2D, NA3D: 0 = rows and columns clamp, 1 = both wrap,
+                      2 = the rows wrap, 3 = the columns wrap; others: 0 */
+  int grid_h, grid_w; /* NA2D, NA3D rows and columns; NA2D 0,0 = square grid
+                         of side sqrt(Nq); NA3D: required */
   /* element strides of dims (b, h, n); all zero = contiguous [B,H,N,d] */
   int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
   void* stream;    /* cudaStream_t; NULL = the calling thread's stream */
@@ -133,8 +145,12 @@ typedef struct attn_params_ex {
                       before its first use (later calls leave it reusable);
                       NULL = the library's own */
   uint64_t workspace_bytes; /* size of `workspace` */
-  int window_w;    /* NA2D: odd window size along the columns; 0 = `window`;
+  int window_w;    /* NA2D, NA3D: odd window size along the columns; 0 =
+                      `window`; others: must be 0 */
+  int grid_d;      /* NA3D: depth of the volume (>= 1); others: must be 0 */
+  int window_d;    /* NA3D: odd window size along the depth; 0 = `window`;
                       others: must be 0 */
+  int wrap_d;      /* NA3D: 1 = the depth wraps, 0 = it clamps; others: 0 */
 } attn_params_ex;
 
 /* Fill *p with defaults (zero pointers and sizes, dilation 1, contiguous). */
@@ -219,7 +235,8 @@ typedef struct attn_bwd_params {
   int mask_kind;        /* attn_mask_kind */
   void* stream;         /* cudaStream_t; NULL = the calling thread's stream */
   uint64_t timeout_ns;  /* bound on every device-side wait; 0 = 2 seconds */
-  int window, window_w, dilation, wrap, grid_h, grid_w;  /* NA2D, as attn_params_ex */
+  int window, window_w, dilation, wrap, grid_h, grid_w;  /* NA2D/NA3D, as attn_params_ex */
+  int grid_d, window_d, wrap_d;                          /* NA3D, as attn_params_ex */
 } attn_bwd_params;
 
 /* Zero every field of *p, dilation 1. */

@@ -9,7 +9,8 @@ fp32 for Q, then K, then V (each [B, H, N, d]); each is multiplied by sigma and
 rounded to bf16 (round to nearest even). The shapes are those of the pages'
 workloads: the SD2.1 512x512 self-attention (seqlen 4096, d_head 64), its UNet
 block with cond/uncond batch and 5 heads, a causal LM shape, a 64x64-token 2-D
-neighbourhood-attention grid and a 16384-token long sequence.
+neighbourhood-attention grid, a 16384-token long sequence and a 16x16x16
+volume of 3-D neighbourhood attention with two wrapped axes.
 """
 from __future__ import annotations
 
@@ -34,17 +35,18 @@ class Workload:
     mask: str = "none"          # none | causal | clamp | wrap
     window: int = 0
     dilation: int = 1
-    grid: tuple = field(default=None)  # (grid_h, grid_w) for neighbourhood masks
+    grid: tuple = field(default=None)  # (grid_h, grid_w) or (depth, rows, cols)
     seed: int = 0
+    wrap_axes: tuple = field(default=None)  # one boolean per grid axis; None: as the mask says
 
     @property
     def heads(self) -> int:
         return self.B * self.H
 
 
-def _w(name, B, H, N, d, sigma, mask="none", window=0, grid=None, seed=0):
+def _w(name, B, H, N, d, sigma, mask="none", window=0, grid=None, seed=0, wrap_axes=None):
     return Workload(name, B, H, N, N, d, sigma, 1.0 / math.sqrt(d), mask, window, 1,
-                    grid, seed)
+                    grid, seed, wrap_axes)
 
 
 # The pages' workloads, in order (seed = 69000 + index).
@@ -57,6 +59,9 @@ WORKLOADS = {
     "na2d_wrap": _w("na2d_wrap", 1, 4, 4096, 32, 1.0, mask="wrap", window=7,
                     grid=(64, 64), seed=69003),
     "long_seq": _w("long_seq", 1, 8, 16384, 128, 1.0, seed=69004),
+    # the NATTEN issue requester's volumes: ~16 patches a side, window 5, 1-2 axes wrapped
+    "na3d_wrap2": _w("na3d_wrap2", 1, 4, 4096, 32, 1.0, mask="clamp", window=5,
+                     grid=(16, 16, 16), seed=69005, wrap_axes=(True, True, False)),
 }
 
 

@@ -1,6 +1,7 @@
 // Host build of the kernel's tile planning (which K/V tiles a Q tile visits,
 // and which of them need the in-tile mask), for CPU tests against the oracle.
 #include "attn_sm103.cuh"
+#include "attn_bwd_sm103.cuh"
 
 namespace {
 template <int MASK>
@@ -84,4 +85,98 @@ extern "C" void na_bits_host(int q, int k0, int N, int grid_h, int grid_w, int w
     default: break;
   }
   for (int i = 0; i < 4; ++i) out[i] = bits[i];
+}
+
+namespace {
+attn::KernelParams na3_params(int N, int grid_d, int grid_h, int grid_w, int window_d, int window_h,
+                              int window_w, int dilation, int wrap_bits) {
+  attn::KernelParams p = na_params(N, N, grid_h, grid_w, window_h, window_w, dilation);
+  p.grid_d = grid_d;
+  p.window_d = window_d;
+  p.na_wrap = wrap_bits;
+  return p;
+}
+
+int na2_mask(int wrap_rows, int wrap_cols, int dilation) {
+  return attn::na_mask(wrap_rows != 0, wrap_cols != 0, dilation > 1);
+}
+
+template <int MASK>
+void key_bits_of(const attn::KernelParams& p, int q0, int kk, uint32_t (&bits)[4]) {
+  attn::dev::na_key_bits<MASK>(p, q0, kk, bits);
+}
+}  // namespace
+
+// Volumes: wrap_bits 1 columns, 2 rows, 4 depth.
+extern "C" int tile_class3_host(int q0, int j, int N, int grid_d, int grid_h, int grid_w,
+                                int window_d, int window_h, int window_w, int dilation,
+                                int wrap_bits) {
+  const attn::KernelParams p =
+      na3_params(N, grid_d, grid_h, grid_w, window_d, window_h, window_w, dilation, wrap_bits);
+  return cls<attn::kMaskNa3>(q0, j, p);
+}
+
+extern "C" void na3_bits_host(int q, int k0, int N, int grid_d, int grid_h, int grid_w,
+                              int window_d, int window_h, int window_w, int dilation,
+                              int wrap_bits, unsigned* out) {
+  const attn::KernelParams p =
+      na3_params(N, grid_d, grid_h, grid_w, window_d, window_h, window_w, dilation, wrap_bits);
+  uint32_t bits[4];
+  attn::dev::na3_tile_bits(p, k0, attn::dev::na_query<attn::kMaskNa3>(p, q), bits);
+  for (int i = 0; i < 4; ++i) out[i] = bits[i];
+}
+
+// The backward's transposed mask: bit e set iff query q0 + e has key kk in its
+// window. grid_d == 0: a 2-D grid (wrap_bits 1 columns, 2 rows); else a volume.
+extern "C" void na_key_bits_host(int q0, int kk, int N, int grid_d, int grid_h, int grid_w,
+                                 int window_d, int window_h, int window_w, int dilation,
+                                 int wrap_bits, unsigned* out) {
+  const attn::KernelParams p =
+      na3_params(N, grid_d, grid_h, grid_w, window_d, window_h, window_w, dilation, wrap_bits);
+  uint32_t bits[4] = {0u, 0u, 0u, 0u};
+  if (grid_d > 0) {
+    key_bits_of<attn::kMaskNa3>(p, q0, kk, bits);
+  } else {
+    switch (na2_mask(wrap_bits & 2, wrap_bits & 1, dilation)) {
+      case attn::kMaskNa + 0: key_bits_of<attn::kMaskNa + 0>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 1: key_bits_of<attn::kMaskNa + 1>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 2: key_bits_of<attn::kMaskNa + 2>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 3: key_bits_of<attn::kMaskNa + 3>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 4: key_bits_of<attn::kMaskNa + 4>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 5: key_bits_of<attn::kMaskNa + 5>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 6: key_bits_of<attn::kMaskNa + 6>(p, q0, kk, bits); break;
+      case attn::kMaskNa + 7: key_bits_of<attn::kMaskNa + 7>(p, q0, kk, bits); break;
+      default: break;
+    }
+  }
+  for (int i = 0; i < 4; ++i) out[i] = bits[i];
+}
+
+// The band of candidate tiles for the 128-token tile starting at t0: out =
+// {lo0, hi0, lo1, hi1}. grid_d == 0: a 2-D grid (wrap_bits 1 columns, 2 rows).
+extern "C" void band_host(int t0, int N, int grid_d, int grid_h, int grid_w, int window_d,
+                          int window_h, int window_w, int dilation, int wrap_bits, int* out) {
+  const attn::KernelParams p =
+      na3_params(N, grid_d, grid_h, grid_w, window_d, window_h, window_w, dilation, wrap_bits);
+  const int t1 = (t0 + attn::kBM < N ? t0 + attn::kBM : N) - 1;
+  attn::dev::Band b{};
+  if (grid_d > 0) {
+    b = attn::dev::na_band<attn::kMaskNa3>(t0, t1, p);
+  } else {
+    switch (na2_mask(wrap_bits & 2, wrap_bits & 1, dilation)) {
+      case attn::kMaskNa + 0: b = attn::dev::na_band<attn::kMaskNa + 0>(t0, t1, p); break;
+      case attn::kMaskNa + 1: b = attn::dev::na_band<attn::kMaskNa + 1>(t0, t1, p); break;
+      case attn::kMaskNa + 2: b = attn::dev::na_band<attn::kMaskNa + 2>(t0, t1, p); break;
+      case attn::kMaskNa + 3: b = attn::dev::na_band<attn::kMaskNa + 3>(t0, t1, p); break;
+      case attn::kMaskNa + 4: b = attn::dev::na_band<attn::kMaskNa + 4>(t0, t1, p); break;
+      case attn::kMaskNa + 5: b = attn::dev::na_band<attn::kMaskNa + 5>(t0, t1, p); break;
+      case attn::kMaskNa + 6: b = attn::dev::na_band<attn::kMaskNa + 6>(t0, t1, p); break;
+      case attn::kMaskNa + 7: b = attn::dev::na_band<attn::kMaskNa + 7>(t0, t1, p); break;
+      default: break;
+    }
+  }
+  out[0] = b.lo0;
+  out[1] = b.hi0;
+  out[2] = b.lo1;
+  out[3] = b.hi1;
 }

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.attn_params_size() == ctypes.sizeof(_lib.AttnParamsEx)
-    assert lib.attn_abi_version() == 3
+    assert lib.attn_abi_version() == 4
 
 
 def test_error_strings(lib):
@@ -77,6 +77,20 @@ BAD = [
     ("neg_ctas", dict(num_ctas=-1), _lib.ATTN_ERR_INVALID_ARG),
     ("schedule3", dict(schedule=3), _lib.ATTN_ERR_INVALID_ARG),
     ("misaligned_ws", dict(workspace=(1 << 20) + 4), _lib.ATTN_ERR_MISALIGNED),
+    ("na3_no_grid", dict(mask_kind=3, window=3), _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_bad_volume", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=9), _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_wrap_d2", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=8, wrap_d=2),
+     _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_even_window_d", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=8, window_d=2),
+     _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_window_d_too_big", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=8, window_d=5),
+     _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_dilated_depth_too_big", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=8, dilation=2),
+     _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_q_ne_k", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=8, Nk=512),
+     _lib.ATTN_ERR_INVALID_ARG),
+    ("grid_d_without_na3", dict(mask_kind=2, window=3, grid_d=1), _lib.ATTN_ERR_INVALID_ARG),
+    ("wrap_d_without_na3", dict(wrap_d=1), _lib.ATTN_ERR_INVALID_ARG),
 ]
 
 
@@ -123,6 +137,10 @@ BWD_BAD = [
     ("na_bad_grid", dict(mask_kind=2, window=3, grid_h=10, grid_w=20), _lib.ATTN_ERR_INVALID_ARG),
     ("na_dilated_window_too_big", dict(mask_kind=2, window=3, dilation=6), _lib.ATTN_ERR_INVALID_ARG),
     ("na_wrap4", dict(mask_kind=2, window=3, wrap=4), _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_bad_volume", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=9), _lib.ATTN_ERR_INVALID_ARG),
+    ("na3_window_d_too_big", dict(mask_kind=3, window=3, grid_d=4, grid_h=8, grid_w=8, window_d=5),
+     _lib.ATTN_ERR_INVALID_ARG),
+    ("window_d_without_na3", dict(window_d=3), _lib.ATTN_ERR_INVALID_ARG),
 ]
 
 

@@ -126,6 +126,21 @@ def test_backward_neighbourhood_per_axis(E, grid, win, wrap_axes, dil):
             wrap_axes=wrap_axes)
 
 
+NA3_BWD = [((16, 16, 16), (5, 5, 5), (True, True, False), 1, 64),
+           ((8, 8, 8), (3, 3, 3), (True, True, True), 1, 32),
+           ((20, 15, 18), (5, 3, 7), (False, True, True), 1, 128),
+           ((6, 10, 30), (1, 3, 9), (False, False, True), 3, 64),
+           ((12, 1, 40), (3, 1, 5), (True, False, False), 1, 64),
+           ((8, 8, 8), (3, 3, 3), (False, False, False), 2, 64)]
+
+
+@pytest.mark.parametrize("grid,win,wrap_axes,dil,d", NA3_BWD)
+def test_backward_neighbourhood_3d(E, grid, win, wrap_axes, dil, d):
+    n = grid[0] * grid[1] * grid[2]
+    run_bwd(E, 1, 2, n, n, d, "clamp", seed=n + dil + d, window=win, dilation=dil, grid=grid,
+            wrap_axes=wrap_axes)
+
+
 def test_backward_neighbourhood_full_window_is_unmasked(E):
     """A window that covers the whole grid (clamp) allows every key: the gradients
     equal those of the unmasked problem computed by the same kernels."""

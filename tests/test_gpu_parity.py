@@ -134,6 +134,47 @@ def test_na2d_heads_last_per_axis_modes(E):
     assert (err <= ATOL + RTOL * np.abs(ref_o)).all(), float(err.max())
 
 
+# Volumes (NA3D): (grid (depth, rows, cols), window per axis, wrap per axis, dilation).
+# The first is the NATTEN issue requester's setting: ~16 patches a side, window 5,
+# two wrapped axes.
+NA3 = [((16, 16, 16), (5, 5, 5), (True, True, False), 1), ((8, 8, 8), (3, 3, 3), (True, True, True), 1),
+       ((20, 15, 18), (5, 3, 7), (False, True, True), 1), ((6, 10, 30), (1, 3, 9), (False, False, True), 3),
+       ((12, 1, 40), (3, 1, 5), (True, False, False), 1), ((9, 9, 9), (9, 9, 9), (True, False, True), 1),
+       ((4, 20, 3), (3, 7, 3), (False, True, False), 1), ((8, 8, 8), (3, 3, 3), (False, False, False), 2),
+       ((3, 5, 7), (3, 5, 7), (False, False, False), 1)]
+
+
+@pytest.mark.parametrize("grid,win,wrap_axes,dil", NA3)
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_neighbourhood_3d(E, grid, win, wrap_axes, dil, d):
+    n = grid[0] * grid[1] * grid[2]
+    run(E, 1, 2, n, n, d, "clamp", window=win, dilation=dil, grid=grid, wrap_axes=wrap_axes,
+        seed=n + d + dil)
+
+
+def test_neighbourhood_3d_mask_name_and_persistent(E):
+    run(E, 2, 1, 4096, 4096, 64, "wrap", window=5, grid=(16, 16, 16), seed=91)
+    run(E, 1, 3, 1000, 1000, 32, "clamp", window=(3, 5, 3), grid=(10, 10, 10), num_ctas=2, seed=92)
+
+
+def test_na3d_heads_last(E):
+    B, X, Y, Z, H, d = 1, 6, 8, 10, 2, 64
+    q, k, v = (torch.randn(B, X, Y, Z, H, d, generator=torch.Generator().manual_seed(s)).to(
+        torch.bfloat16) for s in (4, 5, 6))
+    o, lse = E.na3d(q.cuda(), k.cuda(), v.cuda(), (3, 5, 3), mode=("wrap", "clamp", "wrap"),
+                    return_lse=True)
+    _status_ok(E)
+    n = X * Y * Z
+    to_bhnd = lambda t: t.float().permute(0, 4, 1, 2, 3, 5).reshape(B, H, n, d)
+    ref_o, ref_lse = oracle.attention_rows(to_bhnd(q).numpy(), to_bhnd(k).numpy(),
+                                           to_bhnd(v).numpy(), None, scale=1 / math.sqrt(d),
+                                           mask_kind="clamp", window=(3, 5, 3),
+                                           wrap=(True, False, True), grid=(X, Y, Z))
+    assert o.shape == q.shape
+    o_bhnd = o.permute(0, 4, 1, 2, 3, 5).reshape(B, H, n, d)
+    check(o_bhnd, lse, ref_o, ref_lse)
+
+
 def test_neighbourhood_dilated_d128_and_persistent(E):
     run(E, 2, 1, 1024, 1024, 128, "wrap", window=5, dilation=3, grid=(32, 32), seed=77)
     run(E, 1, 3, 1024, 1024, 32, "clamp", window=5, dilation=2, grid=(32, 32), num_ctas=2,
@@ -185,11 +226,12 @@ def test_workloads_sampled_rows(E, name):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
     o, lse = E.attn_fwd(q.cuda(), k.cuda(), v.cuda(), scale=w.scale, mask=w.mask,
-                        window=w.window, grid=w.grid)
+                        window=w.window, grid=w.grid, wrap_axes=w.wrap_axes)
     _status_ok(E)
     rows = _sample_rows(w.B, w.H, w.Nq, w.seed)
     ref_o, ref_lse = oracle.attention_rows(to_f64(q), to_f64(k), to_f64(v), rows, scale=w.scale,
-                                           mask_kind=w.mask, window=w.window, grid=w.grid)
+                                           mask_kind=w.mask, window=w.window, grid=w.grid,
+                                           wrap=w.wrap_axes if w.wrap_axes is not None else False)
     check(o, lse, ref_o, ref_lse, rows)
 
 

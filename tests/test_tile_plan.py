@@ -36,6 +36,11 @@ def plan(tmp_path_factory):
     lib.tile_class_host.restype = ctypes.c_int
     lib.decode_task_host.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
     lib.na_bits_host.argtypes = [ctypes.c_int] * 10 + [ctypes.POINTER(ctypes.c_uint)]
+    lib.tile_class3_host.argtypes = [ctypes.c_int] * 11
+    lib.tile_class3_host.restype = ctypes.c_int
+    lib.na3_bits_host.argtypes = [ctypes.c_int] * 11 + [ctypes.POINTER(ctypes.c_uint)]
+    lib.na_key_bits_host.argtypes = [ctypes.c_int] * 11 + [ctypes.POINTER(ctypes.c_uint)]
+    lib.band_host.argtypes = [ctypes.c_int] * 10 + [ctypes.POINTER(ctypes.c_int)]
     return lib
 
 
@@ -150,3 +155,124 @@ def test_in_tile_mask_bits_match_oracle_mask(plan, mode, gh, gw, window, dilatio
             n = min(128, N - k0)
             ref[:n] = allowed[q, k0:k0 + n]
             assert np.array_equal(bits, ref), (q, k0)
+
+
+# volumes: (grid (depth, rows, cols), window per axis, wrap per axis, dilation)
+VOLUMES = [
+    ((16, 16, 16), (5, 5, 5), (True, True, False), 1), ((16, 16, 16), (5, 5, 5), (False, False, False), 1),
+    ((20, 15, 18), (5, 3, 7), (False, True, True), 1), ((8, 8, 8), (3, 3, 3), (True, True, True), 2),
+    ((6, 10, 30), (1, 3, 9), (False, False, True), 3), ((12, 1, 40), (3, 1, 5), (True, False, False), 1),
+    ((4, 20, 3), (3, 7, 3), (False, True, False), 1), ((9, 9, 9), (9, 9, 9), (True, False, True), 1),
+]
+
+
+def _wrap_bits(wrap):
+    return (1 if wrap[2] else 0) | (2 if wrap[1] else 0) | (4 if wrap[0] else 0)
+
+
+@pytest.mark.parametrize("grid,window,wrap,dilation", VOLUMES)
+def test_volume_tile_classes_and_bits_match_oracle_mask(plan, grid, window, wrap, dilation):
+    N = grid[0] * grid[1] * grid[2]
+    allowed = twin.mask_matrix(N, N, "clamp", window, dilation, grid, wrap)
+    args = (N,) + tuple(grid) + tuple(window) + (dilation, _wrap_bits(wrap))
+    n_kv = -(-N // 128)
+    visited = wasted = 0
+    for q0 in range(0, N, 128):
+        rows = allowed[q0:min(q0 + 128, N)]
+        for j in range(n_kv):
+            block = rows[:, j * 128:min(j * 128 + 128, N)]
+            c = plan.tile_class3_host(q0, j, *args)
+            assert c in (0, 2), (q0, j, c)
+            if c == 0:
+                assert not block.any(), (q0, j)
+            else:
+                visited += 1
+                wasted += not block.any()
+            if dilation == 1:
+                assert (c != 0) == bool(block.any()), (q0, j, c)
+    assert wasted <= visited // 2 + 1, (visited, wasted)
+    out = (ctypes.c_uint * 4)()
+    rng = np.random.default_rng(1)
+    queries = range(N) if N <= 1000 else rng.choice(N, 300, replace=False)
+    for q in queries:
+        for k0 in range(0, N, 128):
+            plan.na3_bits_host(int(q), k0, *args, out)
+            bits = np.array([(out[i >> 5] >> (i & 31)) & 1 for i in range(128)], dtype=bool)
+            ref = np.zeros(128, dtype=bool)
+            n = min(128, N - k0)
+            ref[:n] = allowed[q, k0:k0 + n]
+            assert np.array_equal(bits, ref), (q, k0)
+
+
+KEY_BITS = [((8, 8), (3, 3), (False, False), 1), ((8, 8), (3, 3), (True, True), 1),
+            ((13, 29), (5, 7), (False, True), 1), ((20, 12), (3, 5), (True, False), 2),
+            ((24, 50), (5, 5), (False, False), 4), ((1, 700), (1, 9), (False, True), 3),
+            ((6, 10, 12), (3, 5, 3), (True, False, True), 1), ((8, 8, 8), (3, 3, 3), (False, True, False), 2)]
+
+
+@pytest.mark.parametrize("grid,window,wrap,dilation", KEY_BITS)
+def test_backward_key_bits_match_transposed_oracle_mask(plan, grid, window, wrap, dilation):
+    """The dK/dV kernel's per-key mask (which queries of a 128-query tile hold
+    the key in their window) equals the oracle twin's column, bit for bit."""
+    N = int(np.prod(grid))
+    allowed = twin.mask_matrix(N, N, "clamp", window, dilation, grid, wrap)
+    if len(grid) == 3:
+        g3, w3, bits_w = grid, window, _wrap_bits(wrap)
+    else:
+        g3, w3 = (0,) + tuple(grid), (1,) + tuple(window)
+        bits_w = (1 if wrap[1] else 0) | (2 if wrap[0] else 0)
+    out = (ctypes.c_uint * 4)()
+    rng = np.random.default_rng(2)
+    keys = range(N) if N <= 800 else rng.choice(N, 250, replace=False)
+    for kk in keys:
+        for q0 in range(0, N, 128):
+            plan.na_key_bits_host(q0, int(kk), N, *g3, *w3, dilation, bits_w, out)
+            bits = np.array([(out[i >> 5] >> (i & 31)) & 1 for i in range(128)], dtype=bool)
+            ref = np.zeros(128, dtype=bool)
+            n = min(128, N - q0)
+            ref[:n] = allowed[q0:q0 + n, kk]
+            assert np.array_equal(bits, ref), (kk, q0)
+
+
+BANDS = [((64, 64), (7, 7), (False, False), 1), ((64, 64), (7, 7), (True, True), 1),
+         ((13, 29), (5, 7), (False, True), 1), ((20, 12), (3, 5), (True, False), 2),
+         ((24, 50), (5, 5), (False, False), 4), ((1, 700), (1, 9), (False, True), 3),
+         ((1, 4096), (1, 63), (False, False), 1), ((39, 39), (39, 39), (True, True), 1),
+         ((5, 5), (3, 3), (True, True), 1),
+         ((16, 16, 16), (5, 5, 5), (True, True, False), 1), ((6, 10, 30), (1, 3, 9), (False, False, True), 3),
+         ((12, 1, 40), (3, 1, 5), (True, False, False), 1), ((1, 20, 20), (1, 5, 5), (False, True, True), 1),
+         ((1, 1, 300), (1, 1, 7), (False, False, True), 2), ((9, 9, 9), (9, 9, 9), (True, False, True), 1)]
+
+
+def _band_tiles(out):
+    return set(range(out[0], out[1])) | set(range(out[2], out[3]))
+
+
+@pytest.mark.parametrize("grid,window,wrap,dilation", BANDS)
+def test_band_holds_every_meeting_tile_both_ways(plan, grid, window, wrap, dilation):
+    """The candidate band of a tile (the tiles the kernels visit) holds every tile
+    of the other side that shares an allowed pair with it: K/V tiles of a Q tile
+    (forward, dQ) and Q tiles of a K/V tile (dK/dV)."""
+    N = int(np.prod(grid))
+    allowed = twin.mask_matrix(N, N, "clamp", window, dilation, grid, wrap)
+    if len(grid) == 3:
+        g3, w3, bits_w = grid, window, _wrap_bits(wrap)
+    else:
+        g3, w3 = (0,) + tuple(grid), (1,) + tuple(window)
+        bits_w = (1 if wrap[1] else 0) | (2 if wrap[0] else 0)
+    n_t = -(-N // 128)
+    pad = np.zeros((n_t * 128, n_t * 128), dtype=bool)
+    pad[:N, :N] = allowed
+    meets = pad.reshape(n_t, 128, n_t, 128).any(axis=(1, 3))  # [q tile, k tile]
+    out = (ctypes.c_int * 4)()
+    total = 0
+    for t in range(n_t):
+        plan.band_host(t * 128, N, *g3, *w3, dilation, bits_w, out)
+        band = _band_tiles(out)
+        # the second interval may share a tile with the first; iteration skips it
+        assert out[0] < out[1] and (out[2] == out[3] or out[0] <= out[2]), list(out)
+        assert set(np.nonzero(meets[t])[0]) <= band, (t, list(out))
+        assert set(np.nonzero(meets[:, t])[0]) <= band, (t, list(out))
+        total += len(band)
+    # a band is a narrow superset: no more than the meeting tiles plus a margin
+    assert total <= meets.sum() + 4 * n_t, (total, int(meets.sum()))
