@@ -653,6 +653,54 @@ __host__ __device__ __forceinline__ int next_tile(const Task& tk, const Band& ba
   return end;
 }
 
+// Successive K/V tiles of a neighbourhood task inside its band, with the Q
+// tiles each one is active for. A whole warp searches 32 band positions at a
+// time (lane i runs the exact tile test on position base + i; ballots collect
+// the answers), so one warp pays one test per 32 tiles instead of one per
+// tile. `which` = 0 or 1: only that Q tile's tiles are wanted (the other's
+// tests are skipped); 2: both. Every lane of the warp must call next().
+template <int MASK>
+struct TileCursor {
+  Band b;
+  int len0, lo1s, len, base, pos, which;
+  uint32_t m0, m1;
+  __device__ __forceinline__ TileCursor(const Band& band, int w) : b(band), which(w) {
+    len0 = b.hi0 - b.lo0;
+    lo1s = max(b.lo1, b.hi0);  // the second interval may share a tile with the first
+    len = len0 + max(b.hi1 - lo1s, 0);
+    base = -32;
+    pos = -1;
+    m0 = m1 = 0u;
+  }
+  __device__ __forceinline__ int tile_at(int q) const {
+    return q < len0 ? b.lo0 + q : lo1s + (q - len0);
+  }
+  // The next active tile (`end` if none) and, in a, whether each Q tile needs it.
+  __device__ __forceinline__ int next(const Task& tk, int end, bool (&a)[2], const KernelParams& p) {
+    for (++pos; pos < len;) {
+      if (pos >= base + 32) {
+        base = pos & ~31;
+        const int q = base + static_cast<int>(threadIdx.x & 31);
+        const int t = q < len ? tile_at(q) : -1;
+        const bool x0 = t >= 0 && which != 1 && tile_active<MASK>(tk, 0, t, p);
+        const bool x1 = t >= 0 && which != 0 && tile_active<MASK>(tk, 1, t, p);
+        m0 = __ballot_sync(0xffffffffu, x0);
+        m1 = __ballot_sync(0xffffffffu, x1);
+      }
+      const uint32_t m = (m0 | m1) >> (pos - base);
+      if (m != 0u) {
+        pos += __ffs(static_cast<int>(m)) - 1;
+        a[0] = ((m0 >> (pos - base)) & 1u) != 0u;
+        a[1] = ((m1 >> (pos - base)) & 1u) != 0u;
+        const int t = tile_at(pos);
+        return t < end ? t : end;
+      }
+      pos = base + 32;
+    }
+    return end;
+  }
+};
+
 // ------------------------------------------------------------- work split
 
 // A segment: KV tiles [kv0, kv1) of task t; `head` marks the CTA's first one.
@@ -911,8 +959,12 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
     q_armed = static_cast<int>(q_it & 1u);
     ++q_it;
     int nth = 0;
-    for (int j = next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p); j < sg.kv1;
-         j = next_tile<MASK>(tk, band, j, sg.kv1, p), ++nth) {
+    constexpr bool kNa = mask_is_na(MASK);
+    TileCursor<MASK> cur(band, 2);
+    bool act[2];
+    for (int j = kNa ? cur.next(tk, sg.kv1, act, p) : next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
+         j < sg.kv1;
+         j = kNa ? cur.next(tk, sg.kv1, act, p) : next_tile<MASK>(tk, band, j, sg.kv1, p), ++nth) {
       const int ks = static_cast<int>(k_it % C::kKStages);
       if (!warp_wait(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
         goto drain;
@@ -1006,13 +1058,17 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
     ++q_it;
     tc_fence_after();
     bool o_ready[2] = {false, false};
-    int j = next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
+    // neighbourhood masks: the cursor's flags; others: the tile test itself
+    constexpr bool kNa = mask_is_na(MASK);
+    TileCursor<MASK> cur(band, 2);
+    bool aj[2] = {false, false}, an[2] = {false, false};
+    int j = kNa ? cur.next(tk, sg.kv1, aj, p) : next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
     if (j < sg.kv1) {
       const int ks = static_cast<int>(k_it % C::kKStages);
       if (!warp_wait(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
       for (int h = 0; h < 2; ++h)
-        if (tile_active<MASK>(tk, h, j, p)) {
+        if (kNa ? aj[h] : tile_active<MASK>(tk, h, j, p)) {
           issue_s<D>(tmem, h, sbase + C::kOffQ + h * C::kTileBytes,
                      sbase + C::kOffK + ks * C::kTileBytes);
           mma_commit(bars.s_full(h));
@@ -1021,7 +1077,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       ++k_it;
     }
     while (j < sg.kv1) {
-      const int jn = next_tile<MASK>(tk, band, j, sg.kv1, p);
+      const int jn = kNa ? cur.next(tk, sg.kv1, an, p) : next_tile<MASK>(tk, band, j, sg.kv1, p);
       const bool has_next = jn < sg.kv1;
       if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
       const int vs = static_cast<int>(v_it % C::kVStages);
@@ -1029,7 +1085,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       tc_fence_after();
       int ksn = -1;
       for (int h = 0; h < 2; ++h) {
-        if (tile_active<MASK>(tk, h, j, p)) {
+        if (kNa ? aj[h] : tile_active<MASK>(tk, h, j, p)) {
           if (!o_ready[h]) {
             if (!warp_wait(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, j, kRoleMma)) goto drain;
           }
@@ -1042,7 +1098,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
           p_par[h] ^= 1u;
           o_ready[h] = true;
         }
-        if (has_next && tile_active<MASK>(tk, h, jn, p)) {
+        if (has_next && (kNa ? an[h] : tile_active<MASK>(tk, h, jn, p))) {
           if (ksn < 0) {
             ksn = static_cast<int>(k_it % C::kKStages);
             if (!warp_wait(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, jn, kRoleMma))
@@ -1061,6 +1117,8 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
         ++k_it;
       }
       j = jn;
+      aj[0] = an[0];
+      aj[1] = an[1];
     }
     for (int h = 0; h < 2; ++h) {
       if (!tk.live[h]) continue;
@@ -1083,6 +1141,13 @@ drain:
 // reads after, a flag observed by another CTA (release / acquire, GPU scope).
 __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// A 64-bit load with acquire semantics at GPU scope.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
 // One arrival on a (task, Q tile) word tagged with this call's epoch; returns
 // the number of parts arrived so far in this call, or 0 if the CAS loop ran
 // past its bound (recorded as a timeout). The first attempt assumes this is
@@ -1103,9 +1168,12 @@ __device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t 
 }
 
 // Epilogue of a task cut between CTAs. Each warp handles its 32 rows on its
-// own: write this part (unnormalised O, the running maximum m in log2 units,
-// the row sum l), count the part on the rows' arrival word, and if it is the
-// last part of those rows, merge all parts:
+// own. It first reads the rows' arrival word: if every other part has
+// arrived already (the usual case for the part a CTA works on last), it
+// merges at once, without storing its own part. Otherwise it writes this part
+// (unnormalised O, the running maximum m in log2 units, the row sum l),
+// counts the part on the arrival word, and if that makes it the last part of
+// those rows, merges all parts:
 //   M = max_i m_i,  L = sum_i 2^(m_i - M) l_i,  O = sum_i 2^(m_i - M) O_i / L,
 //   LSE = ln 2 (M + log2 L).
 // No CTA waits for another: the last part to finish does the merge, reading
@@ -1131,41 +1199,53 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     __syncwarp();
     if (lane == 0) mbar_arrive(bars.o_empty(hh));
   };
-  float* mine = slot_of(blockIdx.x, sg.head);
-  float4* mine4 = reinterpret_cast<float4*>(mine);
-#pragma unroll
-  for (int ch = 0; ch < D / 32; ++ch) {
-    uint32_t ov[32];
-    tmem_ld32(t_o + ch * 32, ov);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      mine4[(ch * 8 + i) * 128 + row] =
-          make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
-                      __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
-  }
-  mine[128 * D + row] = m_ref;
-  mine[128 * D + 128 + row] = l;
-  fence_gpu();
-  __syncwarp();
   const int64_t t_first = static_cast<int64_t>(sg.t) * p.n_kv;
   const int c_lo = cta_of_unit(cta_lo, ctas, t_first);
   const int c_hi = cta_of_unit(cta_lo, ctas, t_first + p.n_kv - 1);
-  uint32_t n = 0;
-  if (lane == 0)
-    n = arrive_part(p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter, p.epoch, ctl);
-  n = __shfl_sync(0xffffffffu, n, 0);
-  if (n != static_cast<uint32_t>(c_hi - c_lo + 1)) {
-    release_o();
-    return !*ctl.abort;
+  const uint32_t n_parts = static_cast<uint32_t>(c_hi - c_lo + 1);
+  unsigned long long* word = p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter;
+  uint32_t seen = 0;
+  if (lane == 0) {
+    const unsigned long long v = ld_acquire_gpu(word);
+    seen = static_cast<uint32_t>(v >> 32) == p.epoch ? static_cast<uint32_t>(v) : 0u;
+  }
+  seen = __shfl_sync(0xffffffffu, seen, 0);
+  if (seen + 1u != n_parts) {
+    float* mine = slot_of(blockIdx.x, sg.head);
+    float4* mine4 = reinterpret_cast<float4*>(mine);
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t ov[32];
+      tmem_ld32(t_o + ch * 32, ov);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        mine4[(ch * 8 + i) * 128 + row] =
+            make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                        __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
+    }
+    mine[128 * D + row] = m_ref;
+    mine[128 * D + 128 + row] = l;
+    fence_gpu();
+    __syncwarp();
+    uint32_t n = 0;
+    if (lane == 0) n = arrive_part(word, p.epoch, ctl);
+    n = __shfl_sync(0xffffffffu, n, 0);
+    if (n != n_parts) {
+      release_o();
+      return !*ctl.abort;
+    }
   }
   fence_gpu();
   const int q = tk.q0[hh] + row;
   // a part of CTA c is that CTA's first segment iff its range starts in this task
   auto part = [&](int c) -> const float* { return slot_of(c, cta_lo[c] >= t_first); };
   const int me = blockIdx.x;
+  // Another part (every other part has been written by now) stands in for
+  // the unused slots of a round, so that all of its loads are in flight
+  // together and read this call's finite values; this CTA's own slot may hold
+  // a previous call's data.
+  const int stand_in = c_lo != me ? c_lo : c_hi;
   // M and L over all parts, online: m and l of up to 8 other parts per round.
-  // Every load reads a valid part (this CTA's stands in for the unused
-  // slots) so that all of a round's loads are in flight together.
   float M = m_ref;
   float L = l;
   for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
@@ -1173,7 +1253,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int c = c0 + u;
-      const float* sl = part(c <= c_hi ? c : me);
+      const float* sl = part(c <= c_hi && c != me ? c : stand_in);
       mi[u] = __ldcg(sl + 128 * D + row);
       li[u] = __ldcg(sl + 128 * D + 128 + row);
     }
@@ -1207,30 +1287,47 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
 #pragma unroll
       for (int i = 0; i < 32; ++i) acc[i] = w_me * __uint_as_float(ov[i]);
     }
-#pragma unroll 1
-    for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
-      float4 v[4][8];
-      float wgt[4];
+    if (c_hi - c_lo == 1) {  // two parts (the usual cut): load only the other one
+      const float* sl = part(stand_in);
+      const float mi = __ldcg(sl + 128 * D + row);
+      const float wgt = mi != -CUDART_INF_F ? ex2(mi - M) : 0.f;
+      const float4* src = reinterpret_cast<const float4*>(sl);
+      float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int c = c0 + u;
-        const bool in = c <= c_hi && c != me;
-        const float* sl = part(c <= c_hi ? c : me);
-        const float mi = __ldcg(sl + 128 * D + row);
-        wgt[u] = (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
-        const float4* src = reinterpret_cast<const float4*>(sl);
+      for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (ch * 8 + i) * 128 + row);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 128 + row);
+      for (int i = 0; i < 8; ++i) {
+        acc[4 * i] += wgt * v[i].x;
+        acc[4 * i + 1] += wgt * v[i].y;
+        acc[4 * i + 2] += wgt * v[i].z;
+        acc[4 * i + 3] += wgt * v[i].w;
       }
+    } else {
+#pragma unroll 1
+      for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
+        float4 v[4][8];
+        float wgt[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + u;
+          const bool in = c <= c_hi && c != me;
+          const float* sl = part(in ? c : stand_in);
+          const float mi = __ldcg(sl + 128 * D + row);
+          wgt[u] = (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
+          const float4* src = reinterpret_cast<const float4*>(sl);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          acc[4 * i] += wgt[u] * v[u][i].x;
-          acc[4 * i + 1] += wgt[u] * v[u][i].y;
-          acc[4 * i + 2] += wgt[u] * v[u][i].z;
-          acc[4 * i + 3] += wgt[u] * v[u][i].w;
+          for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 128 + row);
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            acc[4 * i] += wgt[u] * v[u][i].x;
+            acc[4 * i + 1] += wgt[u] * v[u][i].y;
+            acc[4 * i + 2] += wgt[u] * v[u][i].z;
+            acc[4 * i + 3] += wgt[u] * v[u][i].w;
+          }
+      }
     }
     if (row_ok) {
       uint32_t packed[16];
@@ -1334,10 +1431,13 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     bool first = true;
     // P overwrites the first half of S, and each half of P is announced on
     // its own so that P V starts on the first.
-    const Band band = task_band<MASK>(tk, p);
-    for (int j = mask_is_na(MASK) ? band_next(band, sg.kv0 - 1) : sg.kv0; j < sg.kv1;
-         j = mask_is_na(MASK) ? band_next(band, j) : j + 1) {
-      const int cls = tile_class<MASK>(q0, j, p);
+    // neighbourhood masks: the tiles the cursor finds for this Q tile (class 2)
+    constexpr bool kNa = mask_is_na(MASK);
+    TileCursor<MASK> cur(task_band<MASK>(tk, p), hh);
+    bool act[2];
+    for (int j = kNa ? cur.next(tk, sg.kv1, act, p) : sg.kv0; j < sg.kv1;
+         j = kNa ? cur.next(tk, sg.kv1, act, p) : j + 1) {
+      const int cls = kNa ? 2 : tile_class<MASK>(q0, j, p);
       if (cls == 0) continue;
       if (!warp_wait(bars.s_full(hh), s_par, ctl, j)) return;
       s_par ^= 1u;
