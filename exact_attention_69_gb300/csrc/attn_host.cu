@@ -54,7 +54,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
 
-constexpr int64_t kMinSplitUnits = 4;
+constexpr int64_t kMinSplitUnits = 8;
 
 // How a call's work is laid out over the persistent CTAs.
 struct Plan {

@@ -714,17 +714,6 @@ __host__ __device__ __forceinline__ int64_t unit_lo(int64_t units, int ctas, int
   return static_cast<int64_t>(c) * units / ctas;
 }
 
-// The CTA whose unit range holds unit u, given the table lo[c] = first unit of
-// CTA c (lo[ctas] = units): a binary search, no 64-bit division.
-__device__ __forceinline__ int cta_of_unit(const int64_t* lo, int ctas, int64_t u) {
-  int a = 0, b = ctas - 1;  // lo[a] <= u < lo[b + 1]
-  while (a < b) {
-    const int m = (a + b + 1) >> 1;
-    if (lo[m] <= u) a = m; else b = m - 1;
-  }
-  return a;
-}
-
 template <int MASK>
 struct SegIter {
   int64_t u, hi;
@@ -1186,7 +1175,7 @@ template <int D>
 __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars& bars, const Seg& sg,
                                               const Task& tk, int hh, int row, uint32_t t_o,
                                               float m_ref, float l, const int64_t* cta_lo,
-                                              const Ctl& ctl) {
+                                              uint32_t& o_par, const Ctl& ctl) {
   const int lane = threadIdx.x & 31;
   const int quarter = row >> 5;
   const int ctas = gridDim.x;
@@ -1200,17 +1189,84 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     if (lane == 0) mbar_arrive(bars.o_empty(hh));
   };
   const int64_t t_first = static_cast<int64_t>(sg.t) * p.n_kv;
-  const int c_lo = cta_of_unit(cta_lo, ctas, t_first);
-  const int c_hi = cta_of_unit(cta_lo, ctas, t_first + p.n_kv - 1);
+  const int me = blockIdx.x;
+  // The parts' CTAs are adjacent (CTA c covers units [cta_lo[c], cta_lo[c + 1]),
+  // and no range is empty): walk out from this CTA to the first and the last.
+  int c_lo = me, c_hi = me;
+  while (c_lo > 0 && cta_lo[c_lo] > t_first) --c_lo;
+  while (c_hi + 1 < ctas && cta_lo[c_hi + 1] < t_first + p.n_kv) ++c_hi;
   const uint32_t n_parts = static_cast<uint32_t>(c_hi - c_lo + 1);
+  // a part of CTA c is that CTA's first segment iff its range starts in this task
+  auto part = [&](int c) -> const float* { return slot_of(c, cta_lo[c] >= t_first); };
+  // Another part (every other part has been written by the time it is read)
+  // stands in for the unused slots of a merge round, so that all of its loads
+  // are in flight together and read this call's finite values; this CTA's
+  // own slot may hold a previous call's data.
+  const int stand_in = c_lo != me ? c_lo : c_hi;
   unsigned long long* word = p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter;
-  uint32_t seen = 0;
-  if (lane == 0) {
-    const unsigned long long v = ld_acquire_gpu(word);
-    seen = static_cast<uint32_t>(v >> 32) == p.epoch ? static_cast<uint32_t>(v) : 0u;
+  // Every lane reads the arrival word with acquire semantics (one broadcast
+  // load), before O is complete: the read overlaps the last P V.
+  const unsigned long long w0 = ld_acquire_gpu(word);
+  const uint32_t seen = static_cast<uint32_t>(w0 >> 32) == p.epoch ? static_cast<uint32_t>(w0) : 0u;
+  const bool claim = seen + 1u == n_parts;
+  const int q = tk.q0[hh] + row;
+  const bool row_ok = q < p.Nq;
+  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                        static_cast<int64_t>(q) * p.o_sn;
+  if (claim && n_parts == 2) {
+    // The usual cut: the other part is complete; fetch its m, l and its
+    // first 64 columns of O while the last P V finishes, then merge.
+    const float* sl = part(stand_in);
+    const float mi = __ldcg(sl + 128 * D + row);
+    const float li = __ldcg(sl + 128 * D + 128 + row);
+    constexpr int kPre = D < 64 ? D / 4 : 16;  // float4 columns fetched ahead
+    const float4* src = reinterpret_cast<const float4*>(sl);
+    float4 pre[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) pre[i] = __ldcg(src + i * 128 + row);
+    if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return false;
+    o_par ^= 1u;
+    tc_fence_after();
+    const float M = fmaxf(m_ref, mi);
+    const float w_me = m_ref == -CUDART_INF_F ? 0.f : ex2(m_ref - M);
+    const float w_ot = mi == -CUDART_INF_F ? 0.f : ex2(mi - M);
+    const float L = l * w_me + li * w_ot;
+    const float inv_L = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+      uint32_t ov[32];
+      tmem_ld32(t_o + ch * 32, ov);
+      float4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[i] = ch * 8 + i < kPre ? pre[(ch * 8 + i) % kPre] : __ldcg(src + (ch * 8 + i) * 128 + row);
+      if (row_ok) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          packed[2 * i] = pack_bf16((w_me * __uint_as_float(ov[4 * i]) + w_ot * v[i].x) * inv_L,
+                                    (w_me * __uint_as_float(ov[4 * i + 1]) + w_ot * v[i].y) * inv_L);
+          packed[2 * i + 1] =
+              pack_bf16((w_me * __uint_as_float(ov[4 * i + 2]) + w_ot * v[i].z) * inv_L,
+                        (w_me * __uint_as_float(ov[4 * i + 3]) + w_ot * v[i].w) * inv_L);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+    release_o();
+    if (row_ok && p.lse != nullptr) {
+      const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
+      p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
+    }
+    return !*ctl.abort;
   }
-  seen = __shfl_sync(0xffffffffu, seen, 0);
-  if (seen + 1u != n_parts) {
+  if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return false;
+  o_par ^= 1u;
+  tc_fence_after();
+  if (!claim) {
     float* mine = slot_of(blockIdx.x, sg.head);
     float4* mine4 = reinterpret_cast<float4*>(mine);
 #pragma unroll
@@ -1234,17 +1290,8 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
       release_o();
       return !*ctl.abort;
     }
+    fence_gpu();  // the other lanes' reads of the other parts come after lane 0's arrival
   }
-  fence_gpu();
-  const int q = tk.q0[hh] + row;
-  // a part of CTA c is that CTA's first segment iff its range starts in this task
-  auto part = [&](int c) -> const float* { return slot_of(c, cta_lo[c] >= t_first); };
-  const int me = blockIdx.x;
-  // Another part (every other part has been written by now) stands in for
-  // the unused slots of a round, so that all of its loads are in flight
-  // together and read this call's finite values; this CTA's own slot may hold
-  // a previous call's data.
-  const int stand_in = c_lo != me ? c_lo : c_hi;
   // M and L over all parts, online: m and l of up to 8 other parts per round.
   float M = m_ref;
   float L = l;
@@ -1274,9 +1321,6 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   }
   const float inv_L = L > 0.f ? 1.f / L : 0.f;
   const float w_me = (m_ref == -CUDART_INF_F) ? 0.f : ex2(m_ref - M);
-  const bool row_ok = q < p.Nq;
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
-                        static_cast<int64_t>(q) * p.o_sn;
   // O in chunks of 32 columns: this part's from TMEM, four other parts' rows per round.
 #pragma unroll 1
   for (int ch = 0; ch < D / 32; ++ch) {
@@ -1486,13 +1530,13 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
       first = false;
     }
     // epilogue: O / l, bf16 store, log-sum-exp
+    if (MASK == kMaskNone && p.split && (sg.kv0 > 0 || sg.kv1 < p.n_kv)) {
+      if (!partial_epilogue<D>(p, bars, sg, tk, hh, row, t_o, m_ref, l, cta_lo, o_par, ctl)) return;
+      continue;
+    }
     if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return;
     o_par ^= 1u;
     tc_fence_after();
-    if (MASK == kMaskNone && p.split && (sg.kv0 > 0 || sg.kv1 < p.n_kv)) {
-      if (!partial_epilogue<D>(p, bars, sg, tk, hh, row, t_o, m_ref, l, cta_lo, ctl)) return;
-      continue;
-    }
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
     const bool row_ok = q < p.Nq;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
