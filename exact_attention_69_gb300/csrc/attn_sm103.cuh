@@ -1230,7 +1230,10 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     const float M = fmaxf(m_ref, mi);
     const float w_me = m_ref == -CUDART_INF_F ? 0.f : ex2(m_ref - M);
     const float w_ot = mi == -CUDART_INF_F ? 0.f : ex2(mi - M);
-    const float L = l * w_me + li * w_ot;
+    // the lower CTA's part first, so that either part computes the same bits
+    const bool me_lo = me == c_lo;
+    const float w_lo = me_lo ? w_me : w_ot, w_hi = me_lo ? w_ot : w_me;
+    const float L = __fmaf_rn(me_lo ? li : l, w_hi, __fmul_rn(me_lo ? l : li, w_lo));
     const float inv_L = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
@@ -1241,14 +1244,16 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
       for (int i = 0; i < 8; ++i)
         v[i] = ch * 8 + i < kPre ? pre[(ch * 8 + i) % kPre] : __ldcg(src + (ch * 8 + i) * 128 + row);
       if (row_ok) {
+        auto mix = [&](float own, float oth) {
+          return __fmaf_rn(w_hi, me_lo ? oth : own, __fmul_rn(w_lo, me_lo ? own : oth)) * inv_L;
+        };
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          packed[2 * i] = pack_bf16((w_me * __uint_as_float(ov[4 * i]) + w_ot * v[i].x) * inv_L,
-                                    (w_me * __uint_as_float(ov[4 * i + 1]) + w_ot * v[i].y) * inv_L);
-          packed[2 * i + 1] =
-              pack_bf16((w_me * __uint_as_float(ov[4 * i + 2]) + w_ot * v[i].z) * inv_L,
-                        (w_me * __uint_as_float(ov[4 * i + 3]) + w_ot * v[i].w) * inv_L);
+          packed[2 * i] = pack_bf16(mix(__uint_as_float(ov[4 * i]), v[i].x),
+                                    mix(__uint_as_float(ov[4 * i + 1]), v[i].y));
+          packed[2 * i + 1] = pack_bf16(mix(__uint_as_float(ov[4 * i + 2]), v[i].z),
+                                        mix(__uint_as_float(ov[4 * i + 3]), v[i].w));
         }
         uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
@@ -1292,85 +1297,98 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     }
     fence_gpu();  // the other lanes' reads of the other parts come after lane 0's arrival
   }
-  // M and L over all parts, online: m and l of up to 8 other parts per round.
+  // The merge sums the parts in CTA order (this part at its own place), so
+  // the result has the same bits whichever part does it. M first: the
+  // largest m of all parts (exact in any order); then L.
   float M = m_ref;
-  float L = l;
-  for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
+  float L = 0.f;
+  if (c_hi - c_lo < 8) {  // every part in one round: m and l stay in registers
     float mi[8], li[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int c = c0 + u;
+      const int c = c_lo + u;
       const float* sl = part(c <= c_hi && c != me ? c : stand_in);
       mi[u] = __ldcg(sl + 128 * D + row);
       li[u] = __ldcg(sl + 128 * D + 128 + row);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int c = c0 + u;
-      if (c > c_hi || c == me) mi[u] = -CUDART_INF_F;
-    }
+    for (int u = 0; u < 8; ++u)
+      if (c_lo + u <= c_hi && c_lo + u != me) M = fmaxf(M, mi[u]);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      if (mi[u] == -CUDART_INF_F) continue;
-      if (mi[u] > M) {
-        L = (M == -CUDART_INF_F) ? 0.f : L * ex2(M - mi[u]);
-        M = mi[u];
+      const int c = c_lo + u;
+      const float mc = c == me ? m_ref : mi[u];
+      if (c <= c_hi && mc != -CUDART_INF_F) L = __fmaf_rn(c == me ? l : li[u], ex2(mc - M), L);
+    }
+  } else {  // more parts: the maximum first, then L
+    for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
+      float mi[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u;
+        mi[u] = __ldcg(part(c <= c_hi && c != me ? c : stand_in) + 128 * D + row);
       }
-      L += li[u] * ex2(mi[u] - M);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c0 + u <= c_hi && c0 + u != me) M = fmaxf(M, mi[u]);
+    }
+    for (int c0 = c_lo; c0 <= c_hi; c0 += 8) {
+      float mi[8], li[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u;
+        const float* sl = part(c <= c_hi && c != me ? c : stand_in);
+        mi[u] = __ldcg(sl + 128 * D + row);
+        li[u] = __ldcg(sl + 128 * D + 128 + row);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = c0 + u;
+        const float mc = c == me ? m_ref : mi[u];
+        if (c <= c_hi && mc != -CUDART_INF_F) L = __fmaf_rn(c == me ? l : li[u], ex2(mc - M), L);
+      }
     }
   }
   const float inv_L = L > 0.f ? 1.f / L : 0.f;
   const float w_me = (m_ref == -CUDART_INF_F) ? 0.f : ex2(m_ref - M);
-  // O in chunks of 32 columns: this part's from TMEM, four other parts' rows per round.
+  // O in chunks of 32 columns: this part's from TMEM, four parts' rows per round.
 #pragma unroll 1
   for (int ch = 0; ch < D / 32; ++ch) {
-    float acc[32];
+    float acc[32], own[32];
     {
       uint32_t ov[32];
       tmem_ld32(t_o + ch * 32, ov);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = w_me * __uint_as_float(ov[i]);
-    }
-    if (c_hi - c_lo == 1) {  // two parts (the usual cut): load only the other one
-      const float* sl = part(stand_in);
-      const float mi = __ldcg(sl + 128 * D + row);
-      const float wgt = mi != -CUDART_INF_F ? ex2(mi - M) : 0.f;
-      const float4* src = reinterpret_cast<const float4*>(sl);
-      float4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (ch * 8 + i) * 128 + row);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        acc[4 * i] += wgt * v[i].x;
-        acc[4 * i + 1] += wgt * v[i].y;
-        acc[4 * i + 2] += wgt * v[i].z;
-        acc[4 * i + 3] += wgt * v[i].w;
+      for (int i = 0; i < 32; ++i) {
+        own[i] = __uint_as_float(ov[i]);
+        acc[i] = 0.f;
       }
-    } else {
+    }
 #pragma unroll 1
-      for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
-        float4 v[4][8];
-        float wgt[4];
+    for (int c0 = c_lo; c0 <= c_hi; c0 += 4) {
+      float4 v[4][8];
+      float wgt[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c0 + u;
-          const bool in = c <= c_hi && c != me;
-          const float* sl = part(in ? c : stand_in);
-          const float mi = __ldcg(sl + 128 * D + row);
-          wgt[u] = (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
-          const float4* src = reinterpret_cast<const float4*>(sl);
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u;
+        const bool in = c <= c_hi && c != me;
+        const float* sl = part(in ? c : stand_in);
+        const float mi = __ldcg(sl + 128 * D + row);
+        wgt[u] = c == me ? w_me : (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
+        const float4* src = reinterpret_cast<const float4*>(sl);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 128 + row);
+        for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 128 + row);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const bool is_me = c0 + u == me;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          acc[4 * i] = __fmaf_rn(wgt[u], is_me ? own[4 * i] : v[u][i].x, acc[4 * i]);
+          acc[4 * i + 1] = __fmaf_rn(wgt[u], is_me ? own[4 * i + 1] : v[u][i].y, acc[4 * i + 1]);
+          acc[4 * i + 2] = __fmaf_rn(wgt[u], is_me ? own[4 * i + 2] : v[u][i].z, acc[4 * i + 2]);
+          acc[4 * i + 3] = __fmaf_rn(wgt[u], is_me ? own[4 * i + 3] : v[u][i].w, acc[4 * i + 3]);
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            acc[4 * i] += wgt[u] * v[u][i].x;
-            acc[4 * i + 1] += wgt[u] * v[u][i].y;
-            acc[4 * i + 2] += wgt[u] * v[u][i].z;
-            acc[4 * i + 3] += wgt[u] * v[u][i].w;
-          }
       }
     }
     if (row_ok) {

@@ -142,14 +142,15 @@ def test_backward_neighbourhood_3d(E, grid, win, wrap_axes, dil, d):
 
 
 def test_backward_neighbourhood_full_window_is_unmasked(E):
-    """A window that covers the whole grid (clamp) allows every key: the gradients
-    equal those of the unmasked problem computed by the same kernels."""
+    """A window that covers the whole grid (clamp) allows every key: from the same
+    O and LSE, the backward kernels give the unmasked gradients bit for bit. (The
+    two forwards are separate kernels that round P at different points, so each
+    is checked against the oracle elsewhere, not against the other.)"""
     q, k, v = (t.cuda() for t in make_qkv(1, 2, 15 * 15, 15 * 15, 64, 1.0, 21))
     g = torch.randn(1, 2, 225, 64, generator=torch.Generator().manual_seed(22)).to(torch.bfloat16).cuda()
-    o, lse = E.attn_fwd(q, k, v)
+    o, lse = E.attn_fwd(q, k, v, mask="clamp", window=15, grid=(15, 15))
     ref = E.attn_bwd(q, k, v, o, lse, g)
-    o2, lse2 = E.attn_fwd(q, k, v, mask="clamp", window=15, grid=(15, 15))
-    got = E.attn_bwd(q, k, v, o2, lse2, g, mask="clamp", window=15, grid=(15, 15))
+    got = E.attn_bwd(q, k, v, o, lse, g, mask="clamp", window=15, grid=(15, 15))
     for a, b in zip(got, ref):
         assert torch.equal(a, b)
 
