@@ -103,6 +103,17 @@ class AttnBwdParams(ctypes.Structure):
     ]
 
 
+class AttnTuneResult(ctypes.Structure):
+    """Mirror of ``attn_tune_result``."""
+
+    _fields_ = [
+        ("schedule", ctypes.c_int),
+        ("num_ctas", ctypes.c_int),
+        ("us", ctypes.c_float),
+        ("n_tried", ctypes.c_int),
+    ]
+
+
 class AttnError(RuntimeError):
     def __init__(self, code: int, message: str):
         super().__init__(message)

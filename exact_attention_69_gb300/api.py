@@ -16,6 +16,7 @@ the library's sm_103a kernel per call. Nothing here computes attention.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import torch
@@ -84,7 +85,7 @@ def _check_dev(*ts):
 
 def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, grid,
             layout, num_ctas, timeout_ns, inject, events, stream, schedule=0, workspace=None,
-            wrap_axes=None):
+            wrap_axes=None, tune_iters=0):
     p = _lib.params()
     p.q, p.k, p.v, p.o = q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr()
     p.lse = lse.data_ptr() if lse is not None else None
@@ -104,6 +105,11 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
         p.workspace = workspace.data_ptr()
         p.workspace_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(q.device):
+        if tune_iters > 0:
+            res = _lib.AttnTuneResult()
+            _lib.check(_lib.load().attn_tune(ctypes.byref(p), int(tune_iters), ctypes.byref(res)),
+                       "attn_tune")
+            return res
         # torch events bracket the single launch on the same stream (events
         # recorded inside the library would be invisible to torch)
         if events is not None:
@@ -111,6 +117,7 @@ def _launch(q, k, v, o, lse, *, B, H, Nq, Nk, d, scale, mask, window, dilation, 
         _lib.check(_lib.fwd_ex(p), "attn_fwd")
         if events is not None:
             events[1].record(stream)
+    return None
 
 
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
@@ -303,6 +310,27 @@ def na3d(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kernel_size, *,
             timeout_ns=0, inject=0, events=None, stream=stream,
             wrap_axes=tuple(m == "wrap" for m in modes))
     return (out, lse) if return_lse else out
+
+
+def tune(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float | None = None,
+         mask: str = "none", window=0, dilation: int = 1, grid=None, wrap_axes=None,
+         iters: int = 10, stream=None) -> dict:
+    """Time the forward's schedule candidates on these inputs and return the
+    fastest as {'schedule', 'num_ctas', 'us', 'n_tried'}; pass schedule and
+    num_ctas to later attn_fwd calls of the same shape. Synchronous."""
+    _check_dev(q, k, v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q, memory_format=torch.contiguous_format)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    res = _launch(q, k, v, out, lse, B=B, H=H, Nq=Nq, Nk=Nk, d=d, scale=scale, mask=mask,
+                  window=window, dilation=dilation, grid=grid, layout="bhnd", num_ctas=0,
+                  timeout_ns=0, inject=0, events=None, stream=stream, wrap_axes=wrap_axes,
+                  tune_iters=iters)
+    return {"schedule": res.schedule, "num_ctas": res.num_ctas, "us": float(res.us),
+            "n_tried": res.n_tried}
 
 
 def device_status():

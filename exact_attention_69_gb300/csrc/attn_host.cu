@@ -54,7 +54,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t{255}; }
 
-constexpr int64_t kMinSplitUnits = 8;
+constexpr int64_t kMinSplitUnits = 4;
 
 // How a call's work is laid out over the persistent CTAs.
 struct Plan {
@@ -482,6 +482,75 @@ int attn_device_sm_count(void) {
   int rc = device_state(&ds);
   if (rc != ATTN_OK) return -rc;
   return ds->sm_count;
+}
+
+int attn_tune(const attn_params_ex* p, int iters, attn_tune_result* out) {
+  t_err[0] = 0;
+  if (!p || !out) return fail(ATTN_ERR_INVALID_ARG, "params and result must be non-null");
+  if (iters < 1) return fail(ATTN_ERR_INVALID_ARG, "iters must be >= 1");
+  DeviceState* ds = nullptr;
+  int rc;
+  if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+  const int sm = ds->sm_count;
+  // candidates: (schedule, num_ctas)
+  int cand[16][2];
+  int nc = 0;
+  cand[nc][0] = 1;
+  cand[nc][1] = 0;
+  ++nc;
+  if (p->mask_kind == ATTN_MASK_NONE) {
+    const int fr[] = {8, 7, 6, 5, 4, 3, 2};  // G = sm * fr / 8
+    for (int f : fr) {
+      const int g = sm * f / 8;
+      if (g < 1 || g > attn::kMaxSplitCtas) continue;
+      bool dup = false;
+      for (int i = 0; i < nc; ++i) dup |= cand[i][0] == 2 && cand[i][1] == g;
+      if (dup) continue;
+      cand[nc][0] = 2;
+      cand[nc][1] = g;
+      ++nc;
+    }
+  }
+  cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  cudaError_t e;
+  if ((e = cudaEventCreate(&e0)) != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  if ((e = cudaEventCreate(&e1)) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return cuda_fail(e, "cudaEventCreate");
+  }
+  float best = 0.f;
+  int best_i = -1;
+  rc = ATTN_OK;
+  for (int i = 0; i < nc && rc == ATTN_OK; ++i) {
+    attn_params_ex c = *p;
+    c.schedule = cand[i][0];
+    c.num_ctas = cand[i][1];
+    c.ev_start = c.ev_stop = nullptr;
+    // two untimed launches (workspace growth, caches), then `iters` timed ones
+    for (int w = 0; w < 2 && rc == ATTN_OK; ++w) rc = attn_fwd_ex(&c);
+    if (rc != ATTN_OK) break;
+    if ((e = cudaEventRecord(e0, s)) != cudaSuccess) { rc = cuda_fail(e, "cudaEventRecord"); break; }
+    for (int it = 0; it < iters && rc == ATTN_OK; ++it) rc = attn_fwd_ex(&c);
+    if (rc != ATTN_OK) break;
+    if ((e = cudaEventRecord(e1, s)) != cudaSuccess) { rc = cuda_fail(e, "cudaEventRecord"); break; }
+    if ((e = cudaEventSynchronize(e1)) != cudaSuccess) { rc = cuda_fail(e, "cudaEventSynchronize"); break; }
+    float ms = 0.f;
+    if ((e = cudaEventElapsedTime(&ms, e0, e1)) != cudaSuccess) { rc = cuda_fail(e, "cudaEventElapsedTime"); break; }
+    const float us = 1000.f * ms / static_cast<float>(iters);
+    if (best_i < 0 || us < best) {
+      best = us;
+      best_i = i;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (rc != ATTN_OK) return rc;
+  out->schedule = cand[best_i][0];
+  out->num_ctas = cand[best_i][1];
+  out->us = best;
+  out->n_tried = nc;
+  return ATTN_OK;
 }
 
 void attn_shutdown(void) {

@@ -85,7 +85,7 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 typedef enum {
   ATTN_MASK_NONE = 0,
@@ -194,6 +194,25 @@ int attn_device_sm_count(void);
 /* Bytes of workspace the call described by *p needs on the current device (0
  * if its schedule splits no task), or a negative attn_status. */
 int64_t attn_workspace_bytes(const attn_params_ex* p);
+
+/* Schedule tuning: the split-KV schedule's work split, chosen per problem by
+ * measurement (the pages' kernels tune their tile configuration per problem;
+ * here the tiles are fixed per head dimension and the schedule is tuned).
+ * For the problem described by *p, times `iters` launches (>= 1) of each
+ * candidate: whole (batch, head, 256-query) tasks over every SM, and, without
+ * a mask, equal shares of K/V tiles over G CTAs for several G from the SM count
+ * down to a quarter of it. Uses p's buffers (o and lse are overwritten) and
+ * stream, and is synchronous. p->schedule and p->num_ctas are ignored; the
+ * fastest candidate goes to *out, to be set in the params of later calls.
+ * Returns an attn_status code. */
+typedef struct attn_tune_result {
+  int schedule;      /* 1 = whole tasks, 2 = equal K/V shares */
+  int num_ctas;      /* persistent CTAs (0 = one per SM) */
+  float us;          /* mean time per launch of that candidate */
+  int n_tried;       /* candidates timed */
+} attn_tune_result;
+
+int attn_tune(const attn_params_ex* p, int iters, attn_tune_result* out);
 
 /* Free the library's per-device state (status words). Later calls re-create it. */
 void attn_shutdown(void);

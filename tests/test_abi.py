@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.attn_params_size() == ctypes.sizeof(_lib.AttnParamsEx)
-    assert lib.attn_abi_version() == 4
+    assert lib.attn_abi_version() == 5
 
 
 def test_error_strings(lib):
@@ -156,3 +156,11 @@ def test_backward_rejects_bad_arguments_on_host(lib, name, changes, code):
 def test_backward_params_init_defaults(lib):
     p = _lib.bwd_params()
     assert p.dilation == 1 and p.window == 0 and p.wrap == 0 and p.mask_kind == 0
+
+
+def test_tune_rejects_bad_arguments_on_host(lib):
+    res = _lib.AttnTuneResult()
+    p = _base()
+    assert lib.attn_tune(ctypes.byref(p), 0, ctypes.byref(res)) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_tune(ctypes.byref(p), 5, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_tune(None, 5, ctypes.byref(res)) == _lib.ATTN_ERR_INVALID_ARG

@@ -392,3 +392,22 @@ def test_split_many_parts_bitwise_repeatable(E):
     ref_o, ref_lse = oracle.attention_rows(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()), rows,
                                            scale=0.125)
     check(first[0], first[1], ref_o, ref_lse, rows)
+
+
+@pytest.mark.parametrize("mask,shape", [("none", (1, 1, 4096, 64)), ("none", (2, 5, 4096, 64)),
+                                        ("causal", (2, 4, 1024, 128))])
+def test_tuned_schedule_is_valid_and_exact(E, mask, shape):
+    B, H, N, d = shape
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, N, d, 1.0, 41))
+    best = E.tune(q, k, v, mask=mask, iters=3)
+    _status_ok(E)
+    assert best["schedule"] in (1, 2) and best["us"] > 0 and best["n_tried"] >= 1
+    if mask != "none":
+        assert best["schedule"] == 1 and best["n_tried"] == 1
+    assert 0 <= best["num_ctas"] <= E.sm_count()
+    o, lse = E.attn_fwd(q, k, v, mask=mask, schedule=best["schedule"], num_ctas=best["num_ctas"])
+    _status_ok(E)
+    rows = np.arange(0, B * H * N, 97)
+    ref_o, ref_lse = oracle.attention_rows(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()), rows,
+                                           scale=1.0 / math.sqrt(d), mask_kind=mask)
+    check(o, lse, ref_o, ref_lse, rows)
