@@ -606,8 +606,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
   }
 }
 
+// The caller's stream and the second stream the dK/dV kernel runs on.
+struct BwdStreams {
+  cudaStream_t s, aux;
+  cudaEvent_t fork, join;
+};
+
 template <int D, int MASK>
-cudaError_t launch_bwd_mask(const BwdParams& bp, cudaStream_t s) {
+cudaError_t launch_bwd_mask(const BwdParams& bp, const BwdStreams& st) {
+  const cudaStream_t s = st.s;
   const KernelParams& p = bp.f;
   const int smem = BwdCfg<D>::kSmemBytes > 116 * 1024 ? BwdCfg<D>::kSmemBytes : 116 * 1024;
   auto kq = attn_bwd_dq_kernel<D, MASK>;
@@ -621,13 +628,20 @@ cudaError_t launch_bwd_mask(const BwdParams& bp, cudaStream_t s) {
       static_cast<const __nv_bfloat16*>(bp.o), static_cast<const __nv_bfloat16*>(bp.dout), bp.dd,
       rows, D);
   const int n_qt = (p.Nq + kBM - 1) / kBM;
+  // dQ and dK/dV need only D and the inputs: dK/dV on the second stream fills
+  // the SMs that the last wave of dQ CTAs leaves idle, and the reverse.
+  if ((e = cudaEventRecord(st.fork, s)) != cudaSuccess) return e;
+  if ((e = cudaStreamWaitEvent(st.aux, st.fork, 0)) != cudaSuccess) return e;
   kq<<<static_cast<unsigned>(p.B * p.H * n_qt), kBwdThreads, smem, s>>>(bp);
-  kkv<<<static_cast<unsigned>(p.B * p.H * p.n_kv), kBwdThreads, smem, s>>>(bp);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kkv<<<static_cast<unsigned>(p.B * p.H * p.n_kv), kBwdThreads, smem, st.aux>>>(bp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaEventRecord(st.join, st.aux)) != cudaSuccess) return e;
+  return cudaStreamWaitEvent(s, st.join, 0);
 }
 
 template <int D>
-cudaError_t launch_bwd_dim(const BwdParams& bp, int mask, cudaStream_t s) {
+cudaError_t launch_bwd_dim(const BwdParams& bp, int mask, const BwdStreams& s) {
   switch (mask) {
     case kMaskNone: return launch_bwd_mask<D, kMaskNone>(bp, s);
     case kMaskCausal: return launch_bwd_mask<D, kMaskCausal>(bp, s);

@@ -34,6 +34,8 @@ struct DeviceState {
   uint32_t epoch = 0;          // tag of the last split call
   float* dd = nullptr;         // backward scratch: rowsum(dO * O), grown when too small
   size_t dd_bytes = 0;
+  cudaStream_t aux = nullptr;  // backward: second stream (dK/dV beside dQ) and its events
+  cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 std::mutex g_mu;
@@ -563,6 +565,9 @@ void attn_shutdown(void) {
         cudaFree(g_dev[i].status);
         if (g_dev[i].ws) cudaFree(g_dev[i].ws);
         if (g_dev[i].dd) cudaFree(g_dev[i].dd);
+        if (g_dev[i].aux) cudaStreamDestroy(g_dev[i].aux);
+        if (g_dev[i].fork) cudaEventDestroy(g_dev[i].fork);
+        if (g_dev[i].join) cudaEventDestroy(g_dev[i].join);
       }
       cudaSetDevice(prev);
       g_dev[i].status = nullptr;
@@ -570,6 +575,8 @@ void attn_shutdown(void) {
       g_dev[i].ws_bytes = 0;
       g_dev[i].dd = nullptr;
       g_dev[i].dd_bytes = 0;
+      g_dev[i].aux = nullptr;
+      g_dev[i].fork = g_dev[i].join = nullptr;
     }
   }
 }
@@ -653,6 +660,14 @@ int attn_bwd(const attn_bwd_params* p) {
       ds->dd = static_cast<float*>(ptr);
       ds->dd_bytes = need;
     }
+    if (!ds->aux) {
+      cudaError_t e;
+      if ((e = cudaStreamCreateWithFlags(&ds->aux, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e, "cudaStreamCreateWithFlags");
+      if ((e = cudaEventCreateWithFlags(&ds->fork, cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&ds->join, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e, "cudaEventCreateWithFlags");
+    }
   }
   attn::BwdParams bp;
   std::memset(&bp, 0, sizeof(bp));
@@ -684,7 +699,7 @@ int attn_bwd(const attn_bwd_params* p) {
   bp.dv = p->dv;
   bp.scale = p->scale;
   cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
-  const cudaError_t e = attn::launch_bwd(bp, p->d, mask, s);
+  const cudaError_t e = attn::launch_bwd(bp, p->d, mask, s, ds->aux, ds->fork, ds->join);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ATTN_OK;
 }

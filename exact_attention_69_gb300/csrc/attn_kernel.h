@@ -101,7 +101,10 @@ struct BwdParams {
 cudaError_t launch_d32(const KernelParams& p, int mask, int grid, cudaStream_t s);
 cudaError_t launch_d64(const KernelParams& p, int mask, int grid, cudaStream_t s);
 // Backward launchers (D = rowsum(dO * O), dQ, then dK and dV), in attn_bwd.cu.
-cudaError_t launch_bwd(const BwdParams& p, int d, int mask, cudaStream_t s);
+// The dQ and the dK/dV kernels are independent: dK/dV runs on `aux`, forked
+// from s after D and joined back into s.
+cudaError_t launch_bwd(const BwdParams& p, int d, int mask, cudaStream_t s, cudaStream_t aux,
+                       cudaEvent_t fork, cudaEvent_t join);
 cudaError_t launch_d128(const KernelParams& p, int mask, int grid, cudaStream_t s);
 
 }  // namespace attn
