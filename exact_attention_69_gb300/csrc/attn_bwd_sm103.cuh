@@ -347,14 +347,84 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
 // Neighbourhood masks seen from a key: bit e set iff query q0 + e (< Nq) has
 // key (ky, kx) in its window. Clamped windows are not symmetric at the grid's
 // borders, so each query's window is placed and tested.
+// Query coordinates c on an axis of length G whose window (w wide, dilation
+// 1) holds key coordinate k: [lo, lo + len), circular when the axis wraps.
+// Clamp: the window start clamp(c - w/2, 0, G - w) never decreases with c, so
+// the c with start <= k <= start + w - 1 form one interval: [k - w/2, k + w/2]
+// widened to the border where the start is pinned there. Wrap: [k - w/2, k + w/2].
+template <bool WRAP>
+__host__ __device__ __forceinline__ void na_axis_queries(int k, int G, int w, int& lo, int& len) {
+  const int h = w >> 1;
+  if (WRAP) {
+    lo = k - h < 0 ? k - h + G : k - h;
+    len = w;
+    return;
+  }
+  const int c_max = k >= G - w ? G - 1 : k + h;
+  const int c_min = k - w + 1 <= 0 ? 0 : k - h;
+  lo = c_min;
+  len = c_max - c_min + 1;
+}
+
 template <int MASK>
 __host__ __device__ __forceinline__ void na_key_bits(const KernelParams& p, int q0, int kk,
                                             uint32_t (&bits)[4]) {
   bits[0] = bits[1] = bits[2] = bits[3] = 0u;
   const int n = min(kBM, p.Nq - q0);
-  if constexpr (MASK == kMaskNa3) {
+  if constexpr (mask_is_na2(MASK) && !mask_na_dilated(MASK)) {
+    // dilation 1: the queries that see the key form a row interval and a
+    // column interval; set the columns line by line as the forward does
+    constexpr bool WH = mask_na_wrap_rows(MASK), WW = mask_na_wrap_cols(MASK);
+    const int W = p.grid_w;
+    const int ky = kk / W, kx = kk - ky * W;
+    int ylo, ylen, xlo, xlen;
+    na_axis_queries<WH>(ky, p.grid_h, p.window_h, ylo, ylen);
+    na_axis_queries<WW>(kx, W, p.window_w, xlo, xlen);
+    int qy = q0 / W;
+    int qx0 = q0 - qy * W;
+    for (int i = 0; i < n; ++qy) {
+      const int len = min(W - qx0, n - i);  // this line's columns [qx0, qx0 + len)
+      int dy = qy - ylo;
+      if (WH && dy < 0) dy += p.grid_h;
+      if (dy >= 0 && dy < ylen) na_line_cols<WW, false>(bits, i - qx0, qx0, len, xlo, W, xlen, 1);
+      i += len;
+      qx0 = 0;
+    }
+  } else if constexpr (MASK == kMaskNa3) {
     const bool wd = (p.na_wrap & kNa3WrapDepth) != 0, wh = (p.na_wrap & kNa3WrapRows) != 0,
                ww = (p.na_wrap & kNa3WrapCols) != 0;
+    if (p.dilation == 1) {
+      // as for 2-D: an interval of query coordinates per axis, then lines
+      const int W = p.grid_w, Gh = p.grid_h, plane = Gh * W;
+      const int kt = kk / plane, ky = (kk - kt * plane) / W, kx = kk - kt * plane - ky * W;
+      int tlo, tlen, ylo, ylen, xlo, xlen;
+      if (wd) na_axis_queries<true>(kt, p.grid_d, p.window_d, tlo, tlen);
+      else na_axis_queries<false>(kt, p.grid_d, p.window_d, tlo, tlen);
+      if (wh) na_axis_queries<true>(ky, Gh, p.window_h, ylo, ylen);
+      else na_axis_queries<false>(ky, Gh, p.window_h, ylo, ylen);
+      if (ww) na_axis_queries<true>(kx, W, p.window_w, xlo, xlen);
+      else na_axis_queries<false>(kx, W, p.window_w, xlo, xlen);
+      const int r0 = q0 / W;
+      int qt = r0 / Gh, qy = r0 - qt * Gh;
+      int qx0 = q0 - r0 * W;
+      for (int i = 0; i < n;) {
+        const int len = min(W - qx0, n - i);
+        int dt = qt - tlo, dy = qy - ylo;
+        if (wd && dt < 0) dt += p.grid_d;
+        if (wh && dy < 0) dy += Gh;
+        if (dt >= 0 && dt < tlen && dy >= 0 && dy < ylen) {
+          if (ww) na_line_cols<true, false>(bits, i - qx0, qx0, len, xlo, W, xlen, 1);
+          else na_line_cols<false, false>(bits, i - qx0, qx0, len, xlo, W, xlen, 1);
+        }
+        i += len;
+        qx0 = 0;
+        if (++qy == Gh) {
+          qy = 0;
+          ++qt;
+        }
+      }
+      return;
+    }
     const int plane = p.grid_h * p.grid_w, dl = p.dilation;
     const int kt = kk / plane, ky = (kk - kt * plane) / p.grid_w, kx = kk - kt * plane - ky * p.grid_w;
     int qt = q0 / plane;

@@ -207,7 +207,13 @@ def test_volume_tile_classes_and_bits_match_oracle_mask(plan, grid, window, wrap
 KEY_BITS = [((8, 8), (3, 3), (False, False), 1), ((8, 8), (3, 3), (True, True), 1),
             ((13, 29), (5, 7), (False, True), 1), ((20, 12), (3, 5), (True, False), 2),
             ((24, 50), (5, 5), (False, False), 4), ((1, 700), (1, 9), (False, True), 3),
-            ((6, 10, 12), (3, 5, 3), (True, False, True), 1), ((8, 8, 8), (3, 3, 3), (False, True, False), 2)]
+            ((6, 10, 12), (3, 5, 3), (True, False, True), 1), ((8, 8, 8), (3, 3, 3), (False, True, False), 2),
+            ((64, 64), (7, 7), (False, False), 1), ((64, 64), (7, 7), (True, True), 1),
+            ((20, 12), (5, 3), (True, False), 1), ((1, 700), (1, 9), (False, False), 1),
+            ((39, 39), (39, 39), (True, True), 1), ((5, 5), (5, 5), (False, False), 1),
+            ((7, 30), (7, 1), (False, True), 1), ((30, 7), (1, 7), (True, False), 1),
+            ((16, 16, 16), (5, 5, 5), (True, True, False), 1), ((5, 9, 7), (5, 3, 7), (False, True, True), 1),
+            ((12, 1, 40), (3, 1, 5), (True, False, False), 1), ((3, 5, 7), (3, 5, 7), (False, False, False), 1)]
 
 
 @pytest.mark.parametrize("grid,window,wrap,dilation", KEY_BITS)
