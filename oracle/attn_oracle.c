@@ -29,6 +29,9 @@
  * Allowed sets A(i) (mask_kind):
  *   0 NONE   : every key j < Nk.
  *   1 CAUSAL : j <= i (top-left alignment, as is_causal=True).
+ *   4 CAUSAL_BR : j <= i + (Nk - Nq) (bottom-right alignment: the last query
+ *              sees every key, as when the queries are the newest Nq of Nk
+ *              tokens). With Nq > Nk the first Nq - Nk rows see no key.
  *   2 NA2D   : tokens are laid out row-major on a grid_h x grid_w grid;
  *              query (qy, qx), key (ky, kx); the key is allowed iff both axes
  *              are allowed by the one-axis rule below, each axis with its own
@@ -62,6 +65,7 @@
 #define ORACLE_MASK_CAUSAL 1
 #define ORACLE_MASK_NA2D 2
 #define ORACLE_MASK_NA3D 3
+#define ORACLE_MASK_CAUSAL_BR 4
 
 typedef struct {
   int Nq, Nk, d;
@@ -107,6 +111,8 @@ static int allowed(const problem_t* p, int i, int j) {
       return 1;
     case ORACLE_MASK_CAUSAL:
       return j <= i;
+    case ORACLE_MASK_CAUSAL_BR:
+      return (int64_t)j <= (int64_t)i + (p->Nk - p->Nq);
     case ORACLE_MASK_NA2D: {
       int qy = i / p->grid_w, qx = i % p->grid_w;
       int ky = j / p->grid_w, kx = j % p->grid_w;
@@ -132,7 +138,7 @@ static int allowed(const problem_t* p, int i, int j) {
 /* Returns 0 on success, -1 on bad arguments, -2 on allocation failure. */
 static int check_args(const problem_t* p, int B, int H) {
   if (B < 1 || H < 1 || p->Nq < 1 || p->Nk < 1 || p->d < 1) return -1;
-  if (p->mask_kind < 0 || p->mask_kind > 3) return -1;
+  if (p->mask_kind < 0 || p->mask_kind > 4) return -1;
   if (p->mask_kind == ORACLE_MASK_NA3D) {
     if (p->grid_d < 1 || p->window_d < 1 || p->window_d % 2 == 0) return -1;
     if (p->window_d > 1 && (int64_t)p->window_d * p->dilation > p->grid_d) return -1;

@@ -17,7 +17,9 @@ MASK_NONE = 0
 MASK_CAUSAL = 1
 MASK_NA2D = 2
 MASK_NA3D = 3
-MASK_CODES = {"none": MASK_NONE, "causal": MASK_CAUSAL, "clamp": MASK_NA2D, "wrap": MASK_NA2D}
+MASK_CAUSAL_BR = 4
+MASK_CODES = {"none": MASK_NONE, "causal": MASK_CAUSAL, "clamp": MASK_NA2D, "wrap": MASK_NA2D,
+              "causal_br": MASK_CAUSAL_BR}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "attn_oracle.c")
@@ -53,7 +55,7 @@ def _mask_args(mask_kind, window, wrap, grid, Nq):
     """The C oracle's mask arguments (mask code, window_h, window_w, wrap_h, wrap_w,
     grid_h, grid_w, window_d, wrap_d, grid_d).
 
-    mask_kind: a code, or "none" | "causal" | "clamp" | "wrap"; a neighbourhood mask
+    mask_kind: a code, or "none" | "causal" | "causal_br" | "clamp" | "wrap"; a neighbourhood mask
     on a 3-entry grid (depth, rows, columns) is NA3D, else NA2D. window: k for every
     axis, or one odd size per grid axis. wrap: a bool for every axis, or one per grid
     axis; the mask name "wrap" wraps every axis unless wrap says otherwise. NA2D

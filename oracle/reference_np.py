@@ -37,7 +37,7 @@ def _window_coords_wrap(c: int, G: int, k: int, dil: int) -> set:
 
 def mask_matrix(Nq: int, Nk: int, mask: str, window=0, dilation: int = 1,
                 grid=None, wrap_axes=None) -> np.ndarray:
-    """Boolean [Nq, Nk] allowed-set matrix. mask: none | causal | clamp | wrap.
+    """Boolean [Nq, Nk] allowed-set matrix. mask: none | causal | causal_br | clamp | wrap.
 
     grid: (rows, cols), or (depth, rows, cols) for a volume, tokens row-major with
     the first axis slowest; window: k for every axis, or one size per axis;
@@ -46,10 +46,12 @@ def mask_matrix(Nq: int, Nk: int, mask: str, window=0, dilation: int = 1,
     """
     if mask == "none":
         return np.ones((Nq, Nk), dtype=bool)
-    if mask == "causal":
+    if mask in ("causal", "causal_br"):
+        # top-left: query i sees keys 0..i; bottom-right: keys 0..i + (Nk - Nq)
+        shift = 0 if mask == "causal" else Nk - Nq
         m = np.zeros((Nq, Nk), dtype=bool)
         for i in range(Nq):
-            m[i, : min(i + 1, Nk)] = True
+            m[i, : max(0, min(i + 1 + shift, Nk))] = True
         return m
     grid = tuple(int(g) for g in grid)
     nax = len(grid)

@@ -25,6 +25,9 @@ What pins what:
   na3d_flat_is_na2d       a volume one slice deep with window 1 along depth == NA2D
   na3d_wrap_pad_clamp     issue #142's recipe in 3-D: circular pad of the wrapped axes,
                           clamped NA3D, crop == NA3D wrapping those axes
+  causal_bottom_right     bottom-right causal: == top-left when Nq == Nk; row i == unmasked
+                          attention over the first i + (Nk - Nq) + 1 keys; rows that see
+                          no key give O = 0, LSE = -inf; torch SDPA with tril(Nk - Nq)
   bwd_autograd_fp64       backward: torch autograd through an explicit fp64 forward
   bwd_finite_differences  backward: central differences of sum(dO * O) along random directions
   bwd_invariants          backward: a common shift of all keys leaves O unchanged (sum_j dK_j
@@ -113,6 +116,7 @@ CASES = [
     dict(mask_kind="clamp", Nq=54, Nk=54, window=(5, 3), grid=(6, 9), wrap=(True, False)),
     dict(mask_kind="clamp", Nq=54, Nk=54, window=(3, 3), grid=(6, 9), wrap=(False, True), dilation=2),
     dict(mask_kind="clamp", Nq=15, Nk=15, window=(1, 5), grid=(1, 15)),
+    dict(mask_kind="causal_br", Nq=23, Nk=41),
     dict(mask_kind="clamp", Nq=60, Nk=60, window=3, grid=(3, 4, 5)),
     dict(mask_kind="wrap", Nq=64, Nk=64, window=3, grid=(4, 4, 4)),
     dict(mask_kind="clamp", Nq=90, Nk=90, window=(3, 5, 3), grid=(3, 6, 5), wrap=(True, False, True)),
@@ -158,8 +162,9 @@ def zero_qk_means(orc):
         if m == "none":
             exp_o = np.broadcast_to(v[0, 0].mean(axis=0), (Nq, d))
             exp_n = np.full(Nq, Nk)
-        elif m == "causal":
-            cnt = np.minimum(np.arange(Nq) + 1, Nk)
+        elif m in ("causal", "causal_br"):
+            shift = 0 if m == "causal" else Nk - Nq
+            cnt = np.minimum(np.arange(Nq) + 1 + shift, Nk)
             csum = np.cumsum(v[0, 0], axis=0)
             exp_o = csum[cnt - 1] / cnt[:, None]
             exp_n = cnt
@@ -482,10 +487,55 @@ def na3d_wrap_pad_clamp(orc):
         assert np.max(np.abs(lc - lw)) < 1e-12, (g, win, wrap, dl)
 
 
+
+def causal_bottom_right(orc):
+    rng = np.random.default_rng(29)
+    d = 6
+    # Nq == Nk: the same allowed sets as top-left
+    q, k, v = (_rand(1, 2, 19, d, rng=rng) for _ in range(3))
+    o1, l1 = orc.attention(q, k, v, scale=0.6, mask_kind="causal")
+    o2, l2 = orc.attention(q, k, v, scale=0.6, mask_kind="causal_br")
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # Nq < Nk: row i is unmasked attention of query i over keys 0 .. i + Nk - Nq
+    Nq, Nk = 9, 25
+    q = _rand(1, 1, Nq, d, rng=rng)
+    k, v = (_rand(1, 1, Nk, d, rng=rng) for _ in range(2))
+    o, lse = orc.attention(q, k, v, scale=0.7, mask_kind="causal_br")
+    for i in range(Nq):
+        n = i + Nk - Nq + 1
+        on, ln = orc.attention(q[:, :, i:i + 1], k[:, :, :n], v[:, :, :n], scale=0.7, mask_kind="none")
+        assert np.max(np.abs(on[0, 0, 0] - o[0, 0, i])) < 1e-12 and abs(ln[0, 0, 0] - lse[0, 0, i]) < 1e-12
+    # Nq > Nk: the first Nq - Nk rows see no key; the others see keys 0 .. i - (Nq - Nk)
+    Nq, Nk = 20, 7
+    q = _rand(1, 1, Nq, d, rng=rng)
+    k, v = (_rand(1, 1, Nk, d, rng=rng) for _ in range(2))
+    o, lse = orc.attention(q, k, v, scale=0.7, mask_kind="causal_br")
+    for i in range(Nq):
+        n = i - (Nq - Nk) + 1
+        if n <= 0:
+            assert np.all(o[0, 0, i] == 0.0) and lse[0, 0, i] == -np.inf, i
+        else:
+            on, ln = orc.attention(q[:, :, i:i + 1], k[:, :, :n], v[:, :, :n], scale=0.7,
+                                   mask_kind="none")
+            assert np.max(np.abs(on[0, 0, 0] - o[0, 0, i])) < 1e-12, i
+    # torch SDPA (fp64, math) with the explicit bottom-right mask, Nq < Nk
+    import torch
+    import torch.nn.functional as F
+    Nq, Nk = 13, 30
+    q = _rand(2, 2, Nq, 8, rng=rng)
+    k, v = (_rand(2, 2, Nk, 8, rng=rng) for _ in range(2))
+    o, _ = orc.attention(q, k, v, scale=0.35, mask_kind="causal_br")
+    am = torch.ones(Nq, Nk, dtype=torch.bool).tril(diagonal=Nk - Nq)
+    ref = F.scaled_dot_product_attention(*(torch.from_numpy(x) for x in (q, k, v)), attn_mask=am,
+                                         scale=0.35)
+    assert np.max(np.abs(o - ref.numpy())) < 1e-12
+
+
 BWD_CASES = [
     dict(mask_kind="none", Nq=13, Nk=21),
     dict(mask_kind="causal", Nq=17, Nk=17),
     dict(mask_kind="causal", Nq=9, Nk=20),
+    dict(mask_kind="causal_br", Nq=9, Nk=20),
     dict(mask_kind="clamp", Nq=30, Nk=30, window=(3, 5), grid=(5, 6)),
     dict(mask_kind="wrap", Nq=36, Nk=36, window=3, grid=(6, 6), dilation=2),
     dict(mask_kind="clamp", Nq=48, Nk=48, window=(3, 3, 1), grid=(3, 4, 4), wrap=(True, False, True)),
@@ -578,6 +628,7 @@ def all_checks(goldens):
         ("na3d_closed_form", na3d_closed_form),
         ("na3d_flat_is_na2d", na3d_flat_is_na2d),
         ("na3d_wrap_pad_clamp", na3d_wrap_pad_clamp),
+        ("causal_bottom_right", causal_bottom_right),
         ("bwd_autograd_fp64", bwd_autograd_fp64),
         ("bwd_finite_differences", bwd_finite_differences),
         ("bwd_invariants", bwd_invariants),

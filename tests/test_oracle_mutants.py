@@ -33,6 +33,10 @@ MUTANTS = {
     "na_wrap_axes_swapped": ("const int row_ok = p->wrap_h ?", "const int row_ok = p->wrap_w ?"),
     "dilation_residue_ignored": ("if (kc % dl != residue) return 0;", ""),
     "softmax_sign": ("double w = exp(scores[j] - M);", "double w = exp(M - scores[j]);"),
+    "causal_br_offset_off_by_one": ("return (int64_t)j <= (int64_t)i + (p->Nk - p->Nq);",
+                                    "return (int64_t)j < (int64_t)i + (p->Nk - p->Nq);"),
+    "causal_br_offset_reversed": ("return (int64_t)j <= (int64_t)i + (p->Nk - p->Nq);",
+                                  "return (int64_t)j <= (int64_t)i + (p->Nq - p->Nk);"),
     "na3_depth_dropped": ("return axis_allowed(p->wrap_d, qt, kt, p->grid_d, p->window_d, p->dilation) &&",
                           "return 1 &&"),
     "na3_plane_stride": ("const int plane = p->grid_h * p->grid_w;",
