@@ -26,6 +26,7 @@ ATTN_MASK_NONE = 0
 ATTN_MASK_CAUSAL = 1
 ATTN_MASK_NA2D = 2
 ATTN_MASK_NA3D = 3
+ATTN_MASK_CAUSAL_BR = 4
 
 
 class AttnParamsEx(ctypes.Structure):

@@ -24,7 +24,8 @@ import torch
 from . import _lib
 
 _MASKS = {"none": _lib.ATTN_MASK_NONE, "causal": _lib.ATTN_MASK_CAUSAL,
-          "clamp": _lib.ATTN_MASK_NA2D, "wrap": _lib.ATTN_MASK_NA2D}
+          "causal_br": _lib.ATTN_MASK_CAUSAL_BR, "clamp": _lib.ATTN_MASK_NA2D,
+          "wrap": _lib.ATTN_MASK_NA2D}
 
 
 def _strides(t: torch.Tensor, layout: str):
@@ -128,7 +129,8 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, scale: float 
              workspace: torch.Tensor | None = None, wrap_axes=None):
     """Fused exact attention forward over [B, H, N, d] bf16 tensors.
 
-    mask: 'none' | 'causal' | 'clamp' | 'wrap' (the last two: neighbourhood
+    mask: 'none' | 'causal' (top-left) | 'causal_br' (bottom-right: query i sees keys
+    up to i + Nk - Nq) | 'clamp' | 'wrap' (the last two: neighbourhood
     attention over grid=(rows, columns), square by default, or a volume
     grid=(depth, rows, columns), with an odd `window` or one per axis;
     wrap_axes (one boolean per axis) chooses per axis whether the window

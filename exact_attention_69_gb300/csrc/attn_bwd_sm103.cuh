@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dq_kernel(const __gri
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool row_ok = q < p.Nq;
     const int64_t ri = static_cast<int64_t>(bh) * p.Nq + q;
-    const float lse2 = row_ok ? bp.lse[ri] * 1.44269504088896340736f : 0.f;
+    // a row that saw no key has LSE -inf: +inf here makes its P exactly 0
+    const float lse_r = row_ok ? bp.lse[ri] : 0.f;
+    const float lse2 = lse_r == -CUDART_INF_F ? CUDART_INF_F : lse_r * 1.44269504088896340736f;
     const float drow = row_ok ? bp.dd[ri] : 0.f;
     const NaQuery nq = na_query<MASK>(p, q);
     uint32_t s_par = 0;
@@ -530,7 +532,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
       for (int t = lane; t < kBM; t += 32) {
         const int q = i * kBM + t;
         const int64_t ri = static_cast<int64_t>(bh) * p.Nq + q;
-        vec[t] = q < p.Nq ? bp.lse[ri] * 1.44269504088896340736f : CUDART_INF_F;
+        const float lr = q < p.Nq ? bp.lse[ri] : -CUDART_INF_F;  // no key or no row: P = 0
+        vec[t] = lr == -CUDART_INF_F ? CUDART_INF_F : lr * 1.44269504088896340736f;
         vec[kBM + t] = q < p.Nq ? bp.dd[ri] : 0.f;
       }
       __syncwarp();
@@ -601,7 +604,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_dkv_kernel(const __gr
       const float* vec = reinterpret_cast<const float*>(smem + BC::kOffVec + s * BC::kVecBytes);
       const int q0 = i * kBM;
       // causal: query q sees key kk iff q >= kk; first allowed column of this tile
-      const int first = MASK == kMaskCausal ? kk - q0 : 0;
+      const int first = mask_is_causal(MASK) ? kk - causal_shift<MASK>(p) - q0 : 0;
       uint32_t nab[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
       if (mask_is_na(MASK)) na_key_bits<MASK>(p, q0, kk, nab);
 #pragma unroll
@@ -715,6 +718,7 @@ cudaError_t launch_bwd_dim(const BwdParams& bp, int mask, const BwdStreams& s) {
   switch (mask) {
     case kMaskNone: return launch_bwd_mask<D, kMaskNone>(bp, s);
     case kMaskCausal: return launch_bwd_mask<D, kMaskCausal>(bp, s);
+    case kMaskCausalBR: return launch_bwd_mask<D, kMaskCausalBR>(bp, s);
     case kMaskNa + 0: return launch_bwd_mask<D, kMaskNa + 0>(bp, s);
     case kMaskNa + 1: return launch_bwd_mask<D, kMaskNa + 1>(bp, s);
     case kMaskNa + 2: return launch_bwd_mask<D, kMaskNa + 2>(bp, s);

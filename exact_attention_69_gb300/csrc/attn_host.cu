@@ -136,7 +136,7 @@ int validate(const attn_params_ex* p, Checked* c) {
     return fail(ATTN_ERR_UNSUPPORTED, "head dimension %d is not one of 32, 64, 128", p->d);
   if (!std::isfinite(p->scale) || !(p->scale > 0.f))
     return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
-  if (p->mask_kind < ATTN_MASK_NONE || p->mask_kind > ATTN_MASK_NA3D)
+  if (p->mask_kind < ATTN_MASK_NONE || p->mask_kind > ATTN_MASK_CAUSAL_BR)
     return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", p->mask_kind);
   const int64_t BH = static_cast<int64_t>(p->B) * p->H;
   const int64_t n_qpairs = (static_cast<int64_t>(p->Nq) + 2 * attn::kBM - 1) / (2 * attn::kBM);
@@ -237,8 +237,10 @@ int kernel_mask(const attn_params_ex* p, const Checked& c, attn::KernelParams* k
   kp->dilation = na ? p->dilation : 1;
   kp->na_wrap = (wrap_cols ? attn::kNa3WrapCols : 0) | (wrap_rows ? attn::kNa3WrapRows : 0) |
                 (p->wrap_d ? attn::kNa3WrapDepth : 0);
+  kp->causal_off = p->mask_kind == ATTN_MASK_CAUSAL_BR ? p->Nk - p->Nq : 0;
   switch (p->mask_kind) {
     case ATTN_MASK_CAUSAL: return attn::kMaskCausal;
+    case ATTN_MASK_CAUSAL_BR: return attn::kMaskCausalBR;
     case ATTN_MASK_NA2D: return attn::na_mask(wrap_rows, wrap_cols, p->dilation > 1);
     case ATTN_MASK_NA3D: return attn::kMaskNa3;
     default: return attn::kMaskNone;

@@ -29,13 +29,17 @@ constexpr int kMaxSplitCtas = 256;  // largest grid of the split schedule (its r
 enum MaskKind : int { kMaskNone = 0, kMaskCausal = 1, kMaskNa = 2 };
 constexpr int kNaWrapCols = 1, kNaWrapRows = 2, kNaDilated = 4;
 constexpr int kMaskNa3 = kMaskNa + 8;
-constexpr int kMaskKinds = kMaskNa3 + 1;
+// Bottom-right causal: causal with the key bound shifted by Nk - Nq (read at
+// run time), kept apart so that top-left causal keeps a compile-time bound.
+constexpr int kMaskCausalBR = kMaskNa3 + 1;
+constexpr int kMaskKinds = kMaskCausalBR + 1;
 constexpr int kNa3WrapCols = 1, kNa3WrapRows = 2, kNa3WrapDepth = 4;  // KernelParams::na_wrap
 __host__ __device__ constexpr int na_mask(bool wrap_rows, bool wrap_cols, bool dilated) {
   return kMaskNa + (wrap_cols ? kNaWrapCols : 0) + (wrap_rows ? kNaWrapRows : 0) +
          (dilated ? kNaDilated : 0);
 }
-__host__ __device__ constexpr bool mask_is_na(int m) { return m >= kMaskNa; }
+__host__ __device__ constexpr bool mask_is_na(int m) { return m >= kMaskNa && m <= kMaskNa3; }
+__host__ __device__ constexpr bool mask_is_causal(int m) { return m == kMaskCausal || m == kMaskCausalBR; }
 __host__ __device__ constexpr bool mask_is_na2(int m) { return m >= kMaskNa && m < kMaskNa3; }
 __host__ __device__ constexpr bool mask_na_wrap_rows(int m) {
   return mask_is_na2(m) && ((m - kMaskNa) & kNaWrapRows) != 0;
@@ -62,6 +66,7 @@ struct KernelParams {
   int grid_h, grid_w;           // neighbourhood masks only: token grid
   int window_h, window_w;       // window size along the rows and the columns
   int dilation;                 // neighbourhood masks: key stride along each axis (>= 1)
+  int causal_off;               // kMaskCausalBR: key k allowed iff k <= q + causal_off (Nk - Nq)
   int grid_d, window_d;         // kMaskNa3: depth of the volume and window along it
   int na_wrap;                  // kMaskNa3: kNa3Wrap* bits of the axes that wrap
   int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head

@@ -365,6 +365,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const C
 
 // ------------------------------------------------------------- work and masks
 
+// The causal key bound's shift: key k allowed iff k <= q + shift (0 for
+// top-left, a compile-time constant there; Nk - Nq for bottom-right).
+template <int MASK>
+__host__ __device__ __forceinline__ int causal_shift(const KernelParams& p) {
+  return MASK == kMaskCausalBR ? p.causal_off : 0;
+}
+
 struct Task {
   int b, h, bh;
   int q0[2];
@@ -378,7 +385,7 @@ template <int MASK>
 __host__ __device__ __forceinline__ Task decode_task(int t, const KernelParams& p) {
   const int BH = p.B * p.H;
   int bh, qp;
-  if (MASK == kMaskCausal) {
+  if (mask_is_causal(MASK)) {
     bh = t % BH;
     qp = p.n_qpairs - 1 - t / BH;
   } else {
@@ -623,9 +630,10 @@ __host__ __device__ __forceinline__ int tile_class(int q0, int j, const KernelPa
   const bool ragged = k0 + kBN > p.Nk;
   if (MASK == kMaskNone) return ragged ? 2 : 1;
   const int q1 = min(q0 + kBM, p.Nq);
-  if (MASK == kMaskCausal) {
-    if (k0 > q1 - 1) return 0;
-    return (!ragged && k0 + kBN - 1 <= q0) ? 1 : 2;
+  if (mask_is_causal(MASK)) {  // key k allowed iff k <= q + off
+    const int off = causal_shift<MASK>(p);
+    if (k0 > q1 - 1 + off) return 0;
+    return (!ragged && k0 + kBN - 1 <= q0 + off) ? 1 : 2;
   }
   if (MASK == kMaskNa3) return na3_tile_meets(q0, q1, k0, min(k0 + kBN, p.Nk), p) ? 2 : 0;
   return na_tile_meets<mask_na_wrap_rows(MASK), mask_na_wrap_cols(MASK), mask_na_dilated(MASK)>(
@@ -1415,9 +1423,9 @@ __device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams
                                           const NaQuery& nq) {
   const uint32_t neg_inf = __float_as_uint(-CUDART_INF_F);
   const int k0 = j * kBN;
-  if (MASK == kMaskNone || MASK == kMaskCausal) {
+  if (MASK == kMaskNone || mask_is_causal(MASK)) {
     int lim = p.Nk - 1 - k0;                       // last valid key column
-    if (MASK == kMaskCausal) lim = min(lim, q - k0);
+    if (mask_is_causal(MASK)) lim = min(lim, q + causal_shift<MASK>(p) - k0);
 #pragma unroll
     for (int i = 0; i < 128; ++i)
       if (i > lim) s[i] = neg_inf;
@@ -1556,6 +1564,9 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     o_par ^= 1u;
     tc_fence_after();
     const float inv_l = l > 0.f ? 1.f / l : 0.f;
+    // a row that saw no key (bottom-right causal with Nq > Nk) is 0: O in
+    // TMEM may never have been written for it
+    const bool empty = !(l > 0.f);
     const bool row_ok = q < p.Nq;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
                           static_cast<int64_t>(q) * p.o_sn;
@@ -1572,8 +1583,9 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          packed[i] = pack_bf16(__uint_as_float(ov[2 * i]) * inv_l,
-                                __uint_as_float(ov[2 * i + 1]) * inv_l);
+          packed[i] = empty ? 0u
+                            : pack_bf16(__uint_as_float(ov[2 * i]) * inv_l,
+                                        __uint_as_float(ov[2 * i + 1]) * inv_l);
         uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -1689,6 +1701,7 @@ cudaError_t launch_dim(const KernelParams& p, int mask, int grid, cudaStream_t s
   switch (mask) {
     case kMaskNone: return launch_mask<D, kMaskNone>(p, grid, s);
     case kMaskCausal: return launch_mask<D, kMaskCausal>(p, grid, s);
+    case kMaskCausalBR: return launch_mask<D, kMaskCausalBR>(p, grid, s);
     case kMaskNa + 0: return launch_mask<D, kMaskNa + 0>(p, grid, s);
     case kMaskNa + 1: return launch_mask<D, kMaskNa + 1>(p, grid, s);
     case kMaskNa + 2: return launch_mask<D, kMaskNa + 2>(p, grid, s);

@@ -26,6 +26,10 @@
  * Allowed sets A(i):
  *   ATTN_MASK_NONE   every key j < Nk.
  *   ATTN_MASK_CAUSAL j <= i (top-left alignment, also when Nq != Nk).
+ *   ATTN_MASK_CAUSAL_BR j <= i + (Nk - Nq) (bottom-right alignment: the queries
+ *                    are the last Nq of Nk tokens). With Nq > Nk the first
+ *                    Nq - Nk rows see no key: O = 0, LSE = -inf (and zero
+ *                    gradients in attn_bwd).
  *   ATTN_MASK_NA2D   tokens are row-major on a grid_h x grid_w grid (Nq = Nk =
  *                    grid_h * grid_w); along each axis the window holds k
  *                    positions (k odd: `window` along the rows, `window_w`
@@ -85,13 +89,14 @@
 extern "C" {
 #endif
 
-#define ATTN_ABI_VERSION 5
+#define ATTN_ABI_VERSION 6
 
 typedef enum {
   ATTN_MASK_NONE = 0,
   ATTN_MASK_CAUSAL = 1,
   ATTN_MASK_NA2D = 2,
-  ATTN_MASK_NA3D = 3
+  ATTN_MASK_NA3D = 3,
+  ATTN_MASK_CAUSAL_BR = 4
 } attn_mask_kind;
 
 typedef enum {

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
 
 def test_struct_layout_and_version(lib):
     assert lib.attn_params_size() == ctypes.sizeof(_lib.AttnParamsEx)
-    assert lib.attn_abi_version() == 5
+    assert lib.attn_abi_version() == 6
 
 
 def test_error_strings(lib):
@@ -91,6 +91,8 @@ BAD = [
      _lib.ATTN_ERR_INVALID_ARG),
     ("grid_d_without_na3", dict(mask_kind=2, window=3, grid_d=1), _lib.ATTN_ERR_INVALID_ARG),
     ("wrap_d_without_na3", dict(wrap_d=1), _lib.ATTN_ERR_INVALID_ARG),
+    ("mask5", dict(mask_kind=5), _lib.ATTN_ERR_INVALID_ARG),
+    ("causal_br_window", dict(mask_kind=4, window=3), _lib.ATTN_ERR_INVALID_ARG),
 ]
 
 

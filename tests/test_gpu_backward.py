@@ -78,6 +78,13 @@ def test_backward_longer(E, mask):
     run_bwd(E, 1, 2, 1024, 1024, 64, mask, seed=11)
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(200, 333), (333, 200), (128, 1), (1, 257), (300, 128)])
+def test_backward_causal_bottom_right(E, d, Nq, Nk):
+    """Rows that see no key (Nq > Nk) have zero gradients and add nothing to dK, dV."""
+    run_bwd(E, 2, 1, Nq, Nk, d, "causal_br", seed=Nq + 2 * Nk + d)
+
+
 def test_autograd_wrapper_matches_attn_bwd(E):
     q, k, v = (t.cuda() for t in make_qkv(1, 2, 300, 300, 64, 1.0, 5))
     g = torch.randn(1, 2, 300, 64, generator=torch.Generator().manual_seed(6)).to(torch.bfloat16).cuda()

@@ -44,7 +44,8 @@ def check(o, lse, ref_o, ref_lse, rows=None):
     assert not bad.any(), (f"{int(bad.sum())} of {bad.size} O elements out of tolerance; "
                            f"max err {err.max():.3e}")
     both_inf = np.isneginf(lse) & np.isneginf(ref_lse)
-    lerr = np.where(both_inf, 0.0, np.abs(lse - ref_lse))
+    with np.errstate(invalid="ignore"):  # -inf - -inf in the rows that see no key
+        lerr = np.where(both_inf, 0.0, np.abs(lse - ref_lse))
     assert lerr.max() <= LSE_TOL, f"LSE max err {lerr.max():.3e}"
     return float(err.max()), float(lerr.max())
 
@@ -411,3 +412,20 @@ def test_tuned_schedule_is_valid_and_exact(E, mask, shape):
     ref_o, ref_lse = oracle.attention_rows(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()), rows,
                                            scale=1.0 / math.sqrt(d), mask_kind=mask)
     check(o, lse, ref_o, ref_lse, rows)
+
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(100, 300), (300, 100), (1, 700), (700, 1), (129, 1025), (1000, 260)])
+def test_causal_bottom_right(E, d, Nq, Nk):
+    """Query i sees keys 0 .. i + Nk - Nq; with Nq > Nk the first rows see none
+    (O = 0, LSE = -inf)."""
+    run(E, 2, 1, Nq, Nk, d, "causal_br", seed=Nq * 3 + Nk + d)
+
+
+def test_causal_bottom_right_equals_top_left_when_square(E):
+    q, k, v = (t.cuda() for t in make_qkv(1, 3, 777, 777, 64, 1.0, 51))
+    a = E.attn_fwd(q, k, v, mask="causal")
+    b = E.attn_fwd(q, k, v, mask="causal_br")
+    _status_ok(E)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
