@@ -97,6 +97,42 @@ def count_flops(w):
     return per_pair * 128 * 128 * float(tiles), per_pair * float(m.sum())
 
 
+def host_cpu_model() -> str:
+    """The host CPU as the OS names it (model name, or the Arm implementer and
+    part numbers), with the machine type."""
+    import platform
+    name = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+        for key in ("model name", "Model name", "Hardware"):
+            for ln in info:
+                if ln.split(":")[0].strip() == key:
+                    name = ln.split(":", 1)[1].strip()
+                    break
+            if name:
+                break
+        if not name:
+            impl = next((ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU implementer")), "")
+            part = next((ln.split(":", 1)[1].strip() for ln in info if ln.startswith("CPU part")), "")
+            if impl or part:
+                name = f"implementer {impl} part {part}"
+    except OSError:
+        pass
+    return f"{name or platform.processor() or 'unknown'} ({platform.machine()})"
+
+
+def percentile(xs, q):
+    """q-th percentile (0..100) of a list, linear between order statistics."""
+    ys = sorted(xs)
+    if not ys:
+        return None
+    pos = (len(ys) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
 # ------------------------------------------------------------------ multi-rank
 
 def max_over_ranks(ms: float, dist_mod, device) -> float:
@@ -225,30 +261,43 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
+class OracleSampler:
+    """The fp64 oracle on bounded row samples of workload w: inputs prepared
+    and the cost per row measured once; each run() times one random sample of
+    rows spread over every (batch, head)."""
+
+    def __init__(self, w):
+        import oracle
+        from seeded_inputs import make_workload, to_f64
+        self.oracle = oracle
+        q, k, v = make_workload(w)
+        self.qf, self.kf, self.vf = to_f64(q), to_f64(k), to_f64(v)
+        self.total = w.B * w.H * w.Nq
+        self.kw = dict(scale=w.scale, mask_kind=w.mask, window=w.window, grid=w.grid,
+                       wrap=w.wrap_axes if w.wrap_axes is not None else False)
+        n = min(self.total, 64)
+        rows = np.sort(np.random.default_rng(7).choice(self.total, size=n, replace=False))
+        t = time.perf_counter()
+        oracle.attention_rows(self.qf, self.kf, self.vf, rows, **self.kw)
+        self.per_row = max((time.perf_counter() - t) / n, 1e-7)
+        self.threads = oracle.max_threads()
+
+    def run(self, target_s: float, seed_rows: int, min_rows: int = 1):
+        """(seconds, rows) of one sample sized to take about target_s."""
+        n = int(min(self.total, max(min_rows, target_s / self.per_row)))
+        rows = np.sort(np.random.default_rng(seed_rows).choice(self.total, size=n, replace=False))
+        t = time.perf_counter()
+        self.oracle.attention_rows(self.qf, self.kf, self.vf, rows, **self.kw)
+        return time.perf_counter() - t, n
+
+
 def oracle_sample(w, target_s: float, seed_rows: int = 7):
     """Time the fp64 oracle on a bounded row sample of workload w.
 
-    Returns (seconds, rows, total_rows, threads). Rows are spread over every
-    (batch, head); the sample size is calibrated to take about target_s."""
-    import oracle
-    from seeded_inputs import make_workload, to_f64
-    q, k, v = make_workload(w)
-    qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
-    total = w.B * w.H * w.Nq
-    rng = np.random.default_rng(seed_rows)
-    kw = dict(scale=w.scale, mask_kind=w.mask, window=w.window, grid=w.grid,
-              wrap=w.wrap_axes if w.wrap_axes is not None else False)
-    n = min(total, 64)
-    rows = np.sort(rng.choice(total, size=n, replace=False))
-    t = time.perf_counter()
-    oracle.attention_rows(qf, kf, vf, rows, **kw)
-    per_row = max((time.perf_counter() - t) / n, 1e-7)
-    n = int(min(total, max(64, target_s / per_row)))
-    rows = np.sort(rng.choice(total, size=n, replace=False))
-    t = time.perf_counter()
-    oracle.attention_rows(qf, kf, vf, rows, **kw)
-    dt = time.perf_counter() - t
-    return dt, n, total, oracle.max_threads()
+    Returns (seconds, rows, total_rows, threads)."""
+    smp = OracleSampler(w)
+    dt, n = smp.run(target_s, seed_rows, min_rows=64)
+    return dt, n, smp.total, smp.threads
 
 
 def reference_arm(args, w):
@@ -258,12 +307,16 @@ def reference_arm(args, w):
     if rank != 0:
         return 0
     flops_tile, _ = count_flops(w)
-    per_step_target = float(os.environ.get("ATTN_REF_STEP_S", "3.0"))
+    # each step a bounded sample; the whole run (warm-up and timed steps)
+    # stays within ATTN_REF_TOTAL_S seconds of oracle work
+    n_all = max(1, args.warmup + args.steps)
+    per_step_target = min(float(os.environ.get("ATTN_REF_STEP_S", "3.0")),
+                          float(os.environ.get("ATTN_REF_TOTAL_S", "90")) / n_all)
+    smp = OracleSampler(w)
     times, rows_done = [], 0
-    total_rows = w.B * w.H * w.Nq
-    threads = 1
-    for i in range(args.warmup + args.steps):
-        dt, n, total_rows, threads = oracle_sample(w, per_step_target, seed_rows=100 + i)
+    total_rows, threads = smp.total, smp.threads
+    for i in range(n_all):
+        dt, n = smp.run(per_step_target, seed_rows=100 + i)
         if i >= args.warmup:
             times.append(dt)
             rows_done += n
@@ -279,7 +332,7 @@ def reference_arm(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, rotating_sets=None),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu_model": host_cpu_model()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -435,13 +488,15 @@ def ours_arm(args, w):
                 "frac_of_sustained": achieved / float(peaks["bf16_tflops_sustained"]),
                 "kernel_ms_avg": k_avg_ms,
                 "kernel_ms_eager_avg": sum(k_ms) / len(k_ms), "kernel_ms_eager_min": min(k_ms),
+                "kernel_ms_eager_p10": percentile(k_ms, 10), "kernel_ms_eager_p50": percentile(k_ms, 50),
+                "kernel_ms_eager_p90": percentile(k_ms, 90),
                 "exact_pairs_tflops": flops_exact / (k_avg_ms * 1e-3) / 1e12,
                 "hbm_gbs_compulsory": set_bytes / (k_avg_ms * 1e-3) / 1e9}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         dt, n, total, threads = oracle_sample(w, float(os.environ.get("ATTN_CPU_S", "12")))
         cpu = {"value": flops_tile * (n / total) / dt / 1e12, "unit": "TFLOP/s", "cores": threads,
-               "kind": "oracle",
+               "kind": "oracle", "cpu_model": host_cpu_model(),
                "sample": f"{n} of {total} query rows (random, every head) in {dt:.1f} s, fp64"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,

@@ -44,3 +44,14 @@ def test_two_gloo_ranks_report_the_slowest_rank():
 def test_single_process_is_unchanged():
     import bench
     assert bench.max_over_ranks(7.5, None, None) == 7.5
+
+
+def test_percentile_and_cpu_model_helpers():
+    import bench
+    xs = [5.0, 1.0, 3.0, 2.0, 4.0]
+    assert bench.percentile(xs, 0) == 1.0 and bench.percentile(xs, 100) == 5.0
+    assert bench.percentile(xs, 50) == 3.0
+    assert abs(bench.percentile(xs, 10) - 1.4) < 1e-12
+    assert bench.percentile([7.0], 90) == 7.0 and bench.percentile([], 50) is None
+    m = bench.host_cpu_model()
+    assert isinstance(m, str) and m.endswith(")")
