@@ -240,9 +240,12 @@ int attn_params_size(void);
  * lse: fp32 [B, H, Nq] as written by attn_fwd; all contiguous, device memory
  * owned by the caller, 16-byte aligned. mask_kind and the neighbourhood
  * fields as for attn_fwd (the same checks apply). dq, dk and dv are
- * overwritten. Three kernels are enqueued on the stream (rowsum(dout * O),
- * dQ, dK and dV); the library keeps a lazily grown per-device scratch of
- * B*H*Nq floats for D, so calls on one device must not overlap in time.
+ * overwritten. Three kernels are enqueued: rowsum(dout * O) and dQ on the
+ * stream, dK and dV on a library-owned second stream forked from it after the
+ * first kernel and joined back into it (so later work on the stream, and CUDA
+ * graph capture, see one ordered call). The library keeps a lazily grown
+ * per-device scratch of B*H*Nq floats for D, so calls on one device must not
+ * overlap in time.
  */
 typedef struct attn_bwd_params {
   const void* q;
