@@ -539,6 +539,8 @@ BWD_CASES = [
     dict(mask_kind="clamp", Nq=30, Nk=30, window=(3, 5), grid=(5, 6)),
     dict(mask_kind="wrap", Nq=36, Nk=36, window=3, grid=(6, 6), dilation=2),
     dict(mask_kind="clamp", Nq=48, Nk=48, window=(3, 3, 1), grid=(3, 4, 4), wrap=(True, False, True)),
+    dict(mask_kind="clamp", Nq=72, Nk=72, window=(1, 3, 3), grid=(2, 6, 6), wrap=(False, True, False),
+         dilation=2),
 ]
 
 
