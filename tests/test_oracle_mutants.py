@@ -46,6 +46,8 @@ MUTANTS = {
                                    "p->grid_d, p->window_h, p->dilation)"),
     "na3_axes_transposed": ("int kt = j / plane, ky = (j % plane) / p->grid_w, kx = j % p->grid_w;",
                             "int kx = j / plane, ky = (j % plane) / p->grid_w, kt = j % p->grid_w;"),
+    "bwd_mask_transposed": ("      ok[j] = (unsigned char)allowed(p, i, j);\n      if (!ok[j]) continue;\n      double dot = 0.0;",
+                            "      ok[j] = (unsigned char)allowed(p, j < p->Nq ? j : i, j < p->Nq ? i : j);\n      if (!ok[j]) continue;\n      double dot = 0.0;"),
     "bwd_dropped_d_term": ("const double dsij = pw[j] * (dp[j] - Di);", "const double dsij = pw[j] * dp[j];"),
     "bwd_dk_unscaled": ("dk[(int64_t)j * d + t] += p->scale * dsij * qi[t];",
                         "dk[(int64_t)j * d + t] += dsij * qi[t];"),
