@@ -180,6 +180,68 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Groups of MMAs along K in one statement, one election for the group: the
+// first MMA accumulates iff `accumulate`, the others always do. The start
+// address fields of consecutive k-steps' descriptors differ by the
+// compile-time steps O1.. (address >> 4; no step carries out of the field,
+// shared memory being below 256 KB). A group costs the issuing warp a
+// fraction of the instructions of separately elected MMAs, which keeps the
+// MMA warp's loop small.
+template <int O1>
+__device__ __forceinline__ void mma_ss2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 a1, b1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(O1)
+      : "memory");
+}
+
+template <int O1, int O2, int O3>
+__device__ __forceinline__ void mma_ss4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 a1, b1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "add.s64 a1, %1, %6;\n\tadd.s64 b1, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "add.s64 a1, %1, %7;\n\tadd.s64 b1, %2, %7;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(O1), "n"(O2), "n"(O3)
+      : "memory");
+}
+
+// Four MMAs with A in TMEM: A steps 8 columns (16 bf16 keys) per k-step, B
+// by the descriptor steps O1, O2, O3.
+template <int O1, int O2, int O3>
+__device__ __forceinline__ void mma_ts4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.s64 b1, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "add.u32 a1, %1, 16;\n\tadd.s64 b1, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t"
+      "add.u32 a1, %1, 24;\n\tadd.s64 b1, %2, %7;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(O1), "n"(O2), "n"(O3)
+      : "memory");
+}
+
 // One arrive on `bar` once every tcgen05 operation issued so far by the
 // elected lane is complete (warp-wide; the same lane that issued the MMAs).
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -310,57 +372,66 @@ struct Ctl {
   uint64_t timeout_ns;
 };
 
-static __device__ __forceinline__ void report_timeout(const Ctl& c, uint32_t role, int tile) {
-  if (atomicCAS(c.status, 0u, kStatusTimeout) == 0u) {
-    c.status[1] = role;
-    c.status[2] = static_cast<uint32_t>(tile);
-    c.status[3] = blockIdx.x;
+// Records the first failure in the device status word and raises the CTA's
+// abort flag. Out of line: it runs only when a wait has run out.
+static __device__ __noinline__ void report_timeout(volatile uint32_t* abort, uint32_t* status,
+                                                   uint32_t role, int tile) {
+  if (atomicCAS(status, 0u, kStatusTimeout) == 0u) {
+    status[1] = role;
+    status[2] = static_cast<uint32_t>(tile);
+    status[3] = blockIdx.x;
     __threadfence();
   }
-  *c.abort = 1u;
+  *abort = 1u;
 }
 
-static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c, uint32_t role,
-                                       int tile, bool honour_abort) {
-  const uint64_t t0 = global_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_test_sleep(bar, parity, kSleepHintNs)) return true;
-    if (honour_abort && *c.abort) return false;
-    if ((n & 3u) == 0u) {
-      if (global_ns() - t0 > c.timeout_ns || n >= (1u << 28)) {
-        report_timeout(c, role, tile);
-        return false;
-      }
-    }
-  }
-}
-
-// Waits for the phase of parity `parity` of `bar`. False: the CTA is aborting.
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Ctl& c,
-                                           uint32_t role, int tile, bool honour_abort = true) {
-  if (mbar_test(bar, parity)) return true;
-  return wait_slow(bar, parity, c, role, tile, honour_abort);
-}
-
-// Warp-uniform wait: every lane polls the barrier and warp votes make each
-// decision (done, abort, time out) the same for all lanes, so the warp never
-// diverges. (Polling from one lane while the others wait at a shuffle costs
-// the warps that share the scheduler measurably.)
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, int tile,
-                                          uint32_t role = kRoleSoftmax, bool honour_abort = true) {
-  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+// The waiting part of warp_wait, out of line so that each wait site inlines
+// only its first poll and vote: the control warps' loops stay small enough
+// to run from the instruction cache. Called by all 32 lanes.
+static __device__ __forceinline__ bool warp_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                                   uint32_t* status, uint64_t timeout_ns, int tile,
+                                                   uint32_t role, bool honour_abort) {
   const uint64_t t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
     const bool ok = mbar_test_sleep(bar, parity, kSleepHintNs);
     if (__all_sync(0xffffffffu, ok)) return true;
-    if (honour_abort && __any_sync(0xffffffffu, *c.abort != 0u)) return false;
+    if (honour_abort && __any_sync(0xffffffffu, *abort != 0u)) return false;
     if ((n & 3u) == 0u &&
-        __any_sync(0xffffffffu, global_ns() - t0 > c.timeout_ns || n >= (1u << 28))) {
-      if ((threadIdx.x & 31) == 0) report_timeout(c, role, tile);
+        __any_sync(0xffffffffu, global_ns() - t0 > timeout_ns || n >= (1u << 28))) {
+      if ((threadIdx.x & 31) == 0) report_timeout(abort, status, role, tile);
       __syncwarp();
       return false;
     }
   }
+}
+
+// Warp-uniform wait for the phase of parity `parity` of `bar`: every lane
+// polls the barrier and warp votes make each decision (done, abort, time out)
+// the same for all lanes, so the warp never diverges. (Polling from one lane
+// while the others wait at a shuffle costs the warps that share the scheduler
+// measurably.) False: the CTA is aborting. Used by the softmax warps, whose
+// live S row would have to be saved around a call.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const Ctl& c, int tile,
+                                          uint32_t role = kRoleSoftmax, bool honour_abort = true) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  return warp_wait_slow(bar, parity, c.abort, c.status, c.timeout_ns, tile, role, honour_abort);
+}
+
+static __device__ __noinline__ bool ctl_wait_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                                  uint32_t* status, uint64_t timeout_ns, int tile,
+                                                  uint32_t role, bool honour_abort) {
+  return warp_wait_slow(bar, parity, abort, status, timeout_ns, tile, role, honour_abort);
+}
+
+// warp_wait for the loader and MMA warps: the same protocol with the waiting
+// part out of line. Each of their many wait sites then inlines one poll and
+// one vote, which keeps their loops a few KB long: measured on GB300, with
+// every wait inlined whole the MMA warp's loop took ~50 KB of code and ran at
+// instruction-fetch speed, hundreds of cycles per MMA issued.
+__device__ __forceinline__ bool ctl_wait(uint32_t bar, uint32_t parity, const Ctl& c, int tile,
+                                         uint32_t role, bool honour_abort = true) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  return ctl_wait_slow(bar, parity, c.abort, c.status, c.timeout_ns, tile, role, honour_abort);
 }
 
 // ------------------------------------------------------------- work and masks
@@ -938,17 +1009,19 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
                             const int64_t* cta_lo, const Ctl& ctl) {
   using C = Cfg<D>;
   uint32_t q_it = 0, k_it = 0, v_it = 0;
-  int q_armed = -1, k_armed[C::kKStages], v_armed[C::kVStages];
-  for (int s = 0; s < C::kKStages; ++s) k_armed[s] = -1;
-  for (int s = 0; s < C::kVStages; ++s) v_armed[s] = -1;
+  // Stage bookkeeping for the drain, as bit masks (bit s: stage s holds an
+  // armed copy; its phase parity), so that it stays in registers.
+  int q_armed = -1;
+  uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
   bool injected = false;
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
     const Band band = task_band<MASK>(tk, p);
-    if (!warp_wait(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, -1, kRoleLoader)) goto drain;
+    if (!ctl_wait(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, -1, kRoleLoader)) goto drain;
     mbar_expect_tx(bars.q_full(), 2 * C::kTileBytes);
+#pragma unroll
     for (int h = 0; h < 2; ++h)
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_4d(sbase + C::kOffQ + h * C::kTileBytes + c * C::kChunkBytes, &p.tm_q,
@@ -963,7 +1036,7 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
          j < sg.kv1;
          j = kNa ? cur.next(tk, sg.kv1, act, p) : next_tile<MASK>(tk, band, j, sg.kv1, p), ++nth) {
       const int ks = static_cast<int>(k_it % C::kKStages);
-      if (!warp_wait(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
+      if (!ctl_wait(bars.k_empty(ks), ((k_it / C::kKStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
         goto drain;
       if (p.inject && !injected && nth == 1) {
         injected = true;  // withhold this K tile: the MMA issuer's wait must run out
@@ -972,27 +1045,29 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(sbase + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &p.tm_k,
                       bars.k_full(ks), c * C::kBoxCols, j * kBN, tk.h, tk.b);
-        k_armed[ks] = static_cast<int>((k_it / C::kKStages) & 1u);
+        k_armed |= 1u << ks;
+        k_par = (k_par & ~(1u << ks)) | (((k_it / C::kKStages) & 1u) << ks);
       }
       ++k_it;
       const int vs = static_cast<int>(v_it % C::kVStages);
-      if (!warp_wait(bars.v_empty(vs), ((v_it / C::kVStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
+      if (!ctl_wait(bars.v_empty(vs), ((v_it / C::kVStages) & 1u) ^ 1u, ctl, j, kRoleLoader))
         goto drain;
       mbar_expect_tx(bars.v_full(vs), C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
         tma_load_4d(sbase + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &p.tm_v,
                     bars.v_full(vs), c * C::kBoxCols, j * kBN, tk.h, tk.b);
-      v_armed[vs] = static_cast<int>((v_it / C::kVStages) & 1u);
+      v_armed |= 1u << vs;
+      v_par = (v_par & ~(1u << vs)) | (((v_it / C::kVStages) & 1u) << vs);
       ++v_it;
     }
   }
 drain:
   // The last copy armed on each barrier must have landed before the CTA exits.
-  if (q_armed >= 0) warp_wait(bars.q_full(), q_armed, ctl, -1, kRoleLoader, false);
+  if (q_armed >= 0) ctl_wait(bars.q_full(), q_armed, ctl, -1, kRoleLoader, false);
   for (int s = 0; s < C::kKStages; ++s)
-    if (k_armed[s] >= 0) warp_wait(bars.k_full(s), k_armed[s], ctl, -1, kRoleLoader, false);
+    if ((k_armed >> s) & 1u) ctl_wait(bars.k_full(s), (k_par >> s) & 1u, ctl, -1, kRoleLoader, false);
   for (int s = 0; s < C::kVStages; ++s)
-    if (v_armed[s] >= 0) warp_wait(bars.v_full(s), v_armed[s], ctl, -1, kRoleLoader, false);
+    if ((v_armed >> s) & 1u) ctl_wait(bars.v_full(s), (v_par >> s) & 1u, ctl, -1, kRoleLoader, false);
 }
 
 // Descriptors of consecutive k-steps differ only in the start address field
@@ -1008,14 +1083,17 @@ __device__ __forceinline__ uint32_t opaque(uint32_t x) {
 template <int D>
 __device__ __forceinline__ void issue_s(uint32_t tmem, int h, uint32_t q_tile, uint32_t k_tile) {
   using C = Cfg<D>;
-  q_tile = opaque(q_tile);
-  k_tile = opaque(k_tile);
   const uint64_t a0 = smem_desc(q_tile, 16, 8 * C::kSwizzle, C::kLayout);
   const uint64_t b0 = smem_desc(k_tile, 16, 8 * C::kSwizzle, C::kLayout);
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    const uint32_t off = ((ks * 16) / C::kBoxCols) * C::kChunkBytes + ((ks * 16) % C::kBoxCols) * 2;
-    mma_ss(tmem + C::tm_s(h), a0 + (off >> 4), b0 + (off >> 4), C::kIdescS, ks > 0 ? 1u : 0u);
+  const uint32_t d = tmem + C::tm_s(h);
+  // k-steps of 16 columns (32 bytes) inside a swizzle row; d = 128 has two
+  // 64-column chunks, kChunkBytes apart
+  if constexpr (D == 32) {
+    mma_ss2<2>(d, a0, b0, C::kIdescS, 0u);
+  } else {
+    mma_ss4<2, 4, 6>(d, a0, b0, C::kIdescS, 0u);
+    if constexpr (D == 128)
+      mma_ss4<2, 4, 6>(d, a0 + (C::kChunkBytes >> 4), b0 + (C::kChunkBytes >> 4), C::kIdescS, 1u);
   }
 }
 
@@ -1026,46 +1104,64 @@ template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, bool accumulate,
                                          int part) {
   using C = Cfg<D>;
-  v_tile = opaque(v_tile);
   const uint64_t b0 = smem_desc(v_tile, C::kChunkBytes, 8 * C::kSwizzle, C::kLayout);
   const uint32_t t_o = tmem + C::tm_o(h), t_p = tmem + C::tm_p(h);
-#pragma unroll
-  for (int k = 0; k < kBN / 32; ++k) {
-    const int ks = part * (kBN / 32) + k;
-    mma_ts(t_o, t_p + ks * 8, b0 + ((ks * 16 * C::kSwizzle) >> 4), C::kIdescO,
-           (accumulate || k > 0) ? 1u : 0u);
-  }
+  // k-step ks (16 keys): P columns 8 * ks, V rows 16 * ks (16 * kSwizzle bytes)
+  constexpr int kStep = C::kSwizzle;  // (16 * kSwizzle) >> 4
+  const int ks0 = part * (kBN / 32);
+  mma_ts4<kStep, 2 * kStep, 3 * kStep>(t_o, t_p + ks0 * 8, b0 + ks0 * kStep, C::kIdescO,
+                                       accumulate ? 1u : 0u);
 }
 
 // One warp issues both products. P_h overwrites the first half of S_h, so
 // S_h of the next tile follows P V of this one: per tile, P V_h(j) then
-// S_h(j + 1) for each Q tile.
+// S_h(j + 1) for each Q tile. The per-Q-tile state lives in bit masks (bit h)
+// and the loop over the two Q tiles stays rolled, so that each issue and wait
+// site exists once in the code: the warp's loop then runs from the
+// instruction cache (this warp is the kernel's critical path, and at
+// instruction-fetch speed it spent hundreds of cycles per MMA).
 template <int D, int MASK>
 __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars, uint32_t tmem,
                          const int64_t* cta_lo, const Ctl& ctl) {
   using C = Cfg<D>;
+  constexpr bool kNa = mask_is_na(MASK);
   uint32_t q_it = 0, k_it = 0, v_it = 0;
-  uint32_t p_par[2] = {0, 0}, o_it[2] = {0, 0};
+  uint32_t p_par = 0;  // bit h: parity of Q tile h's next P phases
+  uint32_t o_par = 0;  // bit h: parity of Q tile h's next O phase
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
     const Band band = task_band<MASK>(tk, p);
-    if (!warp_wait(bars.q_full(), q_it & 1u, ctl, -1, kRoleMma)) goto drain;
+    if (!ctl_wait(bars.q_full(), q_it & 1u, ctl, -1, kRoleMma)) goto drain;
     ++q_it;
     tc_fence_after();
-    bool o_ready[2] = {false, false};
-    // neighbourhood masks: the cursor's flags; others: the tile test itself
-    constexpr bool kNa = mask_is_na(MASK);
+    uint32_t o_ready = 0;  // bit h: O_h holds this task's partial sum
+    // bit h of `act`: Q tile h needs the K/V tile (neighbourhood masks: the
+    // cursor's flags; others: the tile test itself)
     TileCursor<MASK> cur(band, 2);
-    bool aj[2] = {false, false}, an[2] = {false, false};
-    int j = kNa ? cur.next(tk, sg.kv1, aj, p) : next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
+    auto step = [&](int from, uint32_t& act) -> int {
+      if constexpr (kNa) {
+        bool a[2];
+        const int t = cur.next(tk, sg.kv1, a, p);
+        act = (a[0] ? 1u : 0u) | (a[1] ? 2u : 0u);
+        return t;
+      } else {
+        const int t = next_tile<MASK>(tk, band, from, sg.kv1, p);
+        act = t < sg.kv1 ? ((tile_active<MASK>(tk, 0, t, p) ? 1u : 0u) |
+                            (tile_active<MASK>(tk, 1, t, p) ? 2u : 0u))
+                         : 0u;
+        return t;
+      }
+    };
+    uint32_t aj = 0, an = 0;
+    int j = step(sg.kv0 - 1, aj);
     if (j < sg.kv1) {
       const int ks = static_cast<int>(k_it % C::kKStages);
-      if (!warp_wait(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, j, kRoleMma)) goto drain;
+      if (!ctl_wait(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
       for (int h = 0; h < 2; ++h)
-        if (kNa ? aj[h] : tile_active<MASK>(tk, h, j, p)) {
+        if ((aj >> h) & 1u) {
           issue_s<D>(tmem, h, sbase + C::kOffQ + h * C::kTileBytes,
                      sbase + C::kOffK + ks * C::kTileBytes);
           mma_commit(bars.s_full(h));
@@ -1074,31 +1170,32 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       ++k_it;
     }
     while (j < sg.kv1) {
-      const int jn = kNa ? cur.next(tk, sg.kv1, an, p) : next_tile<MASK>(tk, band, j, sg.kv1, p);
+      const int jn = step(j, an);
       const bool has_next = jn < sg.kv1;
       if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
       const int vs = static_cast<int>(v_it % C::kVStages);
-      if (!warp_wait(bars.v_full(vs), (v_it / C::kVStages) & 1u, ctl, j, kRoleMma)) goto drain;
+      if (!ctl_wait(bars.v_full(vs), (v_it / C::kVStages) & 1u, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
+      const uint32_t v_tile = sbase + C::kOffV + vs * C::kTileBytes;
       int ksn = -1;
       for (int h = 0; h < 2; ++h) {
-        if (kNa ? aj[h] : tile_active<MASK>(tk, h, j, p)) {
-          if (!o_ready[h]) {
-            if (!warp_wait(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, j, kRoleMma)) goto drain;
+        if ((aj >> h) & 1u) {
+          if (!((o_ready >> h) & 1u)) {
+            if (!ctl_wait(bars.o_empty(h), ((o_par >> h) & 1u) ^ 1u, ctl, j, kRoleMma)) goto drain;
           }
+          const uint32_t par = (p_par >> h) & 1u;
           for (int part = 0; part < 2; ++part) {
-            if (!warp_wait(bars.p_full(h, part), p_par[h], ctl, j, kRoleMma)) goto drain;
+            if (!ctl_wait(bars.p_full(h, part), par, ctl, j, kRoleMma)) goto drain;
             tc_fence_after();
-            issue_pv<D>(tmem, h, sbase + C::kOffV + vs * C::kTileBytes, o_ready[h] || part > 0,
-                        part);
+            issue_pv<D>(tmem, h, v_tile, ((o_ready >> h) & 1u) != 0u || part > 0, part);
           }
-          p_par[h] ^= 1u;
-          o_ready[h] = true;
+          p_par ^= 1u << h;
+          o_ready |= 1u << h;
         }
-        if (has_next && (kNa ? an[h] : tile_active<MASK>(tk, h, jn, p))) {
+        if (has_next && ((an >> h) & 1u)) {
           if (ksn < 0) {
             ksn = static_cast<int>(k_it % C::kKStages);
-            if (!warp_wait(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, jn, kRoleMma))
+            if (!ctl_wait(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, jn, kRoleMma))
               goto drain;
             tc_fence_after();
           }
@@ -1114,22 +1211,21 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
         ++k_it;
       }
       j = jn;
-      aj[0] = an[0];
-      aj[1] = an[1];
+      aj = an;
     }
     for (int h = 0; h < 2; ++h) {
       if (!tk.live[h]) continue;
-      if (!o_ready[h]) {  // keeps the o_empty phases in step even without a PV
-        if (!warp_wait(bars.o_empty(h), (o_it[h] & 1u) ^ 1u, ctl, -1, kRoleMma)) goto drain;
+      if (!((o_ready >> h) & 1u)) {  // keeps the o_empty phases in step even without a PV
+        if (!ctl_wait(bars.o_empty(h), ((o_par >> h) & 1u) ^ 1u, ctl, -1, kRoleMma)) goto drain;
       }
       mma_commit(bars.o_full(h));
-      ++o_it[h];
+      o_par ^= 1u << h;
     }
   }
 drain:
   // Every MMA this thread issued must be complete before TMEM is freed.
   mma_commit(bars.done());
-  warp_wait(bars.done(), 0, ctl, -1, kRoleMma, false);
+  ctl_wait(bars.done(), 0, ctl, -1, kRoleMma, false);
 }
 
 // ------------------------------------------------------------- partial results
@@ -1160,7 +1256,7 @@ __device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t 
     if (old == assumed) return cnt + 1u;
     assumed = old;
   }
-  report_timeout(c, kRoleSoftmax, -2);
+  report_timeout(c.abort, c.status, kRoleSoftmax, -2);
   return 0u;
 }
 
