@@ -84,6 +84,10 @@ int make_plan(const attn_params_ex* p, int sm_count, Plan* pl) {
     const int64_t by_units = (pl->units + kMinSplitUnits - 1) / kMinSplitUnits;
     pl->grid = static_cast<int>(by_units < ctas ? by_units : ctas);
     if (pl->grid > attn::kMaxSplitCtas) pl->grid = attn::kMaxSplitCtas;
+    // the kernel counts a CTA's share in 32 bits: larger shares run as whole tasks
+    if ((pl->units + pl->grid - 1) / pl->grid >= (int64_t{1} << 31)) pl->split = 0;
+  }
+  if (pl->split) {
     pl->part_bytes = static_cast<size_t>(pl->grid) * 2 * 2 * 128 * (p->d + 2) * sizeof(float);
     pl->count_bytes = static_cast<size_t>(pl->n_tasks) * 2 * 4 * sizeof(unsigned long long);
   } else {

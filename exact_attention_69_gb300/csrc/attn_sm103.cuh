@@ -331,10 +331,12 @@ struct Cfg {
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kBarBytes = 512;
   static_assert(8 * (13 + 2 * kKStages + 2 * kVStages) + 8 <= kBarBytes, "barrier area");
-  // first unit of every CTA of a split schedule (kMaxSplitCtas + 1 int64)
+  // first unit of every CTA of a split schedule (kMaxSplitCtas + 1 int64),
+  // then this CTA's first (task, K/V tile) packed in one int64
   static constexpr int kOffTbl = kOffBar + kBarBytes;
-  static constexpr int kTblBytes = 8 * (kMaxSplitCtas + 1);
+  static constexpr int kTblBytes = 8 * (kMaxSplitCtas + 2);
   static constexpr int kSmemBytes = kOffTbl + kTblBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kLayout = D >= 64 ? 2u : 4u;
   static constexpr uint32_t kIdescS = make_idesc(kBM, kBN, false);
   static constexpr uint32_t kIdescO = make_idesc(kBM, D, true);
@@ -793,27 +795,39 @@ __host__ __device__ __forceinline__ int64_t unit_lo(int64_t units, int ctas, int
   return static_cast<int64_t>(c) * units / ctas;
 }
 
+// The split schedule's segments of this CTA, walked without division: the
+// first (task, K/V tile) comes from the prologue's table, then the position
+// advances by each segment's length. (A 64-bit division per segment is a
+// call into a library routine, and the call made the MMA warp, which runs
+// with few registers, spill its loop state to local memory.)
 template <int MASK>
 struct SegIter {
-  int64_t u, hi;
-  int t_rr;
+  int rest;  // units of this CTA not yet handed out (< 2^31: the host splits no larger share)
+  int t_rr, kv;
   bool first;
   __device__ __forceinline__ SegIter(const KernelParams& p, const int64_t* lo) : first(true) {
     if (MASK == kMaskNone && p.split) {
-      u = lo[blockIdx.x];
-      hi = lo[blockIdx.x + 1];
+      rest = static_cast<int>(lo[blockIdx.x + 1] - lo[blockIdx.x]);
+      const int64_t f = lo[kMaxSplitCtas + 1];
+      t_rr = static_cast<int>(f >> 32);
+      kv = static_cast<int>(f & 0xffffffff);
     } else {
       t_rr = blockIdx.x;
     }
   }
   __device__ __forceinline__ bool next(const KernelParams& p, Seg& s) {
     if (MASK == kMaskNone && p.split) {
-      if (u >= hi) return false;
-      s.t = static_cast<int>(u / p.n_kv);
-      s.kv0 = static_cast<int>(u - static_cast<int64_t>(s.t) * p.n_kv);
-      const int64_t len = min(static_cast<int64_t>(p.n_kv - s.kv0), hi - u);
-      s.kv1 = s.kv0 + static_cast<int>(len);
-      u += len;
+      if (rest <= 0) return false;
+      s.t = t_rr;
+      s.kv0 = kv;
+      const int len = min(rest, p.n_kv - kv);
+      s.kv1 = kv + len;
+      rest -= len;
+      kv += len;
+      if (kv == p.n_kv) {
+        kv = 0;
+        ++t_rr;
+      }
     } else {
       if (t_rr >= p.n_tasks) return false;
       s.t = t_rr;
@@ -1070,62 +1084,91 @@ drain:
     if ((v_armed >> s) & 1u) ctl_wait(bars.v_full(s), (v_par >> s) & 1u, ctl, -1, kRoleLoader, false);
 }
 
-// Descriptors of consecutive k-steps differ only in the start address field
-// (bits 0-13, address >> 4), and no step carries out of it (shared memory is
-// below 256 KB): each step adds a compile-time offset to one base descriptor.
-// The MMA issuer runs with few registers: an opaque copy of an address keeps
-// the compiler from hoisting every per-step descriptor out of the tile loop.
+// An opaque copy of a value: keeps the compiler from hoisting every per-step
+// value derived from it out of a loop (used where registers are scarce).
 __device__ __forceinline__ uint32_t opaque(uint32_t x) {
   asm volatile("mov.b32 %0, %0;" : "+r"(x));
   return x;
 }
 
+// Shared-memory descriptors of the MMA operands, built once per CTA. Stage s
+// of the K (V) ring is the stage-0 descriptor plus s * (kTileBytes >> 4) in
+// the start-address field (bits 0-13, address >> 4); shared memory is below
+// 256 KB, so no step carries out of the field. The MMA warp is the kernel's
+// critical path and every instruction of its loop shows in the launch time,
+// so nothing of this is recomputed per tile.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tmem, int h, uint32_t q_tile, uint32_t k_tile) {
+struct Descs {
+  uint64_t q0, q1;  // Q tiles 0 and 1 (K-major)
+  uint64_t k0;      // K ring stage 0 (K-major)
+  uint64_t v0;      // V ring stage 0 (MN-major)
+  __device__ __forceinline__ explicit Descs(uint32_t sbase) {
+    using C = Cfg<D>;
+    q0 = smem_desc(sbase + C::kOffQ, 16, 8 * C::kSwizzle, C::kLayout);
+    q1 = smem_desc(sbase + C::kOffQ + C::kTileBytes, 16, 8 * C::kSwizzle, C::kLayout);
+    k0 = smem_desc(sbase + C::kOffK, 16, 8 * C::kSwizzle, C::kLayout);
+    v0 = smem_desc(sbase + C::kOffV, C::kChunkBytes, 8 * C::kSwizzle, C::kLayout);
+  }
+  static constexpr uint64_t kStageStep = static_cast<uint64_t>(Cfg<D>::kTileBytes >> 4);
+};
+
+// S_h = Q_h K^T: k-steps of 16 columns (32 bytes) inside a swizzle row; d =
+// 128 has two 64-column chunks, kChunkBytes apart.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
   using C = Cfg<D>;
-  const uint64_t a0 = smem_desc(q_tile, 16, 8 * C::kSwizzle, C::kLayout);
-  const uint64_t b0 = smem_desc(k_tile, 16, 8 * C::kSwizzle, C::kLayout);
-  const uint32_t d = tmem + C::tm_s(h);
-  // k-steps of 16 columns (32 bytes) inside a swizzle row; d = 128 has two
-  // 64-column chunks, kChunkBytes apart
   if constexpr (D == 32) {
-    mma_ss2<2>(d, a0, b0, C::kIdescS, 0u);
+    mma_ss2<2>(d_tmem, a0, b0, C::kIdescS, 0u);
   } else {
-    mma_ss4<2, 4, 6>(d, a0, b0, C::kIdescS, 0u);
+    mma_ss4<2, 4, 6>(d_tmem, a0, b0, C::kIdescS, 0u);
     if constexpr (D == 128)
-      mma_ss4<2, 4, 6>(d, a0 + (C::kChunkBytes >> 4), b0 + (C::kChunkBytes >> 4), C::kIdescS, 1u);
+      mma_ss4<2, 4, 6>(d_tmem, a0 + (C::kChunkBytes >> 4), b0 + (C::kChunkBytes >> 4), C::kIdescS,
+                       1u);
   }
 }
 
-// O_h += P_h[:, keys of `part`] V_j[keys of `part`, :], part 0 = keys 0-63, 1 = keys 64-127.
-// V is [key, d] with d contiguous: the B operand (K = keys, N = d) is MN-major;
-// 16 keys = 16 rows of kSwizzle bytes; column chunks are kChunkBytes apart.
+// O_h += P_h[:, keys of `part`] V_j[keys of `part`, :], part 0 = keys 0-63, 1 =
+// keys 64-127. V is [key, d] with d contiguous: the B operand (K = keys, N = d)
+// is MN-major; 16 keys = 16 rows of kSwizzle bytes (k-step ks: P columns
+// 8 * ks, V descriptor + ks * kSwizzle).
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, int h, uint32_t v_tile, bool accumulate,
-                                         int part) {
+__device__ __forceinline__ void issue_pv(uint32_t t_o, uint32_t t_p, uint64_t v_desc, int part,
+                                         uint32_t accumulate) {
   using C = Cfg<D>;
-  const uint64_t b0 = smem_desc(v_tile, C::kChunkBytes, 8 * C::kSwizzle, C::kLayout);
-  const uint32_t t_o = tmem + C::tm_o(h), t_p = tmem + C::tm_p(h);
-  // k-step ks (16 keys): P columns 8 * ks, V rows 16 * ks (16 * kSwizzle bytes)
-  constexpr int kStep = C::kSwizzle;  // (16 * kSwizzle) >> 4
+  constexpr int kStep = C::kSwizzle;
   const int ks0 = part * (kBN / 32);
-  mma_ts4<kStep, 2 * kStep, 3 * kStep>(t_o, t_p + ks0 * 8, b0 + ks0 * kStep, C::kIdescO,
-                                       accumulate ? 1u : 0u);
+  mma_ts4<kStep, 2 * kStep, 3 * kStep>(t_o, t_p + ks0 * 8, v_desc + ks0 * kStep, C::kIdescO,
+                                       accumulate);
 }
+
+// A ring position: stage index and the parity of its current phase, advanced
+// without division.
+template <int N>
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void advance() {
+    if (++s == N) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
 
 // One warp issues both products. P_h overwrites the first half of S_h, so
 // S_h of the next tile follows P V of this one: per tile, P V_h(j) then
-// S_h(j + 1) for each Q tile. The per-Q-tile state lives in bit masks (bit h)
-// and the loop over the two Q tiles stays rolled, so that each issue and wait
-// site exists once in the code: the warp's loop then runs from the
-// instruction cache (this warp is the kernel's critical path, and at
-// instruction-fetch speed it spent hundreds of cycles per MMA).
+// S_h(j + 1) for each Q tile. The loops over the two Q tiles are unrolled, so
+// that every per-Q-tile quantity (descriptors, TMEM columns, barrier
+// addresses, phase bits) is a constant or a register of its own.
 template <int D, int MASK>
 __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars, uint32_t tmem,
                          const int64_t* cta_lo, const Ctl& ctl) {
   using C = Cfg<D>;
   constexpr bool kNa = mask_is_na(MASK);
-  uint32_t q_it = 0, k_it = 0, v_it = 0;
+  const Descs<D> dsc(sbase);
+  uint32_t q_ph = 0;
+  RingPos<C::kKStages> kr;
+  RingPos<C::kVStages> vr;
   uint32_t p_par = 0;  // bit h: parity of Q tile h's next P phases
   uint32_t o_par = 0;  // bit h: parity of Q tile h's next O phase
   SegIter<MASK> it(p, cta_lo);
@@ -1133,15 +1176,20 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
     const Band band = task_band<MASK>(tk, p);
-    if (!ctl_wait(bars.q_full(), q_it & 1u, ctl, -1, kRoleMma)) goto drain;
-    ++q_it;
+    if (!ctl_wait(bars.q_full(), q_ph, ctl, -1, kRoleMma)) goto drain;
+    q_ph ^= 1u;
     tc_fence_after();
     uint32_t o_ready = 0;  // bit h: O_h holds this task's partial sum
-    // bit h of `act`: Q tile h needs the K/V tile (neighbourhood masks: the
-    // cursor's flags; others: the tile test itself)
+    // The next K/V tile after `from` and, in `act`, the Q tiles that need it
+    // (bit h). Unmasked: every tile of the segment, for every live Q tile.
+    // Neighbourhood masks: the cursor's search; others: the tile test.
     TileCursor<MASK> cur(band, 2);
+    const uint32_t live = (tk.live[0] ? 1u : 0u) | (tk.live[1] ? 2u : 0u);
     auto step = [&](int from, uint32_t& act) -> int {
-      if constexpr (kNa) {
+      if constexpr (MASK == kMaskNone) {
+        act = live;
+        return from + 1;
+      } else if constexpr (kNa) {
         bool a[2];
         const int t = cur.next(tk, sg.kv1, a, p);
         act = (a[0] ? 1u : 0u) | (a[1] ? 2u : 0u);
@@ -1157,62 +1205,63 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
     uint32_t aj = 0, an = 0;
     int j = step(sg.kv0 - 1, aj);
     if (j < sg.kv1) {
-      const int ks = static_cast<int>(k_it % C::kKStages);
-      if (!ctl_wait(bars.k_full(ks), (k_it / C::kKStages) & 1u, ctl, j, kRoleMma)) goto drain;
+      if (!ctl_wait(bars.k_full(kr.s), kr.ph, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
+      const uint64_t kd = dsc.k0 + kr.s * Descs<D>::kStageStep;
+#pragma unroll
       for (int h = 0; h < 2; ++h)
         if ((aj >> h) & 1u) {
-          issue_s<D>(tmem, h, sbase + C::kOffQ + h * C::kTileBytes,
-                     sbase + C::kOffK + ks * C::kTileBytes);
+          issue_s<D>(tmem + C::tm_s(h), h ? dsc.q1 : dsc.q0, kd);
           mma_commit(bars.s_full(h));
         }
-      mma_commit(bars.k_empty(ks));
-      ++k_it;
+      mma_commit(bars.k_empty(kr.s));
+      kr.advance();
     }
     while (j < sg.kv1) {
       const int jn = step(j, an);
       const bool has_next = jn < sg.kv1;
       if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
-      const int vs = static_cast<int>(v_it % C::kVStages);
-      if (!ctl_wait(bars.v_full(vs), (v_it / C::kVStages) & 1u, ctl, j, kRoleMma)) goto drain;
+      if (!ctl_wait(bars.v_full(vr.s), vr.ph, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
-      const uint32_t v_tile = sbase + C::kOffV + vs * C::kTileBytes;
-      int ksn = -1;
+      const uint64_t vd = dsc.v0 + vr.s * Descs<D>::kStageStep;
+      bool k_taken = false;
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         if ((aj >> h) & 1u) {
           if (!((o_ready >> h) & 1u)) {
             if (!ctl_wait(bars.o_empty(h), ((o_par >> h) & 1u) ^ 1u, ctl, j, kRoleMma)) goto drain;
           }
           const uint32_t par = (p_par >> h) & 1u;
+#pragma unroll
           for (int part = 0; part < 2; ++part) {
             if (!ctl_wait(bars.p_full(h, part), par, ctl, j, kRoleMma)) goto drain;
             tc_fence_after();
-            issue_pv<D>(tmem, h, v_tile, ((o_ready >> h) & 1u) != 0u || part > 0, part);
+            issue_pv<D>(tmem + C::tm_o(h), tmem + C::tm_p(h), vd, part,
+                        (((o_ready >> h) & 1u) != 0u || part > 0) ? 1u : 0u);
           }
           p_par ^= 1u << h;
           o_ready |= 1u << h;
         }
         if (has_next && ((an >> h) & 1u)) {
-          if (ksn < 0) {
-            ksn = static_cast<int>(k_it % C::kKStages);
-            if (!ctl_wait(bars.k_full(ksn), (k_it / C::kKStages) & 1u, ctl, jn, kRoleMma))
-              goto drain;
+          if (!k_taken) {
+            if (!ctl_wait(bars.k_full(kr.s), kr.ph, ctl, jn, kRoleMma)) goto drain;
             tc_fence_after();
+            k_taken = true;
           }
-          issue_s<D>(tmem, h, sbase + C::kOffQ + h * C::kTileBytes,
-                     sbase + C::kOffK + ksn * C::kTileBytes);
+          issue_s<D>(tmem + C::tm_s(h), h ? dsc.q1 : dsc.q0, dsc.k0 + kr.s * Descs<D>::kStageStep);
           mma_commit(bars.s_full(h));
         }
       }
-      mma_commit(bars.v_empty(vs));
-      ++v_it;
-      if (ksn >= 0) {
-        mma_commit(bars.k_empty(ksn));
-        ++k_it;
+      mma_commit(bars.v_empty(vr.s));
+      vr.advance();
+      if (k_taken) {
+        mma_commit(bars.k_empty(kr.s));
+        kr.advance();
       }
       j = jn;
       aj = an;
     }
+#pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (!tk.live[h]) continue;
       if (!((o_ready >> h) & 1u)) {  // keeps the o_empty phases in step even without a PV
@@ -1238,6 +1287,14 @@ __device__ __forceinline__ void fence_gpu() { asm volatile("fence.acq_rel.gpu;" 
 __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* a) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
+// A 64-bit load with relaxed semantics at GPU scope (an acquire fence after it
+// orders the reads that depend on what it saw).
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
   return v;
 }
 
@@ -1283,9 +1340,11 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   const int lane = threadIdx.x & 31;
   const int quarter = row >> 5;
   const int ctas = gridDim.x;
+  // this warp's quarter of a part slot: [D/4][32 rows] float4, m[32], l[32]
   auto slot_of = [&](int cta, bool head) {
     return p.ws_part +
-           static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2);
+           static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2) +
+           quarter * 32 * (D + 2);
   };
   auto release_o = [&]() {
     tc_fence_before();
@@ -1308,11 +1367,21 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
   // own slot may hold a previous call's data.
   const int stand_in = c_lo != me ? c_lo : c_hi;
   unsigned long long* word = p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter;
-  // Every lane reads the arrival word with acquire semantics (one broadcast
-  // load), before O is complete: the read overlaps the last P V.
-  const unsigned long long w0 = ld_acquire_gpu(word);
-  const uint32_t seen = static_cast<uint32_t>(w0 >> 32) == p.epoch ? static_cast<uint32_t>(w0) : 0u;
-  const bool claim = seen + 1u == n_parts;
+  // Every lane reads the arrival word (relaxed, one broadcast load) before O
+  // is complete, so the read overlaps the last P V; if every other part is
+  // in, an acquire fence orders the reads of those parts after it.
+  const unsigned long long w0 = ld_relaxed_gpu(word);
+  uint32_t seen = static_cast<uint32_t>(w0 >> 32) == p.epoch ? static_cast<uint32_t>(w0) : 0u;
+  bool claim = seen + 1u == n_parts;
+  if (!claim && sg.kv0 == 0) {
+    // The first part of its task is this CTA's last segment, and the task's
+    // other parts began earlier (at their CTAs' starts): read again, now
+    // that this part is complete, before handing it on.
+    const unsigned long long w1 = ld_relaxed_gpu(word);
+    seen = static_cast<uint32_t>(w1 >> 32) == p.epoch ? static_cast<uint32_t>(w1) : 0u;
+    claim = seen + 1u == n_parts;
+  }
+  if (claim) fence_gpu();
   const int q = tk.q0[hh] + row;
   const bool row_ok = q < p.Nq;
   __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
@@ -1321,13 +1390,13 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     // The usual cut: the other part is complete; fetch its m, l and its
     // first 64 columns of O while the last P V finishes, then merge.
     const float* sl = part(stand_in);
-    const float mi = __ldcg(sl + 128 * D + row);
-    const float li = __ldcg(sl + 128 * D + 128 + row);
+    const float mi = __ldcg(sl + 32 * D + lane);
+    const float li = __ldcg(sl + 32 * D + 32 + lane);
     constexpr int kPre = D < 64 ? D / 4 : 16;  // float4 columns fetched ahead
     const float4* src = reinterpret_cast<const float4*>(sl);
     float4 pre[kPre];
 #pragma unroll
-    for (int i = 0; i < kPre; ++i) pre[i] = __ldcg(src + i * 128 + row);
+    for (int i = 0; i < kPre; ++i) pre[i] = __ldcg(src + i * 32 + lane);
     if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return false;
     o_par ^= 1u;
     tc_fence_after();
@@ -1346,7 +1415,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
       float4 v[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        v[i] = ch * 8 + i < kPre ? pre[(ch * 8 + i) % kPre] : __ldcg(src + (ch * 8 + i) * 128 + row);
+        v[i] = ch * 8 + i < kPre ? pre[(ch * 8 + i) % kPre] : __ldcg(src + (ch * 8 + i) * 32 + lane);
       if (row_ok) {
         auto mix = [&](float own, float oth) {
           return __fmaf_rn(w_hi, me_lo ? oth : own, __fmul_rn(w_lo, me_lo ? own : oth)) * inv_L;
@@ -1384,12 +1453,12 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
       tmem_ld32(t_o + ch * 32, ov);
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        mine4[(ch * 8 + i) * 128 + row] =
+        mine4[(ch * 8 + i) * 32 + lane] =
             make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
                         __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
     }
-    mine[128 * D + row] = m_ref;
-    mine[128 * D + 128 + row] = l;
+    mine[32 * D + lane] = m_ref;
+    mine[32 * D + 32 + lane] = l;
     fence_gpu();
     __syncwarp();
     uint32_t n = 0;
@@ -1412,8 +1481,8 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
     for (int u = 0; u < 8; ++u) {
       const int c = c_lo + u;
       const float* sl = part(c <= c_hi && c != me ? c : stand_in);
-      mi[u] = __ldcg(sl + 128 * D + row);
-      li[u] = __ldcg(sl + 128 * D + 128 + row);
+      mi[u] = __ldcg(sl + 32 * D + lane);
+      li[u] = __ldcg(sl + 32 * D + 32 + lane);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
@@ -1430,7 +1499,7 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + u;
-        mi[u] = __ldcg(part(c <= c_hi && c != me ? c : stand_in) + 128 * D + row);
+        mi[u] = __ldcg(part(c <= c_hi && c != me ? c : stand_in) + 32 * D + lane);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -1442,8 +1511,8 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
       for (int u = 0; u < 8; ++u) {
         const int c = c0 + u;
         const float* sl = part(c <= c_hi && c != me ? c : stand_in);
-        mi[u] = __ldcg(sl + 128 * D + row);
-        li[u] = __ldcg(sl + 128 * D + 128 + row);
+        mi[u] = __ldcg(sl + 32 * D + lane);
+        li[u] = __ldcg(sl + 32 * D + 32 + lane);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -1477,11 +1546,11 @@ __device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars&
         const int c = c0 + u;
         const bool in = c <= c_hi && c != me;
         const float* sl = part(in ? c : stand_in);
-        const float mi = __ldcg(sl + 128 * D + row);
+        const float mi = __ldcg(sl + 32 * D + lane);
         wgt[u] = c == me ? w_me : (in && mi != -CUDART_INF_F) ? ex2(mi - M) : 0.f;
         const float4* src = reinterpret_cast<const float4*>(sl);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 128 + row);
+        for (int i = 0; i < 8; ++i) v[u][i] = __ldcg(src + (ch * 8 + i) * 32 + lane);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -1592,6 +1661,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     const int q = q0 + row;
     // neighbourhood: this query's grid coordinates and window starts
     const NaQuery nq = na_query<MASK>(p, q);
+    const bool cut = MASK == kMaskNone && p.split && (sg.kv0 > 0 || sg.kv1 < p.n_kv);
     float m_ref = -CUDART_INF_F;  // running maximum in log2 units (possibly stale by < 2^8)
     float l = 0.f;                // running row sum relative to m_ref
     bool first = true;
@@ -1652,7 +1722,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
       first = false;
     }
     // epilogue: O / l, bf16 store, log-sum-exp
-    if (MASK == kMaskNone && p.split && (sg.kv0 > 0 || sg.kv1 < p.n_kv)) {
+    if (cut) {
       if (!partial_epilogue<D>(p, bars, sg, tk, hh, row, t_o, m_ref, l, cta_lo, o_par, ctl)) return;
       continue;
     }
@@ -1710,9 +1780,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * bars.count());
   volatile uint32_t* abort_flag = tmem_slot + 1;
   int64_t* cta_lo = reinterpret_cast<int64_t*>(smem + C::kOffTbl);
-  if (MASK == kMaskNone && p.split)
+  if (MASK == kMaskNone && p.split) {
     for (int c = threadIdx.x; c <= static_cast<int>(gridDim.x); c += blockDim.x)
       cta_lo[c] = unit_lo(p.units, gridDim.x, c);  // ordered by the __syncthreads below
+    if (threadIdx.x == 0) {
+      const int64_t u0 = unit_lo(p.units, gridDim.x, blockIdx.x);
+      const int64_t t0 = u0 / p.n_kv;
+      cta_lo[kMaxSplitCtas + 1] = (t0 << 32) | (u0 - t0 * p.n_kv);
+    }
+  }
 
   if (threadIdx.x == 0) {
     mbar_init(bars.q_full(), 1);
