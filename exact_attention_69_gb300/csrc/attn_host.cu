@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -317,6 +318,74 @@ int encode_map(CUtensorMap* m, const void* base, int d, int N, int H, int B, con
   return ATTN_OK;
 }
 
+// The kernel parameters of a validated call: tensor maps, output and shapes,
+// the mask fields (returns the kernel's mask variant in *mask), the plan's
+// schedule and the timeout and test hook. Workspace, epoch and status are
+// left for the caller (the regular and the no-alloc entry points differ
+// there and only there).
+int fill_params(const attn_params_ex* p, const Checked& c, const Plan& pl, attn::KernelParams* kp,
+                int* mask) {
+  std::memset(kp, 0, sizeof(*kp));
+  const int box_cols = p->d >= 64 ? 64 : 32;
+  const CUtensorMapSwizzle swz = p->d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  int rc;
+  if ((rc = encode_map(&kp->tm_q, p->q, p->d, p->Nq, p->H, p->B, c.qs, box_cols, swz, "q")) != ATTN_OK ||
+      (rc = encode_map(&kp->tm_k, p->k, p->d, p->Nk, p->H, p->B, c.ks, box_cols, swz, "k")) != ATTN_OK ||
+      (rc = encode_map(&kp->tm_v, p->v, p->d, p->Nk, p->H, p->B, c.vs, box_cols, swz, "v")) != ATTN_OK)
+    return rc;
+  kp->o = p->o;
+  kp->lse = p->lse;
+  kp->o_sb = c.os[0];
+  kp->o_sh = c.os[1];
+  kp->o_sn = c.os[2];
+  kp->B = p->B;
+  kp->H = p->H;
+  kp->Nq = p->Nq;
+  kp->Nk = p->Nk;
+  kp->c = p->scale * 1.4426950408889634f;
+  *mask = kernel_mask(p, c, kp);
+  kp->n_qpairs = pl.n_qpairs;
+  kp->n_kv = pl.n_kv;
+  kp->n_tasks = pl.n_tasks;
+  kp->split = pl.split;
+  kp->units = pl.units;
+  kp->timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
+  kp->inject = p->inject;
+  return ATTN_OK;
+}
+
+// ATTN_LOG=1 in the environment: one line on stderr per launch, naming the
+// kernel specialisation and the schedule.
+bool log_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("ATTN_LOG");
+    return e != nullptr && e[0] != '\0' && e[0] != '0';
+  }();
+  return on;
+}
+
+const char* mask_name(int mask_kind) {
+  switch (mask_kind) {
+    case ATTN_MASK_NONE: return "none";
+    case ATTN_MASK_CAUSAL: return "causal";
+    case ATTN_MASK_CAUSAL_BR: return "causal_br";
+    case ATTN_MASK_NA2D: return "na2d";
+    case ATTN_MASK_NA3D: return "na3d";
+    default: return "?";
+  }
+}
+
+void log_launch(const char* entry, const attn_params_ex* p, const attn::KernelParams& kp, int mask,
+                const Plan& pl) {
+  if (!log_enabled()) return;
+  std::fprintf(stderr,
+               "%s: d=%d mask=%s variant=%d B=%d H=%d Nq=%d Nk=%d grid_hw=%dx%d window=%dx%d "
+               "dilation=%d wrap=%d schedule=%s grid=%d tasks=%d units=%lld\n",
+               entry, p->d, mask_name(p->mask_kind), mask, p->B, p->H, p->Nq, p->Nk, kp.grid_h,
+               kp.grid_w, kp.window_h, kp.window_w, kp.dilation, kp.na_wrap,
+               pl.split ? "split" : "whole", pl.grid, pl.n_tasks, static_cast<long long>(pl.units));
+}
+
 // Device pointers of the call's workspace: the caller's, or the library's own
 // (grown, and zero-filled, when too small). Also hands out the call's epoch.
 int acquire_workspace(const attn_params_ex* p, const Plan& pl, DeviceState* ds, void** ws,
@@ -353,6 +422,12 @@ int acquire_workspace(const attn_params_ex* p, const Plan& pl, DeviceState* ds, 
   return ATTN_OK;
 }
 
+// Reads and clears the no-alloc entry point's status word on device `dev`
+// (zeros if that entry point was not used there), and forgets its per-device
+// state (under g_mu); defined with it below.
+int noalloc_take_status(int dev, uint32_t word[4]);
+void noalloc_forget();
+
 }  // namespace
 
 extern "C" {
@@ -371,33 +446,11 @@ int attn_fwd_ex(const attn_params_ex* p) {
   if ((rc = get_encoder()) != ATTN_OK) return rc;
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-
-  attn::KernelParams kp;
-  std::memset(&kp, 0, sizeof(kp));
-  const int box_cols = p->d >= 64 ? 64 : 32;
-  const CUtensorMapSwizzle swz = p->d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if ((rc = encode_map(&kp.tm_q, p->q, p->d, p->Nq, p->H, p->B, c.qs, box_cols, swz, "q")) != ATTN_OK ||
-      (rc = encode_map(&kp.tm_k, p->k, p->d, p->Nk, p->H, p->B, c.ks, box_cols, swz, "k")) != ATTN_OK ||
-      (rc = encode_map(&kp.tm_v, p->v, p->d, p->Nk, p->H, p->B, c.vs, box_cols, swz, "v")) != ATTN_OK)
-    return rc;
-  kp.o = p->o;
-  kp.lse = p->lse;
-  kp.o_sb = c.os[0];
-  kp.o_sh = c.os[1];
-  kp.o_sn = c.os[2];
-  kp.B = p->B;
-  kp.H = p->H;
-  kp.Nq = p->Nq;
-  kp.Nk = p->Nk;
-  kp.c = p->scale * 1.4426950408889634f;
-  const int mask = kernel_mask(p, c, &kp);
   Plan pl;
   if ((rc = make_plan(p, ds->sm_count, &pl)) != ATTN_OK) return rc;
-  kp.n_qpairs = pl.n_qpairs;
-  kp.n_kv = pl.n_kv;
-  kp.n_tasks = pl.n_tasks;
-  kp.split = pl.split;
-  kp.units = pl.units;
+  attn::KernelParams kp;
+  int mask = 0;
+  if ((rc = fill_params(p, c, pl, &kp, &mask)) != ATTN_OK) return rc;
   if (pl.split) {
     void* ws = nullptr;
     if ((rc = acquire_workspace(p, pl, ds, &ws, &kp.epoch)) != ATTN_OK) return rc;
@@ -405,20 +458,17 @@ int attn_fwd_ex(const attn_params_ex* p) {
     kp.ws_count = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) +
                                                          align256(pl.part_bytes));
   }
-  kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
-  kp.inject = p->inject;
   kp.status = ds->status;
-
-  const int grid = pl.grid;
+  log_launch("attn_fwd", p, kp, mask, pl);
 
   cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
   cudaError_t e;
   if (p->ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_start), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(start)");
   switch (p->d) {
-    case 32: e = attn::launch_d32(kp, mask, grid, s); break;
-    case 64: e = attn::launch_d64(kp, mask, grid, s); break;
-    default: e = attn::launch_d128(kp, mask, grid, s); break;
+    case 32: e = attn::launch_d32(kp, mask, pl.grid, s); break;
+    case 64: e = attn::launch_d64(kp, mask, pl.grid, s); break;
+    default: e = attn::launch_d128(kp, mask, pl.grid, s); break;
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   if (p->ev_stop && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_stop), s)) != cudaSuccess)
@@ -455,14 +505,29 @@ int attn_set_stream(void* stream) {
 
 int attn_get_device_status(uint32_t* detail) {
   t_err[0] = 0;
-  DeviceState* ds = nullptr;
-  int rc = device_state(&ds);
-  if (rc != ATTN_OK) return rc;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "device ordinal %d out of range", dev);
+  // Reads the status words that exist on this device and allocates nothing:
+  // the library's own (created by the first attn_fwd_ex or attn_bwd) and the
+  // no-alloc entry point's (inside its fixed array). The first failure wins.
+  uint32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    status = g_dev[dev].status;
+  }
   uint32_t word[4] = {0, 0, 0, 0};
-  cudaError_t e = cudaMemcpy(word, ds->status, sizeof(word), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
-  if (word[0] != 0 && (e = cudaMemset(ds->status, 0, sizeof(word))) != cudaSuccess)
-    return cuda_fail(e, "cudaMemset(status)");
+  if (status != nullptr) {
+    if ((e = cudaMemcpy(word, status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy(status)");
+    if (word[0] != 0 && (e = cudaMemset(status, 0, sizeof(word))) != cudaSuccess)
+      return cuda_fail(e, "cudaMemset(status)");
+  }
+  uint32_t word2[4] = {0, 0, 0, 0};
+  int rc = noalloc_take_status(dev, word2);
+  if (rc != ATTN_OK) return rc;
+  if (word[0] == 0) std::memcpy(word, word2, sizeof(word));
   if (detail) std::memcpy(detail, word, sizeof(word));
   if (word[0] == 0) return ATTN_OK;
   if (word[0] == ATTN_ERR_TIMEOUT)
@@ -563,6 +628,7 @@ int attn_tune(const attn_params_ex* p, int iters, attn_tune_result* out) {
 
 void attn_shutdown(void) {
   std::lock_guard<std::mutex> lk(g_mu);
+  noalloc_forget();  // the next no-alloc call looks the array's address up again
   for (int i = 0; i < kMaxDevices; ++i) {
     if (g_dev[i].status) {
       int prev = 0;
@@ -733,12 +799,14 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 struct NoAllocDevice {
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int sm_count = 0;
-  uint32_t epoch = 0;                // tag of the last call on this device
+  uint32_t epoch = 0;                // tag of the last call on this device (never reset: the
+                                     // array keeps earlier calls' arrival words)
 };
 NoAllocDevice g_noalloc[kMaxDevices];
 
-// Once per device, with that device current: the device address of the
-// scratch array (the symbol name itself is only a host-side stand-in).
+// Once per device (again after attn_shutdown), with that device current: the
+// device address of the scratch array (the symbol name itself is only a
+// host-side stand-in).
 int noalloc_setup(NoAllocDevice** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -763,6 +831,30 @@ int noalloc_setup(NoAllocDevice** out) {
   }
   *out = &d;
   return ATTN_OK;
+}
+
+int noalloc_take_status(int dev, uint32_t word[4]) {
+  word[0] = word[1] = word[2] = word[3] = 0;
+  bool used;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    used = g_noalloc[dev].scratch != nullptr;
+  }
+  if (!used) return ATTN_OK;
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_noalloc_scratch, 4 * sizeof(uint32_t), 0,
+                                       cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(no-alloc status)");
+  if (word[0] != 0) {
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    if ((e = cudaMemcpyToSymbol(g_noalloc_scratch, zero, sizeof(zero), 0,
+                                cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpyToSymbol(no-alloc status)");
+  }
+  return ATTN_OK;
+}
+
+void noalloc_forget() {
+  for (int i = 0; i < kMaxDevices; ++i) g_noalloc[i].scratch = nullptr;
 }
 
 }  // namespace
@@ -791,30 +883,8 @@ extern "C" int attn_fwd_noalloc(const attn_params_ex* p) {
                 need, kNoAllocScratchBytes);
 
   attn::KernelParams kp;
-  std::memset(&kp, 0, sizeof(kp));
-  const int box_cols = p->d >= 64 ? 64 : 32;
-  const CUtensorMapSwizzle swz = p->d >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if ((rc = encode_map(&kp.tm_q, p->q, p->d, p->Nq, p->H, p->B, c.qs, box_cols, swz, "q")) != ATTN_OK ||
-      (rc = encode_map(&kp.tm_k, p->k, p->d, p->Nk, p->H, p->B, c.ks, box_cols, swz, "k")) != ATTN_OK ||
-      (rc = encode_map(&kp.tm_v, p->v, p->d, p->Nk, p->H, p->B, c.vs, box_cols, swz, "v")) != ATTN_OK)
-    return rc;
-  kp.o = p->o;
-  kp.lse = p->lse;
-  kp.o_sb = c.os[0];
-  kp.o_sh = c.os[1];
-  kp.o_sn = c.os[2];
-  kp.B = p->B;
-  kp.H = p->H;
-  kp.Nq = p->Nq;
-  kp.Nk = p->Nk;
-  kp.c = p->scale * 1.4426950408889634f;
-  kp.n_qpairs = pl.n_qpairs;
-  kp.n_kv = pl.n_kv;
-  kp.n_tasks = pl.n_tasks;
-  kp.split = pl.split;
-  kp.units = pl.units;
-  kp.timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
-  kp.inject = p->inject;
+  int mask = 0;
+  if ((rc = fill_params(&split, c, pl, &kp, &mask)) != ATTN_OK) return rc;
   // Layout of the scratch: status word, partial results, arrival words. The
   // arrival words carry each call's tag, so nothing has to be cleared between
   // calls (the array starts zeroed, and tag 0 is never used).
@@ -829,14 +899,15 @@ extern "C" int attn_fwd_noalloc(const attn_params_ex* p) {
     if (++nd->epoch == 0) nd->epoch = 1;
     kp.epoch = nd->epoch;
   }
+  log_launch("attn_fwd_noalloc", p, kp, mask, pl);
   cudaStream_t s = p->stream ? static_cast<cudaStream_t>(p->stream) : t_stream;
   cudaError_t e;
   if (p->ev_start && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_start), s)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord(start)");
   switch (p->d) {
-    case 32: e = attn::launch_d32(kp, attn::kMaskNone, pl.grid, s); break;
-    case 64: e = attn::launch_d64(kp, attn::kMaskNone, pl.grid, s); break;
-    default: e = attn::launch_d128(kp, attn::kMaskNone, pl.grid, s); break;
+    case 32: e = attn::launch_d32(kp, mask, pl.grid, s); break;
+    case 64: e = attn::launch_d64(kp, mask, pl.grid, s); break;
+    default: e = attn::launch_d128(kp, mask, pl.grid, s); break;
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   if (p->ev_stop && (e = cudaEventRecord(static_cast<cudaEvent_t>(p->ev_stop), s)) != cudaSuccess)

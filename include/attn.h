@@ -79,6 +79,11 @@
  * argument checks happen on the host before any CUDA call, so an invalid call
  * touches no device state. attn_last_error() gives a one-line message for
  * the calling thread's last failure.
+ *
+ * Logging: with ATTN_LOG=1 in the environment, every forward launch writes one
+ * line to stderr: the entry point, head dimension, mask and kernel variant,
+ * shapes, the neighbourhood parameters and the schedule (whole tasks or split,
+ * persistent grid size, tasks, K/V-tile units).
  */
 #ifndef EXACT_ATTENTION_69_ATTN_H
 #define EXACT_ATTENTION_69_ATTN_H
@@ -179,11 +184,14 @@ int attn_fwd_ex(const attn_params_ex* p);
  * the calling thread's later attn_fwd calls. Thread-local; always ATTN_OK. */
 int attn_set_stream(void* stream);
 
-/* Read and clear the current device's status word. Call after synchronising
- * the stream of the calls in question. Returns ATTN_OK, ATTN_ERR_TIMEOUT, or
- * ATTN_ERR_CUDA if the word could not be read. If detail is not NULL it
- * receives 4 words: code, role (0 loader, 1 MMA issuer, 2 softmax), KV tile
- * index, CTA index of the first failure. */
+/* Read and clear the current device's status words: the library's own (used
+ * by attn_fwd, attn_fwd_ex, attn_bwd) and the one inside attn_fwd_noalloc's
+ * fixed array. Allocates nothing (a word that does not exist yet reads as
+ * zero). Call after synchronising the stream of the calls in question.
+ * Returns ATTN_OK, ATTN_ERR_TIMEOUT, or ATTN_ERR_CUDA if a word could not be
+ * read. If detail is not NULL it receives 4 words: code, role (0 loader, 1
+ * MMA issuer, 2 softmax), KV tile index, CTA index of the first failure (the
+ * library's own word first). */
 int attn_get_device_status(uint32_t* detail);
 
 /* Static one-line description of a status code. */
@@ -219,7 +227,11 @@ typedef struct attn_tune_result {
 
 int attn_tune(const attn_params_ex* p, int iters, attn_tune_result* out);
 
-/* Free the library's per-device state (status words). Later calls re-create it. */
+/* Free the library's per-device state (status words, workspaces, the
+ * backward's stream and scratch) and forget the no-alloc array's device
+ * addresses. Later calls re-create it; the first attn_fwd_noalloc call on a
+ * device after this looks the address up again, so it too must come before
+ * any stream capture. */
 void attn_shutdown(void);
 
 /* ATTN_ABI_VERSION of the built library. */
@@ -293,8 +305,8 @@ int attn_bwd(const attn_bwd_params* p);
  *  - All calls on a device share its array and each overwrites what the last
  *    one left. Calls that overlap on the GPU (e.g. on two streams at once)
  *    race and give wrong results: serialise them.
- *  - A device-side wait that runs out is recorded only in the array's own
- *    status word, which attn_get_device_status does not read.
+ *  - A device-side wait that runs out is recorded in the array's own status
+ *    word; attn_get_device_status reads and clears it (allocating nothing).
  */
 int attn_fwd_noalloc(const attn_params_ex* p);
 

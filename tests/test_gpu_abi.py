@@ -1,0 +1,151 @@
+"""The named C entry point on the GPU, and one kernel launch per call.
+
+attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, mask_kind, window, dilation,
+wrap) is the op boundary (the NATTEN issue #142 thread calls its library's
+forward the same way: output, q, k, v, log-sum-exp, window, dilation, ...).
+It is called here through ctypes, on a stream set with attn_set_stream, and
+compared with the fp64 oracle. "Profiling in PyTorch" part 3 shows the fused
+backends as a single kernel per attention call; a stream capture of one call
+(the graph it records holds a single kernel node) asserts the same of this
+library.
+"""
+import ctypes
+import math
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from seeded_inputs import make_qkv, to_f64
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL, LSE_TOL = 1e-2, 1e-2, 1e-3
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_69_gb300 import _lib, build
+    build.build()
+    return _lib
+
+
+def _check(o, lse, ref_o, ref_lse):
+    o = o.float().cpu().numpy().astype(np.float64)
+    err = np.abs(o - ref_o)
+    assert (err <= ATOL + RTOL * np.abs(ref_o)).all(), f"O max err {err.max():.3e}"
+    if lse is not None:
+        lerr = np.abs(lse.cpu().numpy().astype(np.float64) - ref_lse).max()
+        assert lerr <= LSE_TOL, f"LSE max err {lerr:.3e}"
+
+
+CASES = [  # (mask name, mask code, window, wrap, B, H, N, d)
+    ("none", 0, 0, 0, 2, 3, 1000, 64),
+    ("causal", 1, 0, 0, 1, 4, 777, 128),
+    ("clamp", 2, 7, 0, 1, 2, 32 * 32, 32),
+    ("wrap", 2, 5, 1, 2, 1, 24 * 24, 64),
+]
+
+
+@pytest.mark.parametrize("with_lse", [True, False])
+@pytest.mark.parametrize("name,code,window,wrap,B,H,N,d", CASES)
+def test_named_entry_point_on_a_stream(lib, name, code, window, wrap, B, H, N, d, with_lse):
+    """attn_fwd with the calling thread's stream set to a non-default stream;
+    the stream is then joined and the results compared with the oracle."""
+    q, k, v = make_qkv(B, H, N, N, d, 1.0, 900 + N + d)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o = torch.full_like(qc, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), device="cuda") if with_lse else None
+    scale = 1.0 / math.sqrt(d)
+    L = lib.load()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    try:
+        assert L.attn_set_stream(ctypes.c_void_p(side.cuda_stream)) == lib.ATTN_OK
+        rc = L.attn_fwd(qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), o.data_ptr(),
+                        lse.data_ptr() if with_lse else None, B, H, N, N, d, ctypes.c_float(scale),
+                        code, window, 1, wrap)
+        lib.check(rc, "attn_fwd")
+    finally:
+        L.attn_set_stream(None)
+    side.synchronize()
+    code_, detail = lib.device_status()
+    assert code_ == 0, detail
+    ref_o, ref_lse = oracle.attention(to_f64(q), to_f64(k), to_f64(v), scale=scale,
+                                      mask_kind=name, window=window)
+    _check(o, lse, ref_o, ref_lse)
+
+
+def test_named_entry_point_rejects_a_non_square_grid(lib):
+    """NA through the named call infers a square grid; 1000 tokens are not one."""
+    q = torch.empty(8, dtype=torch.bfloat16, device="cuda")
+    rc = lib.load().attn_fwd(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), None,
+                             1, 1, 1000, 1000, 64, ctypes.c_float(0.125), 2, 7, 1, 0)
+    assert rc == lib.ATTN_ERR_INVALID_ARG
+
+
+def _captured_kernel_nodes(call, stream):
+    """Kernel nodes of a CUDA graph captured (driver API, thread-local mode)
+    around call() on `stream`: (count of kernel nodes, count of all nodes)."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    h = ctypes.c_void_p(stream.cuda_stream)
+    assert cu.cuStreamBeginCapture_v2(h, 1) == 0  # CU_STREAM_CAPTURE_MODE_THREAD_LOCAL
+    try:
+        call()
+    finally:
+        graph = ctypes.c_void_p()
+        rc = cu.cuStreamEndCapture(h, ctypes.byref(graph))
+    assert rc == 0, f"cuStreamEndCapture returned {rc}"
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * max(n.value, 1))()
+    assert cu.cuGraphGetNodes(graph, nodes, ctypes.byref(n)) == 0
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kernels += t.value == 0  # CU_GRAPH_NODE_TYPE_KERNEL
+    cu.cuGraphDestroy(graph)
+    return kernels, n.value
+
+
+@pytest.mark.parametrize("B,H,N,d,kw", [
+    (2, 5, 4096, 64, dict()),                            # split schedule: cut tasks merged in-kernel
+    (1, 2, 1000, 128, dict(mask="causal")),
+    (1, 2, 1024, 32, dict(mask="wrap", window=7)),
+])
+def test_one_kernel_launch_per_call(lib, B, H, N, d, kw):
+    """Every forward call is exactly one kernel launch (no memsets, no merge or
+    reduction kernels): a stream capture of one call holds one node, a kernel."""
+    import exact_attention_69_gb300 as E
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, N, d, 1.0, 60 + d))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        E.attn_fwd(q, k, v, out=o, lse=lse, stream=s, **kw)  # first-use allocations happen here
+    s.synchronize()
+    kernels, nodes = _captured_kernel_nodes(
+        lambda: E.attn_fwd(q, k, v, out=o, lse=lse, stream=s, **kw), s)
+    assert (kernels, nodes) == (1, 1)
+
+
+def test_attn_log_reports_the_launch():
+    """ATTN_LOG=1: one line on stderr per launch with the specialisation and
+    the schedule."""
+    code = ("import torch, exact_attention_69_gb300 as E; from seeded_inputs import make_qkv; "
+            "q,k,v=[t.cuda() for t in make_qkv(1,2,1000,1000,64,1.0,5)]; "
+            "E.attn_fwd(q,k,v); E.attn_fwd(q,k,v,mask='causal'); torch.cuda.synchronize()")
+    env = dict(os.environ, ATTN_LOG="1", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stderr.splitlines() if ln.startswith("attn_fwd:")]
+    assert len(lines) == 2, r.stderr
+    assert "d=64" in lines[0] and "mask=none" in lines[0] and "grid=" in lines[0]
+    assert "mask=causal" in lines[1] and "schedule=whole" in lines[1]

@@ -3,7 +3,11 @@ memory (code inside an allocator or memory pool, or an embedded runtime that
 owns every allocation). It keeps its scratch in a fixed array inside the
 library; here it is called through the C ABI and its outputs are compared with
 those of the regular entry point, on two calls in a row with different inputs
-(the second call runs over whatever the first left in the shared scratch).
+(the second call runs over whatever the first left in the shared scratch), and
+with the fp64 oracle directly; a large call followed by smaller ones checks
+that what one call leaves in the shared array does not leak into the next;
+an injected stall checks that its bounded waits report through
+attn_get_device_status.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
@@ -15,7 +19,8 @@ import numpy as np
 import pytest
 import torch
 
-from seeded_inputs import make_qkv
+import oracle
+from seeded_inputs import make_qkv, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -102,3 +107,69 @@ def test_noalloc_rejects_masks(lib):
     p.scale = 0.1
     p.mask_kind = lib.ATTN_MASK_CAUSAL
     assert lib.load().attn_fwd_noalloc(ctypes.byref(p)) == lib.ATTN_ERR_INVALID_ARG
+
+
+def _close_oracle(o, lse, q, k, v):
+    ref_o, ref_lse = oracle.attention(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()),
+                                      scale=1.0 / math.sqrt(q.shape[-1]))
+    err = np.abs(o.float().cpu().numpy() - ref_o)
+    assert (err <= ATOL + RTOL * np.abs(ref_o)).all(), f"O max err {err.max():.3e}"
+    lerr = np.abs(lse.cpu().numpy() - ref_lse).max()
+    assert lerr <= LSE_TOL, f"LSE max err {lerr:.3e}"
+
+
+@pytest.mark.parametrize("shape,num_ctas", [((1, 2, 700, 900, 64), 5), ((2, 1, 513, 1025, 32), 0),
+                                            ((1, 1, 300, 2000, 128), 7)])
+def test_noalloc_matches_the_oracle(lib, shape, num_ctas):
+    B, H, Nq, Nk, d = shape
+    q, k, v = (t.cuda() for t in make_qkv(B, H, Nq, Nk, d, 1.0, 300 + Nq))
+    o, lse = _noalloc(lib, q, k, v, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    assert lib.device_status()[0] == 0
+    _close_oracle(o, lse, q, k, v)
+
+
+def test_noalloc_large_then_small_calls(lib):
+    """A large call (many tasks, every SM, parts and arrival words all over the
+    array) followed by smaller problems with other task counts and grids: each
+    call must see only its own arrivals and parts."""
+    import exact_attention_69_gb300 as E
+    seq = [((2, 8, 4096, 4096, 64), 0), ((1, 1, 512, 4096, 64), 20), ((1, 3, 300, 700, 64), 3),
+           ((2, 8, 4096, 4096, 64), 0), ((1, 1, 256, 1024, 64), 9)]
+    for i, ((B, H, Nq, Nk, d), nc) in enumerate(seq):
+        q, k, v = (t.cuda() for t in make_qkv(B, H, Nq, Nk, d, 1.0, 400 + i))
+        o, lse = _noalloc(lib, q, k, v, num_ctas=nc)
+        ref_o, ref_lse = E.attn_fwd(q, k, v)
+        torch.cuda.synchronize()
+        assert lib.device_status()[0] == 0
+        _close(o, lse, ref_o, ref_lse)
+        if Nq * Nk <= 700 * 700:
+            _close_oracle(o, lse, q, k, v)
+
+
+def test_noalloc_bounded_wait_is_reported(lib):
+    """The loader withholds one K tile: the MMA warp's wait runs out after the
+    short bound, the kernel stops, attn_get_device_status reports the timeout
+    from the fixed array's status word (and clears it), and the next call is
+    correct."""
+    q, k, v = (t.cuda() for t in make_qkv(1, 1, 256, 1024, 64, 1.0, 12))
+    _noalloc(lib, q, k, v, num_ctas=1, timeout_ns=20_000_000, inject=1)
+    torch.cuda.synchronize()
+    code, detail = lib.device_status()
+    assert code == lib.ATTN_ERR_TIMEOUT and detail[0] == lib.ATTN_ERR_TIMEOUT, (code, detail)
+    assert lib.device_status()[0] == 0  # reading cleared it
+    o, lse = _noalloc(lib, q, k, v, num_ctas=3)
+    torch.cuda.synchronize()
+    assert lib.device_status()[0] == 0
+    _close_oracle(o, lse, q, k, v)
+
+
+def test_noalloc_after_shutdown(lib):
+    """attn_shutdown forgets the array's device address; the next call looks it
+    up again and works."""
+    q, k, v = (t.cuda() for t in make_qkv(1, 2, 400, 600, 64, 1.0, 13))
+    lib.load().attn_shutdown()
+    o, lse = _noalloc(lib, q, k, v, num_ctas=4)
+    torch.cuda.synchronize()
+    assert lib.device_status()[0] == 0
+    _close_oracle(o, lse, q, k, v)
