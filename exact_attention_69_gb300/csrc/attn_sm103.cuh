@@ -1329,11 +1329,14 @@ __device__ __forceinline__ uint32_t arrive_part(unsigned long long* w, uint32_t 
 // No CTA waits for another: the last part to finish does the merge, reading
 // its own O from TMEM (o_empty is arrived only at the end, which costs
 // nothing: the next task's first P V also needs this warpgroup's next P).
-// A part is stored column-group major ([d/4][128 rows] of float4, then m[128],
-// l[128]) so that every warp access is one contiguous 512-byte run.
+// A part is stored per 32-row quarter, [d/4][32 rows] of float4, then m[32]
+// and l[32], so that every warp access is one contiguous 512-byte run.
+// Inlined into the softmax loop: as a call, the softmax warps saved their
+// live registers to local memory around it and reloaded them from L2 after
+// the epilogue's stores, measured ~2000 cycles per cut on GB300.
 // False: the CTA is aborting.
 template <int D>
-__device__ __noinline__ bool partial_epilogue(const KernelParams& p, const Bars& bars, const Seg& sg,
+__device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Bars& bars, const Seg& sg,
                                               const Task& tk, int hh, int row, uint32_t t_o,
                                               float m_ref, float l, const int64_t* cta_lo,
                                               uint32_t& o_par, const Ctl& ctl) {
