@@ -1703,6 +1703,9 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
       const float2 c2 = make_float2(c, c), nm2 = make_float2(neg_m, neg_m);
       float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
+      // The first half's store completes while the second half's
+      // exponentials are computed (tcgen05.wait::st waits for every store of
+      // the thread); then each half is announced on its own barrier.
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t pk[32];
@@ -1714,12 +1717,18 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
           sum4[i & 3] = __fadd2_rn(sum4[i & 3], pe);
           pk[i] = pack_bf16(pe.x, pe.y);
         }
+        if (part == 1) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars.p_full(hh, 0));
+        }
         tmem_st32(t_p + 32 * part, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.p_full(hh, part));
       }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars.p_full(hh, 1));
       const float2 sa = __fadd2_rn(sum4[0], sum4[1]), sb = __fadd2_rn(sum4[2], sum4[3]);
       l += (sa.x + sa.y) + (sb.x + sb.y);
       first = false;
