@@ -63,19 +63,25 @@ constexpr int64_t kMinSplitUnits = 4;
 struct Plan {
   int grid = 0;
   int split = 0;
-  int n_qpairs = 0, n_kv = 0, n_tasks = 0;
+  int q_tiles = 2, n_qtasks = 0, n_kv = 0, n_tasks = 0;
   int64_t units = 0;
   size_t part_bytes = 0, count_bytes = 0;
   size_t ws_bytes() const { return split ? align256(part_bytes) + align256(count_bytes) : 0; }
 };
 
 int make_plan(const attn_params_ex* p, int sm_count, Plan* pl) {
-  pl->n_qpairs = (p->Nq + 2 * attn::kBM - 1) / (2 * attn::kBM);
-  pl->n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
-  pl->n_tasks = p->B * p->H * pl->n_qpairs;
-  pl->units = static_cast<int64_t>(pl->n_tasks) * pl->n_kv;
   int ctas = sm_count;
   if (p->num_ctas > 0 && p->num_ctas < ctas) ctas = p->num_ctas;
+  // A task is a pair of Q tiles, whose softmax warpgroups take turns on the
+  // tensor core; a masked launch with fewer pairs than CTAs (small or
+  // neighbourhood problems, never split) gives each task one Q tile instead,
+  // so that twice as many SMs work, each on a shorter chain.
+  const int pairs = p->B * p->H * ((p->Nq + 2 * attn::kBM - 1) / (2 * attn::kBM));
+  pl->q_tiles = (p->mask_kind != ATTN_MASK_NONE && pairs < ctas) ? 1 : 2;
+  pl->n_qtasks = (p->Nq + pl->q_tiles * attn::kBM - 1) / (pl->q_tiles * attn::kBM);
+  pl->n_kv = (p->Nk + attn::kBN - 1) / attn::kBN;
+  pl->n_tasks = p->B * p->H * pl->n_qtasks;
+  pl->units = static_cast<int64_t>(pl->n_tasks) * pl->n_kv;
   if (p->schedule == 2 && p->mask_kind != ATTN_MASK_NONE)
     return fail(ATTN_ERR_INVALID_ARG, "schedule 2 applies to ATTN_MASK_NONE only");
   pl->split = p->schedule == 2 ||
@@ -144,8 +150,8 @@ int validate(const attn_params_ex* p, Checked* c) {
   if (p->mask_kind < ATTN_MASK_NONE || p->mask_kind > ATTN_MASK_CAUSAL_BR)
     return fail(ATTN_ERR_INVALID_ARG, "unknown mask kind %d", p->mask_kind);
   const int64_t BH = static_cast<int64_t>(p->B) * p->H;
-  const int64_t n_qpairs = (static_cast<int64_t>(p->Nq) + 2 * attn::kBM - 1) / (2 * attn::kBM);
-  if (BH * n_qpairs >= (int64_t{1} << 31))
+  const int64_t n_qtiles = (static_cast<int64_t>(p->Nq) + attn::kBM - 1) / attn::kBM;
+  if (BH * n_qtiles >= (int64_t{1} << 31))
     return fail(ATTN_ERR_INVALID_ARG, "too many (batch, head, query-tile) tasks");
   const bool na3 = p->mask_kind == ATTN_MASK_NA3D;
   if (!na3 && (p->grid_d != 0 || p->window_d != 0 || p->wrap_d != 0))
@@ -344,7 +350,8 @@ int fill_params(const attn_params_ex* p, const Checked& c, const Plan& pl, attn:
   kp->Nk = p->Nk;
   kp->c = p->scale * 1.4426950408889634f;
   *mask = kernel_mask(p, c, kp);
-  kp->n_qpairs = pl.n_qpairs;
+  kp->q_tiles = pl.q_tiles;
+  kp->n_qtasks = pl.n_qtasks;
   kp->n_kv = pl.n_kv;
   kp->n_tasks = pl.n_tasks;
   kp->split = pl.split;

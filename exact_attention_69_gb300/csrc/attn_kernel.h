@@ -69,9 +69,11 @@ struct KernelParams {
   int causal_off;               // kMaskCausalBR: key k allowed iff k <= q + causal_off (Nk - Nq)
   int grid_d, window_d;         // kMaskNa3: depth of the volume and window along it
   int na_wrap;                  // kMaskNa3: kNa3Wrap* bits of the axes that wrap
-  int n_qpairs;                 // ceil(Nq / 256): a task is one pair of Q tiles of one head
+  int q_tiles;                  // Q tiles (of 128 rows) per task: 2, or 1 when a launch has
+                                // fewer pairs than persistent CTAs
+  int n_qtasks;                 // ceil(Nq / (128 * q_tiles)): tasks per (batch, head)
   int n_kv;                     // ceil(Nk / 128)
-  int n_tasks;                  // B * H * n_qpairs
+  int n_tasks;                  // B * H * n_qtasks
   // Work split. split == 0: whole tasks, round robin over the CTAs. split == 1
   // (unmasked only): the tasks' K/V tiles form one sequence of `units`
   // (task-major) and CTA c takes units [c*units/G, (c+1)*units/G); a task cut

@@ -451,28 +451,29 @@ struct Task {
   bool live[2];
 };
 
-// Task t -> (batch, head, pair of Q tiles). Causal: pairs in decreasing
-// length order across all heads (longest first); otherwise head-major so that
-// CTAs working at the same time share a head's K/V in L2.
+// Task t -> (batch, head, Q tiles: a pair, or one when p.q_tiles == 1). Causal:
+// tasks in decreasing length order across all heads (longest first);
+// otherwise head-major so that CTAs working at the same time share a head's
+// K/V in L2.
 template <int MASK>
 __host__ __device__ __forceinline__ Task decode_task(int t, const KernelParams& p) {
   const int BH = p.B * p.H;
   int bh, qp;
   if (mask_is_causal(MASK)) {
     bh = t % BH;
-    qp = p.n_qpairs - 1 - t / BH;
+    qp = p.n_qtasks - 1 - t / BH;
   } else {
-    bh = t / p.n_qpairs;
-    qp = t - bh * p.n_qpairs;
+    bh = t / p.n_qtasks;
+    qp = t - bh * p.n_qtasks;
   }
   Task k;
   k.bh = bh;
   k.b = bh / p.H;
   k.h = bh - k.b * p.H;
-  k.q0[0] = qp * 2 * kBM;
+  k.q0[0] = qp * p.q_tiles * kBM;
   k.q0[1] = k.q0[0] + kBM;
   k.live[0] = k.q0[0] < p.Nq;
-  k.live[1] = k.q0[1] < p.Nq;
+  k.live[1] = p.q_tiles == 2 && k.q0[1] < p.Nq;
   return k;
 }
 
@@ -685,7 +686,7 @@ __host__ __device__ __forceinline__ int band_next(const Band& b, int j) {
 template <int MASK>
 __host__ __device__ __forceinline__ Band task_band(const Task& tk, const KernelParams& p) {
   if constexpr (mask_is_na(MASK)) {
-    return na_band<MASK>(tk.q0[0], min(tk.q0[1] + kBM, p.Nq) - 1, p);
+    return na_band<MASK>(tk.q0[0], min(tk.q0[tk.live[1] ? 1 : 0] + kBM, p.Nq) - 1, p);
   } else {
     Band b;
     b.lo0 = 0;

@@ -52,18 +52,21 @@ extern "C" int tile_class_host(int kind, int q0, int j, int Nq, int Nk, int grid
   }
 }
 
-// Task index -> (b, h, first row of Q tile 0), as the kernel decodes it.
-extern "C" void decode_task_host(int mask, int t, int B, int H, int Nq, int* out) {
+// Task index -> (b, h, first row of Q tile 0, whether Q tile 1 is live), as
+// the kernel decodes it with q_tiles Q tiles per task.
+extern "C" void decode_task_host(int mask, int t, int B, int H, int Nq, int q_tiles, int* out) {
   attn::KernelParams p{};
   p.B = B;
   p.H = H;
   p.Nq = Nq;
-  p.n_qpairs = (Nq + 2 * attn::kBM - 1) / (2 * attn::kBM);
+  p.q_tiles = q_tiles;
+  p.n_qtasks = (Nq + q_tiles * attn::kBM - 1) / (q_tiles * attn::kBM);
   attn::dev::Task k = mask == attn::kMaskCausal ? attn::dev::decode_task<attn::kMaskCausal>(t, p)
                                                 : attn::dev::decode_task<attn::kMaskNone>(t, p);
   out[0] = k.b;
   out[1] = k.h;
   out[2] = k.q0[0];
+  out[3] = k.live[1] ? 1 : 0;
 }
 
 // The in-tile neighbourhood mask of query q for the K/V tile starting at key

@@ -34,7 +34,7 @@ def plan(tmp_path_factory):
     lib = ctypes.CDLL(out)
     lib.tile_class_host.argtypes = [ctypes.c_int] * 12
     lib.tile_class_host.restype = ctypes.c_int
-    lib.decode_task_host.argtypes = [ctypes.c_int] * 5 + [ctypes.POINTER(ctypes.c_int)]
+    lib.decode_task_host.argtypes = [ctypes.c_int] * 6 + [ctypes.POINTER(ctypes.c_int)]
     lib.na_bits_host.argtypes = [ctypes.c_int] * 10 + [ctypes.POINTER(ctypes.c_uint)]
     lib.tile_class3_host.argtypes = [ctypes.c_int] * 11
     lib.tile_class3_host.restype = ctypes.c_int
@@ -109,21 +109,27 @@ def test_tile_classes_match_oracle_mask(plan, mask, Nq, Nk, grid, window, dilati
     assert wasted <= visited // 2 + 1, (visited, wasted)
 
 
+@pytest.mark.parametrize("q_tiles", [1, 2])
 @pytest.mark.parametrize("mask", ["none", "causal"])
-def test_tasks_cover_every_q_tile_once(plan, mask):
+def test_tasks_cover_every_q_tile_once(plan, mask, q_tiles):
+    """Tasks of one Q tile or of a pair: every 128-row Q tile of every head is
+    in exactly one task (a pair's second tile only if it starts below Nq)."""
     B, H, Nq = 3, 5, 1000
-    n_qpairs = -(-Nq // 256)
+    span = 128 * q_tiles
+    n_tasks = -(-Nq // span)
     seen = set()
-    out = (ctypes.c_int * 3)()
-    for t in range(B * H * n_qpairs):
-        plan.decode_task_host(KIND[mask], t, B, H, Nq, out)
-        key = (out[0], out[1], out[2])
-        assert key not in seen
-        seen.add(key)
-    assert seen == {(b, h, 256 * p) for b in range(B) for h in range(H) for p in range(n_qpairs)}
-    if mask == "causal":  # longest pairs (largest row offset) come first
-        plan.decode_task_host(1, 0, B, H, Nq, out)
-        assert out[2] == 256 * (n_qpairs - 1)
+    out = (ctypes.c_int * 4)()
+    for t in range(B * H * n_tasks):
+        plan.decode_task_host(KIND[mask], t, B, H, Nq, q_tiles, out)
+        tiles = [out[2]] + ([out[2] + 128] if out[3] else [])
+        for q0 in tiles:
+            key = (out[0], out[1], q0)
+            assert key not in seen
+            seen.add(key)
+    assert seen == {(b, h, 128 * i) for b in range(B) for h in range(H) for i in range(-(-Nq // 128))}
+    if mask == "causal":  # longest tasks (largest row offset) come first
+        plan.decode_task_host(1, 0, B, H, Nq, q_tiles, out)
+        assert out[2] == span * (n_tasks - 1)
 
 
 @pytest.mark.parametrize("mode,gh,gw,window,dilation", [
