@@ -135,6 +135,31 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// As tma_load_4d, with an L2 eviction-priority policy for the tile (from
+// l2_policy_evict_first / l2_policy_evict_last).
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int c0, int c1, int c2, int c3, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;\n\t}" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: data read once (Q) goes first when L2 needs room; data read by
+// every task of a head (K, V) goes last.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // --- tcgen05: tensor memory and the 5th-generation tensor core
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -1029,6 +1054,7 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
   int q_armed = -1;
   uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
   bool injected = false;
+  const uint64_t pol_once = l2_policy_evict_first(), pol_reuse = l2_policy_evict_last();
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
@@ -1039,8 +1065,8 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
 #pragma unroll
     for (int h = 0; h < 2; ++h)
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d(sbase + C::kOffQ + h * C::kTileBytes + c * C::kChunkBytes, &p.tm_q,
-                    bars.q_full(), c * C::kBoxCols, tk.q0[h], tk.h, tk.b);
+        tma_load_4d_hint(sbase + C::kOffQ + h * C::kTileBytes + c * C::kChunkBytes, &p.tm_q,
+                         bars.q_full(), c * C::kBoxCols, tk.q0[h], tk.h, tk.b, pol_once);
     q_armed = static_cast<int>(q_it & 1u);
     ++q_it;
     int nth = 0;
@@ -1058,8 +1084,8 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
       } else {
         mbar_expect_tx(bars.k_full(ks), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sbase + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &p.tm_k,
-                      bars.k_full(ks), c * C::kBoxCols, j * kBN, tk.h, tk.b);
+          tma_load_4d_hint(sbase + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes, &p.tm_k,
+                           bars.k_full(ks), c * C::kBoxCols, j * kBN, tk.h, tk.b, pol_reuse);
         k_armed |= 1u << ks;
         k_par = (k_par & ~(1u << ks)) | (((k_it / C::kKStages) & 1u) << ks);
       }
@@ -1069,8 +1095,8 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
         goto drain;
       mbar_expect_tx(bars.v_full(vs), C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d(sbase + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &p.tm_v,
-                    bars.v_full(vs), c * C::kBoxCols, j * kBN, tk.h, tk.b);
+        tma_load_4d_hint(sbase + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes, &p.tm_v,
+                         bars.v_full(vs), c * C::kBoxCols, j * kBN, tk.h, tk.b, pol_reuse);
       v_armed |= 1u << vs;
       v_par = (v_par & ~(1u << vs)) | (((v_it / C::kVStages) & 1u) << vs);
       ++v_it;
@@ -1435,13 +1461,13 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
         uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          __stcs(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
       }
     }
     release_o();
     if (row_ok && p.lse != nullptr) {
       const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
-      p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
+      __stcs(p.lse + static_cast<int64_t>(tk.bh) * p.Nq + q, lse);
     }
     return !*ctl.abort;
   }
@@ -1575,13 +1601,13 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
       uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        __stcs(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
     }
   }
   release_o();
   if (row_ok && p.lse != nullptr) {
     const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
-    p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
+    __stcs(p.lse + static_cast<int64_t>(tk.bh) * p.Nq + q, lse);
   }
   return !*ctl.abort;
 }
@@ -1768,12 +1794,12 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
         uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          __stcs(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
       }
     }
     if (row_ok && p.lse != nullptr) {
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
-      p.lse[static_cast<int64_t>(tk.bh) * p.Nq + q] = lse;
+      __stcs(p.lse + static_cast<int64_t>(tk.bh) * p.Nq + q, lse);
     }
   }
 }
