@@ -1325,6 +1325,133 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long
   return v;
 }
 
+// Stores a warp's block of 32 output rows x 32 bf16 columns (64 bytes per
+// row; the lane's own row in pk). Storing each lane's row as it stands would
+// make every 16-byte store instruction touch 32 rows; instead the four lanes
+// 4g..4g+3 first trade 16-byte chunks (a rotation by the lane's index, four
+// shuffle rounds, the opposite rotation), after which lane 4g + c holds
+// chunk c of rows 4g..4g+3, and store k writes eight whole 64-byte row
+// segments (row 4g + k of each group). `seg` points at column 0 of the
+// block's row 0, `stride` is the row stride in elements; rows from `rows`
+// on are not written. Called by all 32 lanes.
+__device__ __forceinline__ void store_rows32(const uint32_t (&pk)[16], __nv_bfloat16* seg,
+                                             int64_t stride, int rows) {
+  const int lane = threadIdx.x & 31, c = lane & 3, g4 = lane & ~3;
+  uint32_t a[4][4], b[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) a[i][w] = pk[4 * i + w];
+  // chunk i of the rotated row: chunk (i + c) mod 4
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) b[i][w] = (c & 1) ? a[(i + 1) & 3][w] : a[i][w];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) a[i][w] = (c & 2) ? b[(i + 2) & 3][w] : b[i][w];
+  // round i: from lane g4 + (c - i) mod 4, whose rotated chunk i is its chunk c
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int src = g4 | ((c - i) & 3);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) b[i][w] = __shfl_sync(0xffffffffu, a[i][w], src);
+  }
+  // b[i] is chunk c of row g4 + (c - i) mod 4; put row g4 + k at index k
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) a[r][w] = (c & 1) ? b[(1 - r) & 3][w] : b[(4 - r) & 3][w];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) b[r][w] = (c & 2) ? a[(r + 2) & 3][w] : a[r][w];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    if (g4 + r < rows)
+      __stcs(reinterpret_cast<uint4*>(seg + (g4 + r) * stride + c * 8),
+             make_uint4(b[r][0], b[r][1], b[r][2], b[r][3]));
+}
+
+// A 32-row quarter of a part slot: [D/4][32 rows] float4, then m[32], l[32].
+// CTA `cta` keeps two slots per Q tile: one for its first segment (`head`),
+// one for its last.
+template <int D>
+__device__ __forceinline__ float* part_slot(const KernelParams& p, int cta, bool head, int hh,
+                                            int quarter) {
+  return p.ws_part + static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2) +
+         quarter * 32 * (D + 2);
+}
+
+// Arrival word of (task t, Q tile hh, 32-row quarter).
+__device__ __forceinline__ unsigned long long* arrival_word(const KernelParams& p, int t, int hh,
+                                                            int quarter) {
+  return p.ws_count + (2 * static_cast<int64_t>(t) + hh) * 4 + quarter;
+}
+
+// The CTAs [c_lo, c_hi] holding the parts of task t under the split
+// schedule: they are adjacent (CTA c covers units [cta_lo[c], cta_lo[c + 1]),
+// and no range is empty), so walk out from this CTA to the first and last.
+__device__ __forceinline__ void cut_span(const KernelParams& p, const int64_t* cta_lo, int t,
+                                         int& c_lo, int& c_hi) {
+  const int64_t t_first = static_cast<int64_t>(t) * p.n_kv;
+  c_lo = c_hi = blockIdx.x;
+  while (c_lo > 0 && cta_lo[c_lo] > t_first) --c_lo;
+  while (c_hi + 1 < static_cast<int>(gridDim.x) && cta_lo[c_hi + 1] < t_first + p.n_kv) ++c_hi;
+}
+
+// The merge of a task cut in two parts, by the part that finishes last: this
+// part's unnormalised O (TMEM), maximum m_ref and row sum l, with the other
+// part's mi, li and O row (float4 column group g from oth(g)); the lower
+// CTA's part comes first in every sum, so either part computes the same
+// bits. Writes the bf16 row and the log-sum-exp and hands O_h back to the
+// MMA warp. O_h must be complete (o_full seen).
+template <int D, typename Oth>
+__device__ __forceinline__ void merge_two(const KernelParams& p, const Bars& bars, const Task& tk,
+                                          int hh, int row, uint32_t t_o, float m_ref, float l,
+                                          float mi, float li, bool me_lo, Oth oth) {
+  const int lane = threadIdx.x & 31;
+  const int q = tk.q0[hh] + row;
+  const bool row_ok = q < p.Nq;
+  const int q_blk = q - lane;  // the warp's first row
+  __nv_bfloat16* seg = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                       static_cast<int64_t>(q_blk) * p.o_sn;
+  const float M = fmaxf(m_ref, mi);
+  const float w_me = m_ref == -CUDART_INF_F ? 0.f : ex2(m_ref - M);
+  const float w_ot = mi == -CUDART_INF_F ? 0.f : ex2(mi - M);
+  const float w_lo = me_lo ? w_me : w_ot, w_hi = me_lo ? w_ot : w_me;
+  const float L = __fmaf_rn(me_lo ? li : l, w_hi, __fmul_rn(me_lo ? l : li, w_lo));
+  const float inv_L = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t ov[32];
+    tmem_ld32(t_o + ch * 32, ov);
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = oth(ch * 8 + i);
+    auto mix = [&](float own, float other) {
+      return __fmaf_rn(w_hi, me_lo ? other : own, __fmul_rn(w_lo, me_lo ? own : other)) * inv_L;
+    };
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      packed[2 * i] = pack_bf16(mix(__uint_as_float(ov[4 * i]), v[i].x),
+                                mix(__uint_as_float(ov[4 * i + 1]), v[i].y));
+      packed[2 * i + 1] = pack_bf16(mix(__uint_as_float(ov[4 * i + 2]), v[i].z),
+                                    mix(__uint_as_float(ov[4 * i + 3]), v[i].w));
+    }
+    store_rows32(packed, seg + ch * 32, p.o_sn, p.Nq - q_blk);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bars.o_empty(hh));
+  if (row_ok && p.lse != nullptr) {
+    const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
+    __stcs(p.lse + static_cast<int64_t>(tk.bh) * p.Nq + q, lse);
+  }
+}
+
 // One arrival on a (task, Q tile) word tagged with this call's epoch; returns
 // the number of parts arrived so far in this call, or 0 if the CAS loop ran
 // past its bound (recorded as a timeout). The first attempt assumes this is
@@ -1369,13 +1496,7 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
                                               uint32_t& o_par, const Ctl& ctl) {
   const int lane = threadIdx.x & 31;
   const int quarter = row >> 5;
-  const int ctas = gridDim.x;
-  // this warp's quarter of a part slot: [D/4][32 rows] float4, m[32], l[32]
-  auto slot_of = [&](int cta, bool head) {
-    return p.ws_part +
-           static_cast<int64_t>((2 * cta + (head ? 0 : 1)) * 2 + hh) * 128 * (D + 2) +
-           quarter * 32 * (D + 2);
-  };
+  auto slot_of = [&](int cta, bool head) { return part_slot<D>(p, cta, head, hh, quarter); };
   auto release_o = [&]() {
     tc_fence_before();
     __syncwarp();
@@ -1383,11 +1504,8 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
   };
   const int64_t t_first = static_cast<int64_t>(sg.t) * p.n_kv;
   const int me = blockIdx.x;
-  // The parts' CTAs are adjacent (CTA c covers units [cta_lo[c], cta_lo[c + 1]),
-  // and no range is empty): walk out from this CTA to the first and the last.
-  int c_lo = me, c_hi = me;
-  while (c_lo > 0 && cta_lo[c_lo] > t_first) --c_lo;
-  while (c_hi + 1 < ctas && cta_lo[c_hi + 1] < t_first + p.n_kv) ++c_hi;
+  int c_lo, c_hi;
+  cut_span(p, cta_lo, sg.t, c_lo, c_hi);
   const uint32_t n_parts = static_cast<uint32_t>(c_hi - c_lo + 1);
   // a part of CTA c is that CTA's first segment iff its range starts in this task
   auto part = [&](int c) -> const float* { return slot_of(c, cta_lo[c] >= t_first); };
@@ -1396,7 +1514,7 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
   // are in flight together and read this call's finite values; this CTA's
   // own slot may hold a previous call's data.
   const int stand_in = c_lo != me ? c_lo : c_hi;
-  unsigned long long* word = p.ws_count + (2 * static_cast<int64_t>(sg.t) + hh) * 4 + quarter;
+  unsigned long long* word = arrival_word(p, sg.t, hh, quarter);
   // Every lane reads the arrival word (relaxed, one broadcast load) before O
   // is complete, so the read overlaps the last P V; if every other part is
   // in, an acquire fence orders the reads of those parts after it.
@@ -1414,8 +1532,6 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
   if (claim) fence_gpu();
   const int q = tk.q0[hh] + row;
   const bool row_ok = q < p.Nq;
-  __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
-                        static_cast<int64_t>(q) * p.o_sn;
   if (claim && n_parts == 2) {
     // The usual cut: the other part is complete; fetch its m, l and its
     // first 64 columns of O while the last P V finishes, then merge.
@@ -1430,45 +1546,9 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
     if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return false;
     o_par ^= 1u;
     tc_fence_after();
-    const float M = fmaxf(m_ref, mi);
-    const float w_me = m_ref == -CUDART_INF_F ? 0.f : ex2(m_ref - M);
-    const float w_ot = mi == -CUDART_INF_F ? 0.f : ex2(mi - M);
-    // the lower CTA's part first, so that either part computes the same bits
-    const bool me_lo = me == c_lo;
-    const float w_lo = me_lo ? w_me : w_ot, w_hi = me_lo ? w_ot : w_me;
-    const float L = __fmaf_rn(me_lo ? li : l, w_hi, __fmul_rn(me_lo ? l : li, w_lo));
-    const float inv_L = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t ov[32];
-      tmem_ld32(t_o + ch * 32, ov);
-      float4 v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        v[i] = ch * 8 + i < kPre ? pre[(ch * 8 + i) % kPre] : __ldcg(src + (ch * 8 + i) * 32 + lane);
-      if (row_ok) {
-        auto mix = [&](float own, float oth) {
-          return __fmaf_rn(w_hi, me_lo ? oth : own, __fmul_rn(w_lo, me_lo ? own : oth)) * inv_L;
-        };
-        uint32_t packed[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          packed[2 * i] = pack_bf16(mix(__uint_as_float(ov[4 * i]), v[i].x),
-                                    mix(__uint_as_float(ov[4 * i + 1]), v[i].y));
-          packed[2 * i + 1] = pack_bf16(mix(__uint_as_float(ov[4 * i + 2]), v[i].z),
-                                        mix(__uint_as_float(ov[4 * i + 3]), v[i].w));
-        }
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          __stcs(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
-      }
-    }
-    release_o();
-    if (row_ok && p.lse != nullptr) {
-      const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
-      __stcs(p.lse + static_cast<int64_t>(tk.bh) * p.Nq + q, lse);
-    }
+    merge_two<D>(p, bars, tk, hh, row, t_o, m_ref, l, mi, li, me == c_lo, [&](int g) {
+      return g < kPre ? pre[g % kPre] : __ldcg(src + g * 32 + lane);
+    });
     return !*ctl.abort;
   }
   if (!warp_wait(bars.o_full(hh), o_par, ctl, -1)) return false;
@@ -1554,6 +1634,8 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
   }
   const float inv_L = L > 0.f ? 1.f / L : 0.f;
   const float w_me = (m_ref == -CUDART_INF_F) ? 0.f : ex2(m_ref - M);
+  __nv_bfloat16* seg = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                       static_cast<int64_t>(q - lane) * p.o_sn;  // the warp's first row
   // O in chunks of 32 columns: this part's from TMEM, four parts' rows per round.
 #pragma unroll 1
   for (int ch = 0; ch < D / 32; ++ch) {
@@ -1594,15 +1676,10 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
         }
       }
     }
-    if (row_ok) {
-      uint32_t packed[16];
+    uint32_t packed[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) packed[i] = pack_bf16(acc[2 * i] * inv_L, acc[2 * i + 1] * inv_L);
-      uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        __stcs(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
-    }
+    for (int i = 0; i < 16; ++i) packed[i] = pack_bf16(acc[2 * i] * inv_L, acc[2 * i + 1] * inv_L);
+    store_rows32(packed, seg + ch * 32, p.o_sn, p.Nq - (q - lane));
   }
   release_o();
   if (row_ok && p.lse != nullptr) {
@@ -1773,8 +1850,8 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     // TMEM may never have been written for it
     const bool empty = !(l > 0.f);
     const bool row_ok = q < p.Nq;
-    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
-                          static_cast<int64_t>(q) * p.o_sn;
+    __nv_bfloat16* seg = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                         static_cast<int64_t>(q - lane) * p.o_sn;  // the warp's first row
 #pragma unroll
     for (int ch = 0; ch < D / 32; ++ch) {
       uint32_t ov[32];
@@ -1784,18 +1861,13 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.o_empty(hh));
       }
-      if (row_ok) {
-        uint32_t packed[16];
+      uint32_t packed[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          packed[i] = empty ? 0u
-                            : pack_bf16(__uint_as_float(ov[2 * i]) * inv_l,
-                                        __uint_as_float(ov[2 * i + 1]) * inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          __stcs(dst + i, make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
-      }
+      for (int i = 0; i < 16; ++i)
+        packed[i] = empty ? 0u
+                          : pack_bf16(__uint_as_float(ov[2 * i]) * inv_l,
+                                      __uint_as_float(ov[2 * i + 1]) * inv_l);
+      store_rows32(packed, seg + ch * 32, p.o_sn, p.Nq - (q - lane));
     }
     if (row_ok && p.lse != nullptr) {
       const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994530942f : -CUDART_INF_F;
