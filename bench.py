@@ -18,9 +18,12 @@ allowed pairs is reported beside it.
 One JSON line on rank 0 with: value (whole-job TFLOP/s, the K timed steps
 replayed as one CUDA graph between two events on its stream), roofline of the
 kernel (its average launch duration from those events, against the measured
-bf16 peak; eager per-launch events beside it as a cross-check), e2e (the same metric with host inputs and outputs copied
-inside the timed region), cpu_baseline (the fp64 CPU oracle on a bounded
-sample), clocks sampled during the timed region.
+bf16 peak; eager per-launch events beside it as a cross-check), e2e (the same
+metric with every step's inputs copied in from pinned host memory and its
+outputs read back inside the timed region: a stream of calls whose copies
+overlap the neighbouring steps' kernels; the one-stream serial figure beside
+it), cpu_baseline (the fp64 CPU oracle on a bounded sample), clocks sampled
+during the timed region.
 
 With --impl reference the line is the CPU oracle itself (the only reference
 implementation: the pages ship no code), timed on the host cores.
@@ -442,36 +445,80 @@ def ours_arm(args, w):
     ms_step = ms_total / args.steps
     value = whole_job_tflops(world, flops_tile, args.steps, ms_total)
 
-    # end to end through the public API: pinned host inputs in, host outputs back
+    # End to end through the public API: pinned host inputs in, host outputs back,
+    # every step. A stream of independent calls: step i's inputs are copied in on
+    # one stream, its kernel runs on a second, its outputs are copied out on a
+    # third, with two device buffer sets, so the copies of steps i + 1 and i - 1
+    # overlap the kernel of step i (events order each buffer's reuse). The same
+    # steps one after the other on one stream are reported as serial_value.
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    qd, kd, vd, od, ld = sets[0]
-    oh = torch.empty(od.shape, dtype=od.dtype, pin_memory=True)
-    lh = torch.empty(ld.shape, dtype=ld.dtype, pin_memory=True)
+    bufs = [sets[0], sets[1 % n_sets]]
+    oh = [torch.empty(bufs[0][3].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    lh = [torch.empty(bufs[0][4].shape, dtype=torch.float32, pin_memory=True) for _ in range(2)]
     e_steps = max(3, min(args.steps, 200))
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def e2e_step():
+    def e2e_step(i):
+        b = i % 2
+        qd, kd, vd, od, ld = bufs[b]
+        if used[b]:  # buffer b's last kernel and read-back are done
+            s_in.wait_event(ev_out[b])
+        used[b] = True
+        with torch.cuda.stream(s_in):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+        ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        E.attn_fwd(qd, kd, vd, out=od, lse=ld, stream=s_cmp, **kw)
+        ev_cmp[b].record(s_cmp)
+        s_out.wait_event(ev_cmp[b])
+        with torch.cuda.stream(s_out):
+            oh[b].copy_(od, non_blocking=True)
+            lh[b].copy_(ld, non_blocking=True)
+        ev_out[b].record(s_out)
+
+    def e2e_serial_step():
+        qd, kd, vd, od, ld = bufs[0]
         qd.copy_(qh, non_blocking=True)
         kd.copy_(kh, non_blocking=True)
         vd.copy_(vh, non_blocking=True)
         E.attn_fwd(qd, kd, vd, out=od, lse=ld, **kw)
-        oh.copy_(od, non_blocking=True)
-        lh.copy_(ld, non_blocking=True)
+        oh[0].copy_(od, non_blocking=True)
+        lh[0].copy_(ld, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1)
-    e_ms = max_over_ranks(e_ms, dist if world > 1 else None, dev)
+    def timed(run, start_stream, end_stream):
+        for i in range(3):
+            run(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(start_stream)
+        end_stream.wait_stream(start_stream)
+        for i in range(e_steps):
+            run(i)
+        e1.record(end_stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), dist if world > 1 else None, dev)
+
+    s_out.wait_stream(stream)
+    s_in.wait_stream(stream)
+    e_ms = timed(e2e_step, s_in, s_out)
+    e_ms_serial = timed(lambda i: e2e_serial_step(), stream, stream)
+    code, detail = E.device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} {detail} in the end-to-end steps")
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    d2h = oh[0].numel() * oh[0].element_size() + lh[0].numel() * lh[0].element_size()
     e2e = {"value": whole_job_tflops(world, flops_tile, e_steps, e_ms), "unit": "TFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
+           "ms_per_step": e_ms / e_steps,
+           "pipeline": "3 streams, 2 device buffer sets: copies of steps i+1 and i-1 overlap the kernel of step i",
+           "serial_value": whole_job_tflops(world, flops_tile, e_steps, e_ms_serial),
+           "serial_ms_per_step": e_ms_serial / e_steps}
 
     if rank != 0:
         if world > 1:
