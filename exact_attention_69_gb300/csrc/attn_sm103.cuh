@@ -1231,6 +1231,10 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
     };
     uint32_t aj = 0, an = 0;
     int j = step(sg.kv0 - 1, aj);
+    if constexpr (MASK != kMaskNone) {
+      // a task without a K/V tile (a Q tile of rows that see no key) is done with Q at once
+      if (j >= sg.kv1) mma_commit(bars.q_empty());
+    }
     if (j < sg.kv1) {
       if (!ctl_wait(bars.k_full(kr.s), kr.ph, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();

@@ -413,6 +413,15 @@ def test_causal_bottom_right(E, d, Nq, Nk):
     run(E, 2, 1, Nq, Nk, d, "causal_br", seed=Nq * 3 + Nk + d)
 
 
+@pytest.mark.parametrize("num_ctas,d", [(3, 64), (5, 128), (0, 32)])
+def test_causal_bottom_right_many_empty_tasks_per_cta(E, num_ctas, d):
+    """Nq much larger than Nk: most Q tiles have no key at all, and each CTA
+    takes several of those tasks in a row (few CTAs for many tasks). Every
+    task, even one without a K/V tile, must hand its Q buffer back so that the
+    next task's Q can be loaded."""
+    run(E, 2, 3, 3000, 100, d, "causal_br", seed=3100 + d, num_ctas=num_ctas)
+
+
 def test_causal_bottom_right_equals_top_left_when_square(E):
     q, k, v = (t.cuda() for t in make_qkv(1, 3, 777, 777, 64, 1.0, 51))
     a = E.attn_fwd(q, k, v, mask="causal")
