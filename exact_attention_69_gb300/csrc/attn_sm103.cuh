@@ -1941,6 +1941,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+  // Everything above touches only this CTA's shared memory and TMEM. Before
+  // the first global access, wait until the previous kernel on the stream has
+  // completed (a no-op without a programmatic dependency); then let the next
+  // launch's CTAs start on the SMs this grid leaves.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp < 4) {
     // warpgroup 0 needs few registers; the softmax warpgroups take them
@@ -1979,8 +1985,20 @@ cudaError_t launch_mask(const KernelParams& p, int grid, cudaStream_t s) {
   const int smem = smem_request<D>();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the CTAs of this launch may start (shared
+  // memory, barriers, TMEM) while the previous kernel on the stream finishes;
+  // they wait for its completion before their first global memory access.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = mask_is_causal(MASK) ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int D>
