@@ -149,3 +149,44 @@ def test_attn_log_reports_the_launch():
     assert len(lines) == 2, r.stderr
     assert "d=64" in lines[0] and "mask=none" in lines[0] and "grid=" in lines[0]
     assert "mask=causal" in lines[1] and "schedule=whole" in lines[1]
+
+
+@pytest.mark.parametrize("mask,kw", [("none", {}), ("wrap", dict(window=7, grid=(32, 32))),
+                                     ("causal", {})])
+def test_calls_pipelined_over_three_streams(lib, mask, kw):
+    """A stream of calls whose inputs arrive by host copies on another stream
+    (event waits order them) and whose outputs leave on a third: each call
+    must see its own inputs, whatever the launch overlaps, so every step's
+    result equals the same call made alone."""
+    import exact_attention_69_gb300 as E
+    steps, B, H, N, d = 6, 1, 2, 1024, 64
+    hosts = [tuple(t.pin_memory() for t in make_qkv(B, H, N, N, d, 1.0, 500 + i)) for i in range(steps)]
+    dev = [tuple(torch.empty(B, H, N, d, dtype=torch.bfloat16, device="cuda") for _ in range(3))
+           for _ in range(2)]
+    outs = [torch.empty(B, H, N, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    res = [torch.empty(B, H, N, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(steps)]
+    s_in, s_cmp, s_out = (torch.cuda.Stream() for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for i in range(steps):
+        b = i % 2
+        if i >= 2:
+            s_in.wait_event(ev_out[b])
+        with torch.cuda.stream(s_in):
+            for dst, src in zip(dev[b], hosts[i]):
+                dst.copy_(src, non_blocking=True)
+        ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        E.attn_fwd(*dev[b], out=outs[b], return_lse=False, mask=mask, stream=s_cmp, **kw)
+        ev_cmp[b].record(s_cmp)
+        s_out.wait_event(ev_cmp[b])
+        with torch.cuda.stream(s_out):
+            res[i].copy_(outs[b], non_blocking=True)
+        ev_out[b].record(s_out)
+    torch.cuda.synchronize()
+    assert lib.device_status()[0] == 0
+    for i in range(steps):
+        alone = E.attn_fwd(*(t.cuda() for t in hosts[i]), return_lse=False, mask=mask, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(res[i], alone.cpu()), f"step {i} differs from the same call made alone"
