@@ -461,6 +461,11 @@ __device__ __forceinline__ bool ctl_wait(uint32_t bar, uint32_t parity, const Ct
   return ctl_wait_slow(bar, parity, c.abort, c.status, c.timeout_ns, tile, role, honour_abort);
 }
 
+// Waits until the kernel this launch depends on (the previous one on the
+// stream, under programmatic dependent launch) has completed and its memory
+// operations are visible; returns at once without such a dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------- work and masks
 
 // The causal key bound's shift: key k allowed iff k <= q + shift (0 for
@@ -1057,9 +1062,20 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
   const uint64_t pol_once = l2_policy_evict_first(), pol_reuse = l2_policy_evict_last();
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
+  bool dep_waited = false;
   while (it.next(p, sg)) {
     const Task tk = decode_task<MASK>(sg.t, p);
     const Band band = task_band<MASK>(tk, p);
+    constexpr bool kNa = mask_is_na(MASK);
+    TileCursor<MASK> cur(band, 2);
+    bool act[2];
+    // the first tile is found (kernel parameters only) before the previous
+    // kernel's completion is awaited
+    const int j0 = kNa ? cur.next(tk, sg.kv1, act, p) : next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
+    if (!dep_waited) {
+      grid_dep_wait();
+      dep_waited = true;
+    }
     if (!ctl_wait(bars.q_empty(), (q_it & 1u) ^ 1u, ctl, -1, kRoleLoader)) goto drain;
     mbar_expect_tx(bars.q_full(), 2 * C::kTileBytes);
 #pragma unroll
@@ -1070,10 +1086,7 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
     q_armed = static_cast<int>(q_it & 1u);
     ++q_it;
     int nth = 0;
-    constexpr bool kNa = mask_is_na(MASK);
-    TileCursor<MASK> cur(band, 2);
-    bool act[2];
-    for (int j = kNa ? cur.next(tk, sg.kv1, act, p) : next_tile<MASK>(tk, band, sg.kv0 - 1, sg.kv1, p);
+    for (int j = j0;
          j < sg.kv1;
          j = kNa ? cur.next(tk, sg.kv1, act, p) : next_tile<MASK>(tk, band, j, sg.kv1, p), ++nth) {
       const int ks = static_cast<int>(k_it % C::kKStages);
@@ -1763,6 +1776,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
   const float c = p.c;
   uint32_t s_par = 0, o_par = 0;
 
+  grid_dep_wait();  // before the first global store (O, LSE, partial results)
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
@@ -1941,11 +1955,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Ctl ctl{abort_flag, p.status, p.timeout_ns};
-  // Everything above touches only this CTA's shared memory and TMEM. Before
-  // the first global access, wait until the previous kernel on the stream has
-  // completed (a no-op without a programmatic dependency); then let the next
-  // launch's CTAs start on the SMs this grid leaves.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Everything above touches only this CTA's shared memory and TMEM; the next
+  // launch's CTAs may start on the SMs this grid leaves. The loader and the
+  // softmax warps wait for the previous kernel on the stream to complete
+  // before their first global access (grid_dep_wait); the MMA warp reads only
+  // what the loader's copies brought in.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp < 4) {
