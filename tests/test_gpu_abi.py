@@ -6,8 +6,8 @@ forward the same way: output, q, k, v, log-sum-exp, window, dilation, ...).
 It is called here through ctypes, on a stream set with attn_set_stream, and
 compared with the fp64 oracle. "Profiling in PyTorch" part 3 shows the fused
 backends as a single kernel per attention call; a stream capture of one call
-(the graph it records holds a single kernel node) asserts the same of this
-library.
+(the graph it records holds a single kernel node) and torch.profiler's device
+events assert the same of this library.
 """
 import ctypes
 import math
@@ -133,6 +133,45 @@ def test_one_kernel_launch_per_call(lib, B, H, N, d, kw):
     kernels, nodes = _captured_kernel_nodes(
         lambda: E.attn_fwd(q, k, v, out=o, lse=lse, stream=s, **kw), s)
     assert (kernels, nodes) == (1, 1)
+
+
+@pytest.mark.parametrize("B,H,N,d,kw", [
+    (2, 5, 4096, 64, dict()),
+    (1, 2, 1000, 128, dict(mask="causal")),
+    (1, 2, 1024, 32, dict(mask="wrap", window=7)),
+])
+def test_profiler_sees_one_kernel_per_call(lib, B, H, N, d, kw):
+    """The same invariant through torch.profiler, as "Profiling in PyTorch"
+    part 3 reads it: three calls record three device events, each the fused
+    forward kernel, and no memset, copy or other kernel. A torch fill launched
+    in the same region is the control that the profiler records device
+    activity at all (the raw kineto events hold kernels that no torch op
+    launched, which torch's own event tree leaves out)."""
+    from torch.autograd import DeviceType
+    if not torch.autograd.kineto_available():
+        pytest.skip("torch built without the kineto profiler")
+    import exact_attention_69_gb300 as E
+    q, k, v = (t.cuda() for t in make_qkv(B, H, N, N, d, 1.0, 70 + d))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    E.attn_fwd(q, k, v, out=o, lse=lse, **kw)  # first-use allocations happen here
+    torch.cuda.synchronize()
+    acts = [torch.profiler.ProfilerActivity.CPU, torch.profiler.ProfilerActivity.CUDA]
+    with torch.profiler.profile(activities=acts):  # a process's first session sees no device work
+        torch.ones(1, device="cuda")
+        torch.cuda.synchronize()
+    with torch.profiler.profile(activities=acts) as prof:
+        torch.ones(1, device="cuda")
+        for _ in range(3):
+            E.attn_fwd(q, k, v, out=o, lse=lse, **kw)
+        torch.cuda.synchronize()
+    dev = [e.name() for e in prof.profiler.kineto_results.events()
+           if e.device_type() == DeviceType.CUDA]
+    control = [n for n in dev if "FillFunctor" in n]
+    if not control:
+        pytest.skip(f"the profiler records no device activity here ({len(dev)} device events)")
+    ours = [n for n in dev if n not in control]
+    assert len(ours) == 3 and all("attn_fwd_kernel" in n for n in ours), dev
 
 
 def test_attn_log_reports_the_launch():
