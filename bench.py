@@ -448,22 +448,26 @@ def ours_arm(args, w):
     # End to end through the public API: pinned host inputs in, host outputs back,
     # every step. A stream of independent calls: step i's inputs are copied in on
     # one stream, its kernel runs on a second, its outputs are copied out on a
-    # third, with two device buffer sets, so the copies of steps i + 1 and i - 1
-    # overlap the kernel of step i (events order each buffer's reuse). The same
+    # third, with three device buffer sets, so the copies of steps i + 1 and i - 1
+    # overlap the kernel of step i and the next step's copy in never waits for
+    # the read-back of the step before (events order each buffer's reuse). The same
     # steps one after the other on one stream are reported as serial_value.
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    bufs = [sets[0], sets[1 % n_sets]]
-    oh = [torch.empty(bufs[0][3].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
-    lh = [torch.empty(bufs[0][4].shape, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    n_bufs = 3
+    bufs = [sets[i] for i in range(min(n_bufs, n_sets))]
+    while len(bufs) < n_bufs:  # filled by each step's own copy in before its kernel reads it
+        bufs.append(tuple(torch.empty_like(t) for t in sets[0]))
+    oh = [torch.empty(bufs[0][3].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(n_bufs)]
+    lh = [torch.empty(bufs[0][4].shape, dtype=torch.float32, pin_memory=True) for _ in range(n_bufs)]
     e_steps = max(3, min(args.steps, 200))
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    used = [False, False]
+    ev_in = [torch.cuda.Event() for _ in range(n_bufs)]
+    ev_cmp = [torch.cuda.Event() for _ in range(n_bufs)]
+    ev_out = [torch.cuda.Event() for _ in range(n_bufs)]
+    used = [False] * n_bufs
 
     def e2e_step(i):
-        b = i % 2
+        b = i % n_bufs
         qd, kd, vd, od, ld = bufs[b]
         if used[b]:  # buffer b's last kernel and read-back are done
             s_in.wait_event(ev_out[b])
@@ -521,7 +525,7 @@ def ours_arm(args, w):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e_steps,
            "mode": "pipelined" if piped >= serial else "serial",
            "pipelined_value": piped, "pipelined_ms_per_step": e_ms / e_steps,
-           "pipeline": "3 streams, 2 device buffer sets: copies of steps i+1 and i-1 overlap the kernel of step i",
+           "pipeline": "3 streams, 3 device buffer sets: copies of steps i+1 and i-1 overlap the kernel of step i",
            "serial_value": serial, "serial_ms_per_step": e_ms_serial / e_steps}
 
     if rank != 0:
