@@ -358,6 +358,7 @@ int fill_params(const attn_params_ex* p, const Checked& c, const Plan& pl, attn:
   kp->units = pl.units;
   kp->timeout_ns = p->timeout_ns ? p->timeout_ns : kDefaultTimeoutNs;
   kp->inject = p->inject;
+  kp->twin = attn::twin_tasks(*kp, *mask);
   return ATTN_OK;
 }
 
@@ -387,10 +388,11 @@ void log_launch(const char* entry, const attn_params_ex* p, const attn::KernelPa
   if (!log_enabled()) return;
   std::fprintf(stderr,
                "%s: d=%d mask=%s variant=%d B=%d H=%d Nq=%d Nk=%d grid_hw=%dx%d window=%dx%d "
-               "dilation=%d wrap=%d schedule=%s grid=%d tasks=%d units=%lld\n",
+               "dilation=%d wrap=%d schedule=%s grid=%d tasks=%d units=%lld q_tiles=%d twin=%d\n",
                entry, p->d, mask_name(p->mask_kind), mask, p->B, p->H, p->Nq, p->Nk, kp.grid_h,
                kp.grid_w, kp.window_h, kp.window_w, kp.dilation, kp.na_wrap,
-               pl.split ? "split" : "whole", pl.grid, pl.n_tasks, static_cast<long long>(pl.units));
+               pl.split ? "split" : "whole", pl.grid, pl.n_tasks, static_cast<long long>(pl.units),
+               kp.q_tiles, kp.twin);
 }
 
 // Device pointers of the call's workspace: the caller's, or the library's own

@@ -71,6 +71,8 @@ struct KernelParams {
   int na_wrap;                  // kMaskNa3: kNa3Wrap* bits of the axes that wrap
   int q_tiles;                  // Q tiles (of 128 rows) per task: 2, or 1 when a launch has
                                 // fewer pairs than persistent CTAs
+  int twin;                     // neighbourhood masks with q_tiles == 1: both softmax warpgroups
+                                // on the one Q tile, its K/V tiles taken in turn (set at launch)
   int n_qtasks;                 // ceil(Nq / (128 * q_tiles)): tasks per (batch, head)
   int n_kv;                     // ceil(Nk / 128)
   int n_tasks;                  // B * H * n_qtasks
@@ -113,5 +115,8 @@ cudaError_t launch_d64(const KernelParams& p, int mask, int grid, cudaStream_t s
 cudaError_t launch_bwd(const BwdParams& p, int d, int mask, cudaStream_t s, cudaStream_t aux,
                        cudaEvent_t fork, cudaEvent_t join);
 cudaError_t launch_d128(const KernelParams& p, int mask, int grid, cudaStream_t s);
+// 1 if a launch of kernel variant `mask` with these parameters should run its
+// tasks as twins (KernelParams::twin), else 0; in attn_fwd_d64.cu.
+int twin_tasks(const KernelParams& p, int mask);
 
 }  // namespace attn

@@ -355,11 +355,12 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
   static constexpr int kBarBytes = 512;
-  static_assert(8 * (13 + 2 * kKStages + 2 * kVStages) + 8 <= kBarBytes, "barrier area");
+  static_assert(8 * (15 + 2 * kKStages + 2 * kVStages) + 8 <= kBarBytes, "barrier area");
   // first unit of every CTA of a split schedule (kMaxSplitCtas + 1 int64),
   // then this CTA's first (task, K/V tile) packed in one int64
   static constexpr int kOffTbl = kOffBar + kBarBytes;
   static constexpr int kTblBytes = 8 * (kMaxSplitCtas + 2);
+  static_assert(kTblBytes >= 2 * kBM * 4, "the twin exchange (m and l of 128 rows) shares the table");
   static constexpr int kSmemBytes = kOffTbl + kTblBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kLayout = D >= 64 ? 2u : 4u;
@@ -388,7 +389,10 @@ struct Bars {
   __device__ uint32_t k_empty(int s) const { return base + 104 + 8 * (kst + s); }
   __device__ uint32_t v_full(int s) const { return base + 104 + 8 * (2 * kst + s); }
   __device__ uint32_t v_empty(int s) const { return base + 104 + 8 * (2 * kst + vst + s); }
-  __device__ int count() const { return 13 + 2 * kst + 2 * vst; }
+  // twin tasks: warpgroup 1's m and l handed to warpgroup 0, and handed back
+  __device__ uint32_t x_full() const { return base + 104 + 8 * (2 * kst + 2 * vst); }
+  __device__ uint32_t x_empty() const { return base + 112 + 8 * (2 * kst + 2 * vst); }
+  __device__ int count() const { return 15 + 2 * kst + 2 * vst; }
 };
 
 // ------------------------------------------------------------- bounded waits
@@ -481,6 +485,19 @@ struct Task {
   bool live[2];
 };
 
+// Neighbourhood launches with one Q tile per task and long K/V chains run each
+// task as a twin task (the host sets p.twin): both softmax warpgroups hold the
+// same 128 queries and take its K/V tiles in turn (each with its own S, P, O,
+// running maximum and row sum), and warpgroup 0 merges the two halves at the
+// end, as the split schedule merges parts: M = max(m0, m1),
+// L = l0 2^(m0 - M) + l1 2^(m1 - M), O = (O0 2^(m0 - M) + O1 2^(m1 - M)) / L.
+// The K/V chain of a task is then half as long, and the tensor core runs one
+// half's S while the other's softmax works.
+template <int MASK>
+__host__ __device__ __forceinline__ bool twin_mode(const KernelParams& p) {
+  return mask_is_na(MASK) && p.twin != 0;
+}
+
 // Task t -> (batch, head, Q tiles: a pair, or one when p.q_tiles == 1). Causal:
 // tasks in decreasing length order across all heads (longest first);
 // otherwise head-major so that CTAs working at the same time share a head's
@@ -504,6 +521,10 @@ __host__ __device__ __forceinline__ Task decode_task(int t, const KernelParams& 
   k.q0[1] = k.q0[0] + kBM;
   k.live[0] = k.q0[0] < p.Nq;
   k.live[1] = p.q_tiles == 2 && k.q0[1] < p.Nq;
+  if (twin_mode<MASK>(p)) {  // both warpgroups on the one Q tile
+    k.q0[1] = k.q0[0];
+    k.live[1] = k.live[0];
+  }
   return k;
 }
 
@@ -774,9 +795,11 @@ __host__ __device__ __forceinline__ int next_tile(const Task& tk, const Band& ba
 template <int MASK>
 struct TileCursor {
   Band b;
-  int len0, lo1s, len, base, pos, which;
+  int len0, lo1s, len, base, pos, which, cnt;
   uint32_t m0, m1;
-  __device__ __forceinline__ TileCursor(const Band& band, int w) : b(band), which(w) {
+  bool twin;
+  __device__ __forceinline__ TileCursor(const Band& band, int w, bool tw = false)
+      : b(band), which(w), cnt(0), twin(tw) {
     len0 = b.hi0 - b.lo0;
     lo1s = max(b.lo1, b.hi0);  // the second interval may share a tile with the first
     len = len0 + max(b.hi1 - lo1s, 0);
@@ -802,8 +825,20 @@ struct TileCursor {
       const uint32_t m = (m0 | m1) >> (pos - base);
       if (m != 0u) {
         pos += __ffs(static_cast<int>(m)) - 1;
-        a[0] = ((m0 >> (pos - base)) & 1u) != 0u;
-        a[1] = ((m1 >> (pos - base)) & 1u) != 0u;
+        if (twin) {
+          // a twin task's tiles go to its two warpgroups in turn
+          const int owner = cnt & 1;
+          ++cnt;
+          if (which != 2 && which != owner) {
+            ++pos;
+            continue;
+          }
+          a[0] = owner == 0;
+          a[1] = owner == 1;
+        } else {
+          a[0] = ((m0 >> (pos - base)) & 1u) != 0u;
+          a[1] = ((m1 >> (pos - base)) & 1u) != 0u;
+        }
         const int t = tile_at(pos);
         return t < end ? t : end;
       }
@@ -1067,7 +1102,7 @@ __device__ void loader_role(const KernelParams& p, uint32_t sbase, const Bars& b
     const Task tk = decode_task<MASK>(sg.t, p);
     const Band band = task_band<MASK>(tk, p);
     constexpr bool kNa = mask_is_na(MASK);
-    TileCursor<MASK> cur(band, 2);
+    TileCursor<MASK> cur(band, 2, twin_mode<MASK>(p));
     bool act[2];
     // the first tile is found (kernel parameters only) before the previous
     // kernel's completion is awaited
@@ -1211,6 +1246,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
   RingPos<C::kVStages> vr;
   uint32_t p_par = 0;  // bit h: parity of Q tile h's next P phases
   uint32_t o_par = 0;  // bit h: parity of Q tile h's next O phase
+  const bool twin = mask_is_na(MASK) && p.twin != 0;
   SegIter<MASK> it(p, cta_lo);
   Seg sg;
   while (it.next(p, sg)) {
@@ -1223,7 +1259,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
     // The next K/V tile after `from` and, in `act`, the Q tiles that need it
     // (bit h). Unmasked: every tile of the segment, for every live Q tile.
     // Neighbourhood masks: the cursor's search; others: the tile test.
-    TileCursor<MASK> cur(band, 2);
+    TileCursor<MASK> cur(band, 2, twin_mode<MASK>(p));
     const uint32_t live = (tk.live[0] ? 1u : 0u) | (tk.live[1] ? 2u : 0u);
     auto step = [&](int from, uint32_t& act) -> int {
       if constexpr (MASK == kMaskNone) {
@@ -1265,10 +1301,26 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
       const int jn = step(j, an);
       const bool has_next = jn < sg.kv1;
       if (!has_next) mma_commit(bars.q_empty());  // every S of the task is issued
+      bool k_taken = false;
+      uint32_t early = 0;
+      if constexpr (kNa) {
+        // Twin tasks: this tile is one warpgroup's, the next the other's, so
+        // the next S waits for nothing of this tile's softmax; it goes first,
+        // and the tensor core runs it while this tile's P is computed.
+        if (twin && has_next) {
+          early = an;
+          if (!ctl_wait(bars.k_full(kr.s), kr.ph, ctl, jn, kRoleMma)) goto drain;
+          tc_fence_after();
+          k_taken = true;
+          const bool h1 = an == 2u;
+          issue_s<D>(tmem + (h1 ? C::tm_s(1) : C::tm_s(0)), h1 ? dsc.q1 : dsc.q0,
+                     dsc.k0 + kr.s * Descs<D>::kStageStep);
+          mma_commit(h1 ? bars.s_full(1) : bars.s_full(0));
+        }
+      }
       if (!ctl_wait(bars.v_full(vr.s), vr.ph, ctl, j, kRoleMma)) goto drain;
       tc_fence_after();
       const uint64_t vd = dsc.v0 + vr.s * Descs<D>::kStageStep;
-      bool k_taken = false;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if ((aj >> h) & 1u) {
@@ -1286,7 +1338,7 @@ __device__ void mma_role(const KernelParams& p, uint32_t sbase, const Bars& bars
           p_par ^= 1u << h;
           o_ready |= 1u << h;
         }
-        if (has_next && ((an >> h) & 1u)) {
+        if (has_next && ((an >> h) & 1u) && !((early >> h) & 1u)) {
           if (!k_taken) {
             if (!ctl_wait(bars.k_full(kr.s), kr.ph, ctl, jn, kRoleMma)) goto drain;
             tc_fence_after();
@@ -1706,6 +1758,66 @@ __device__ __forceinline__ bool partial_epilogue(const KernelParams& p, const Ba
   return !*ctl.abort;
 }
 
+// Warpgroup 0's end of a twin task: both halves' O (TMEM; O_1 from the
+// other warpgroup's columns, same lanes), this half's m and l, the other's
+// from the exchange. A half with no tile (m = -inf) is left out by a select,
+// not a zero weight: its O columns may hold an earlier task's values.
+// False: the CTA is aborting.
+template <int D>
+__device__ __forceinline__ bool twin_epilogue(const KernelParams& p, const Bars& bars, const Task& tk,
+                                           int row, uint32_t t_o0, uint32_t t_o1, float m0,
+                                           float l0, const float* xch, uint32_t& o_par,
+                                           uint32_t& o_par1, uint32_t& x_par, const Ctl& ctl) {
+  const int lane = threadIdx.x & 31;
+  if (!warp_wait(bars.o_full(0), o_par, ctl, -1)) return false;
+  o_par ^= 1u;
+  if (!warp_wait(bars.o_full(1), o_par1, ctl, -1)) return false;
+  o_par1 ^= 1u;
+  if (!warp_wait(bars.x_full(), x_par, ctl, -1)) return false;
+  x_par ^= 1u;
+  tc_fence_after();
+  const float m1 = xch[row], l1 = xch[kBM + row];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bars.x_empty());
+  const float M = fmaxf(m0, m1);
+  const bool h0 = m0 != -CUDART_INF_F, h1 = m1 != -CUDART_INF_F;
+  const float w0 = h0 ? ex2(m0 - M) : 0.f, w1 = h1 ? ex2(m1 - M) : 0.f;
+  const float L = __fmaf_rn(l1, w1, __fmul_rn(l0, w0));
+  const float inv_L = L > 0.f ? 1.f / L : 0.f;
+  const bool empty = !(L > 0.f);
+  const int q = tk.q0[0] + row;
+  __nv_bfloat16* seg = reinterpret_cast<__nv_bfloat16*>(p.o) + tk.b * p.o_sb + tk.h * p.o_sh +
+                       static_cast<int64_t>(q - lane) * p.o_sn;  // the warp's first row
+  auto mix = [&](uint32_t a, uint32_t b) {
+    const float x = h0 ? __fmul_rn(__uint_as_float(a), w0) : 0.f;
+    return (h1 ? __fmaf_rn(__uint_as_float(b), w1, x) : x) * inv_L;
+  };
+#pragma unroll
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t oa[32], ob[32];
+    tmem_ld32(t_o0 + ch * 32, oa);
+    tmem_ld32(t_o1 + ch * 32, ob);
+    if (ch == D / 32 - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars.o_empty(0));
+        mbar_arrive(bars.o_empty(1));
+      }
+    }
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      packed[i] = empty ? 0u : pack_bf16(mix(oa[2 * i], ob[2 * i]), mix(oa[2 * i + 1], ob[2 * i + 1]));
+    store_rows32(packed, seg + ch * 32, p.o_sn, p.Nq - (q - lane));
+  }
+  if (q < p.Nq && p.lse != nullptr) {
+    const float lse = L > 0.f ? (M + __log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
+    __stcs(p.lse + static_cast<int64_t>(tk.bh) * p.Nq + q, lse);
+  }
+  return !*ctl.abort;
+}
+
 // Keys of a partial tile (class 2) that the query may not see become -inf.
 template <int MASK>
 __device__ __forceinline__ void mask_tile(uint32_t (&s)[128], const KernelParams& p, int j, int q,
@@ -1763,7 +1875,7 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha) {
 
 template <int D, int MASK>
 __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t tmem,
-                             const int64_t* cta_lo, const Ctl& ctl) {
+                             const int64_t* cta_lo, float* xch, const Ctl& ctl) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hh = (warp - 4) >> 2;          // which Q tile of the pair
@@ -1775,6 +1887,8 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
   const uint32_t t_p = lane_base + C::tm_p(hh);
   const float c = p.c;
   uint32_t s_par = 0, o_par = 0;
+  const bool twin = twin_mode<MASK>(p);
+  uint32_t o_par1 = 0, x_par = 0;  // twin tasks: warpgroup 0's view of O_1, the exchange
 
   grid_dep_wait();  // before the first global store (O, LSE, partial results)
   SegIter<MASK> it(p, cta_lo);
@@ -1794,7 +1908,7 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
     // its own so that P V starts on the first.
     // neighbourhood masks: the tiles the cursor finds for this Q tile (class 2)
     constexpr bool kNa = mask_is_na(MASK);
-    TileCursor<MASK> cur(task_band<MASK>(tk, p), hh);
+    TileCursor<MASK> cur(task_band<MASK>(tk, p), hh, twin);
     bool act[2];
     for (int j = kNa ? cur.next(tk, sg.kv1, act, p) : sg.kv0; j < sg.kv1;
          j = kNa ? cur.next(tk, sg.kv1, act, p) : j + 1) {
@@ -1854,6 +1968,23 @@ __device__ void softmax_role(const KernelParams& p, const Bars& bars, uint32_t t
       const float2 sa = __fadd2_rn(sum4[0], sum4[1]), sb = __fadd2_rn(sum4[2], sum4[3]);
       l += (sa.x + sa.y) + (sb.x + sb.y);
       first = false;
+    }
+    if (twin) {
+      if (hh == 1) {
+        // this half's m and l to warpgroup 0, which merges both halves and
+        // hands O_1 back to the MMA warp
+        if (!warp_wait(bars.x_empty(), x_par ^ 1u, ctl, -1)) return;
+        x_par ^= 1u;
+        xch[row] = m_ref;
+        xch[kBM + row] = l;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.x_full());
+        continue;
+      }
+      if (!twin_epilogue<D>(p, bars, tk, row, t_o, lane_base + C::tm_o(1), m_ref, l, xch, o_par,
+                            o_par1, x_par, ctl))
+        return;
+      continue;
     }
     // epilogue: O / l, bf16 store, log-sum-exp
     if (cut) {
@@ -1930,6 +2061,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(bars.o_empty(h), 4);
     }
     mbar_init(bars.done(), 1);
+    mbar_init(bars.x_full(), 4);   // one arrive per warp of warpgroup 1
+    mbar_init(bars.x_empty(), 4);  // one arrive per warp of warpgroup 0
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bars.k_full(s), 1);
       mbar_init(bars.k_empty(s), 1);
@@ -1973,7 +2106,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     __syncwarp();
   } else {
     set_max_regs_inc<kRegsSoftmax>();
-    softmax_role<D, MASK>(p, bars, tmem, cta_lo, ctl);
+    softmax_role<D, MASK>(p, bars, tmem, cta_lo, reinterpret_cast<float*>(cta_lo), ctl);
   }
 
   tc_fence_before();
@@ -1991,6 +2124,25 @@ constexpr int kMinSmemBytes = 116 * 1024;  // more than half an SM: one CTA (and
 template <int D>
 constexpr int smem_request() {
   return Cfg<D>::kSmemBytes > kMinSmemBytes ? Cfg<D>::kSmemBytes : kMinSmemBytes;
+}
+
+// A twin task pays an exchange and a merge (~2K cycles) to halve its K/V
+// chain. Measured on GB300: a gain with ~10 tiles a Q tile (16^3 volume,
+// window 5: 8 %), a loss with 5 (64 x 64 grid, window 7: 2-3 %).
+constexpr int kTwinMinTiles = 8;
+
+// Whether a neighbourhood launch with one Q tile per task runs its tasks as
+// twins: the K/V tiles of a task from the middle of head 0, counted on the host.
+template <int MASK>
+bool twin_worthwhile(const KernelParams& p) {
+  if (!mask_is_na(MASK) || p.q_tiles != 1 || p.n_qtasks <= 0 || p.twin != 0) return false;
+  const Task tk = decode_task<MASK>(p.n_qtasks / 2, p);
+  const Band band = task_band<MASK>(tk, p);
+  int n = 0;
+  for (int j = next_tile<MASK>(tk, band, -1, p.n_kv, p); j < p.n_kv && n < kTwinMinTiles;
+       j = next_tile<MASK>(tk, band, j, p.n_kv, p))
+    ++n;
+  return n >= kTwinMinTiles;
 }
 
 template <int D, int MASK>
@@ -2013,6 +2165,21 @@ cudaError_t launch_mask(const KernelParams& p, int grid, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = mask_is_causal(MASK) ? 0 : 1;
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+inline int twin_dim(const KernelParams& p, int mask) {
+  switch (mask) {
+    case kMaskNa + 0: return twin_worthwhile<kMaskNa + 0>(p);
+    case kMaskNa + 1: return twin_worthwhile<kMaskNa + 1>(p);
+    case kMaskNa + 2: return twin_worthwhile<kMaskNa + 2>(p);
+    case kMaskNa + 3: return twin_worthwhile<kMaskNa + 3>(p);
+    case kMaskNa + 4: return twin_worthwhile<kMaskNa + 4>(p);
+    case kMaskNa + 5: return twin_worthwhile<kMaskNa + 5>(p);
+    case kMaskNa + 6: return twin_worthwhile<kMaskNa + 6>(p);
+    case kMaskNa + 7: return twin_worthwhile<kMaskNa + 7>(p);
+    case kMaskNa3: return twin_worthwhile<kMaskNa3>(p);
+    default: return 0;
+  }
 }
 
 template <int D>

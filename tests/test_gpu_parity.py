@@ -428,3 +428,50 @@ def test_causal_bottom_right_equals_top_left_when_square(E):
     b = E.attn_fwd(q, k, v, mask="causal_br")
     _status_ok(E)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# Twin tasks: neighbourhood launches with one Q tile per task and K/V chains of
+# 8 tiles or more give both softmax warpgroups the same queries, the K/V tiles
+# in turn, and merge the two halves in the CTA. (B, H, grid, window, dilation,
+# wrap axes, d, CTAs; 0 = one per SM). One Q tile per task needs fewer Q-tile
+# pairs than CTAs; with fewer CTAs than single-tile tasks, some CTAs run two
+# twin tasks in a row (the exchange's phases carry over).
+TWIN = [
+    (1, 2, (40, 40), 39, 1, None, 64, 0),                     # every key in every window
+    (1, 3, (48, 48), 21, 1, (True, False), 32, 40),      # 27 pairs, 54 tasks
+    (2, 1, (32, 32), 9, 2, (False, True), 128, 12),      # 8 pairs, 16 tasks
+    (1, 2, (16, 16, 16), 5, 1, (True, True, False), 32, 0),   # the NATTEN-issue volume
+    (1, 1, (12, 14, 10), (7, 7, 3), 1, (False, True, False), 64, 10),  # 7 pairs
+    (1, 2, (16, 16, 24), 3, 2, (False, False, False), 128, 64),  # 48 pairs
+]
+
+
+@pytest.mark.parametrize("B,H,grid,win,dil,wrap_axes,d,num_ctas", TWIN)
+def test_twin_tasks_match_the_oracle(E, B, H, grid, win, dil, wrap_axes, d, num_ctas):
+    n = math.prod(grid)
+    run(E, B, H, n, n, d, "clamp", window=win, dilation=dil, grid=grid, wrap_axes=wrap_axes,
+        num_ctas=num_ctas, seed=n + d + 17 * dil)
+
+
+def test_twin_decision_in_the_log():
+    """ATTN_LOG's twin flag: on for every case above, off for a 64 x 64 grid
+    with window 7 (5 K/V tiles a Q tile) and for launches with Q-tile pairs."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    calls = [f"E.attn_fwd(*qkv({math.prod(g)}, {d}, {B}, {H}), mask='clamp', window={w!r}, "
+             f"dilation={dl}, grid={g!r}, wrap_axes={wa!r}, num_ctas={nc})"
+             for B, H, g, w, dl, wa, d, nc in TWIN]
+    calls += ["E.attn_fwd(*qkv(4096, 32, 1, 4), mask='clamp', window=7, grid=(64, 64))",
+              "E.attn_fwd(*qkv(4096, 32, 8, 16), mask='clamp', window=7, grid=(64, 64))"]
+    code = ("import torch, exact_attention_69_gb300 as E; from seeded_inputs import make_qkv\n"
+            "def qkv(n, d, B, H): return [t.cuda() for t in make_qkv(B, H, n, n, d, 1.0, 3)]\n"
+            + "\n".join(calls) + "\ntorch.cuda.synchronize()\n")
+    env = dict(os.environ, ATTN_LOG="1", PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=root, timeout=600)
+    assert r.returncode == 0, r.stderr
+    flags = [ln.rsplit("twin=", 1)[1].strip() for ln in r.stderr.splitlines()
+             if ln.startswith("attn_fwd:")]
+    assert flags == ["1"] * len(TWIN) + ["0", "0"], r.stderr
