@@ -870,6 +870,7 @@ template <int MASK>
 struct SegIter {
   int rest;  // units of this CTA not yet handed out (< 2^31: the host splits no larger share)
   int t_rr, kv;
+  int rnd = 0;  // causal: tasks taken so far
   bool first;
   __device__ __forceinline__ SegIter(const KernelParams& p, const int64_t* lo) : first(true) {
     if (MASK == kMaskNone && p.split) {
@@ -894,6 +895,20 @@ struct SegIter {
         kv = 0;
         ++t_rr;
       }
+    } else if constexpr (mask_is_causal(MASK)) {
+      // Causal tasks come longest first; dealt back and forth (CTA c takes
+      // task c of the first round, task G - 1 - c of the second, ...), the
+      // CTAs' total lengths come out nearly equal, where a plain round robin
+      // gives CTA 0 the longest task of every round. A CTA past the last
+      // task in one round is past it in every later one.
+      const int G = static_cast<int>(gridDim.x);
+      const int t = rnd * G + ((rnd & 1) ? G - 1 - static_cast<int>(blockIdx.x)
+                                         : static_cast<int>(blockIdx.x));
+      if (t >= p.n_tasks) return false;
+      ++rnd;
+      s.t = t;
+      s.kv0 = 0;
+      s.kv1 = p.n_kv;
     } else {
       if (t_rr >= p.n_tasks) return false;
       s.t = t_rr;
