@@ -183,3 +183,19 @@ extern "C" void band_host(int t0, int N, int grid_d, int grid_h, int grid_w, int
   out[2] = b.lo1;
   out[3] = b.hi1;
 }
+
+// Whether a launch with one Q tile per task (fewer Q-tile pairs than CTAs)
+// runs its tasks as twins: the decision the host takes at launch. grid_d == 0:
+// a 2-D grid (wrap_bits 1 columns, 2 rows); else a volume (4 depth as well).
+extern "C" int twin_host(int B, int H, int N, int grid_d, int grid_h, int grid_w, int window_d,
+                         int window_h, int window_w, int dilation, int wrap_bits) {
+  attn::KernelParams p =
+      na3_params(N, grid_d, grid_h, grid_w, window_d, window_h, window_w, dilation, wrap_bits);
+  p.B = B;
+  p.H = H;
+  p.q_tiles = 1;
+  p.n_qtasks = (N + attn::kBM - 1) / attn::kBM;
+  p.n_tasks = B * H * p.n_qtasks;
+  const int mask = grid_d == 0 ? na2_mask(wrap_bits & 2, wrap_bits & 1, dilation) : attn::kMaskNa3;
+  return attn::dev::twin_dim(p, mask);
+}

@@ -41,6 +41,8 @@ def plan(tmp_path_factory):
     lib.na3_bits_host.argtypes = [ctypes.c_int] * 11 + [ctypes.POINTER(ctypes.c_uint)]
     lib.na_key_bits_host.argtypes = [ctypes.c_int] * 11 + [ctypes.POINTER(ctypes.c_uint)]
     lib.band_host.argtypes = [ctypes.c_int] * 10 + [ctypes.POINTER(ctypes.c_int)]
+    lib.twin_host.argtypes = [ctypes.c_int] * 11
+    lib.twin_host.restype = ctypes.c_int
     return lib
 
 
@@ -288,3 +290,79 @@ def test_band_holds_every_meeting_tile_both_ways(plan, grid, window, wrap, dilat
         total += len(band)
     # a band is a narrow superset: no more than the meeting tiles plus a margin
     assert total <= meets.sum() + 4 * n_t, (total, int(meets.sum()))
+
+
+# The host's twin decision (both softmax warpgroups on one Q tile, its K/V tiles
+# in turn) for the twin configurations of the GPU tests and the 64 x 64 grid
+# with window 7 of the neighbourhood workloads: twins from 8 active K/V tiles a
+# Q tile on (a task from the middle of head 0), counted with the kernel's own
+# band and tile tests. The GPU tests read the same flags from ATTN_LOG.
+TWIN_DECISIONS = [  # (grid, window, dilation, wrap (per axis), twin)
+    ((40, 40), 39, 1, (False, False), 1),
+    ((48, 48), 21, 1, (True, False), 1),
+    ((32, 32), 9, 2, (False, True), 1),
+    ((16, 16, 16), 5, 1, (True, True, False), 1),
+    ((12, 14, 10), (7, 7, 3), 1, (False, True, False), 1),
+    ((16, 16, 24), 3, 2, (False, False, False), 1),
+    ((64, 64), 7, 1, (False, False), 0),
+    ((64, 64), 7, 1, (True, True), 0),
+]
+
+
+@pytest.mark.parametrize("grid,window,dilation,wrap,twin_on", TWIN_DECISIONS)
+def test_twin_decision(plan, grid, window, dilation, wrap, twin_on):
+    N = int(np.prod(grid))
+    win = window if isinstance(window, tuple) else (window,) * len(grid)
+    if len(grid) == 3:
+        g3, w3, bits = grid, win, _wrap_bits(wrap)
+    else:
+        g3, w3 = (0,) + tuple(grid), (1,) + tuple(win)
+        bits = (1 if wrap[1] else 0) | (2 if wrap[0] else 0)
+    assert plan.twin_host(1, 2, N, *g3, *w3, dilation, bits) == twin_on
+    # the count is of one task's tiles: the decision does not depend on B or H
+    assert plan.twin_host(3, 5, N, *g3, *w3, dilation, bits) == twin_on
+
+
+def _dealt(rnd, cta, G):
+    """Causal tasks dealt back and forth: the task of a CTA's round `rnd`."""
+    return rnd * G + (G - 1 - cta if rnd & 1 else cta)
+
+
+@pytest.mark.parametrize("n_tasks,G", [(512, 152), (1, 152), (151, 152), (152, 152), (153, 152),
+                                       (305, 152), (1000, 7), (6, 1), (77, 3)])
+def test_causal_tasks_dealt_back_and_forth_cover_every_task_once(n_tasks, G):
+    """Each CTA takes its round-r task until the first one past n_tasks (the
+    kernel stops there): every task is taken once, by one CTA."""
+    seen = []
+    for c in range(G):
+        r = 0
+        while _dealt(r, c, G) < n_tasks:
+            seen.append(_dealt(r, c, G))
+            r += 1
+        # once past the end, every later round is too
+        assert all(_dealt(rr, c, G) >= n_tasks for rr in range(r, r + 4))
+    assert sorted(seen) == list(range(n_tasks))
+
+
+def test_causal_deal_evens_out_the_lm_shape(plan):
+    """B4 H16 N2048 causal over 152 CTAs: a task (a pair of Q tiles) takes as
+    many K/V tile steps as its second tile sees; longest first. Dealt back and
+    forth, no CTA holds more than 32 steps against 38 for a round robin (the
+    mean is 30.3)."""
+    B, H, N, G = 4, 16, 2048, 152
+    n_tasks = B * H * (N // 256)
+    out = (ctypes.c_int * 4)()
+    steps = []
+    for t in range(n_tasks):
+        plan.decode_task_host(1, t, B, H, N, 2, out)
+        steps.append((out[2] + 256) // 128)  # K/V tiles of the pair's second Q tile
+    assert steps == sorted(steps, reverse=True)
+    load_rr = [sum(steps[t] for t in range(c, n_tasks, G)) for c in range(G)]
+    load_snake = [0] * G
+    for c in range(G):
+        r = 0
+        while _dealt(r, c, G) < n_tasks:
+            load_snake[c] += steps[_dealt(r, c, G)]
+            r += 1
+    assert max(load_rr) == 38 and max(load_snake) == 32
+    assert sum(load_snake) == sum(load_rr) == sum(steps)
